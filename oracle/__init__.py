@@ -1,0 +1,214 @@
+"""FP64 CPU oracle for single-token paged-KV GQA decode attention.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers; the product path never
+imports this package, and this package imports nothing from it.
+
+* ``decode``       -- the definition (plain two-pass softmax over the paged
+                      layout) for every (s, h) row or for a list of rows; the C
+                      source ``paged_attn_oracle.c`` states it in full.
+* ``pieces``       -- the per-range softmax pieces (M, l, o) of rows.
+* ``combine`` / ``finish`` -- the merge of two partial softmax states and the
+                      final normalisation, as "Paged Attention Kernel
+                      Architecture for BI-V100" (section 2, Level 1: the
+                      ``attention_partial`` compound value and its binary
+                      ``combine``) defines them, with an empty state (M = -inf)
+                      contributing weight zero.
+
+Pins (tests/test_oracle_pins.py) tie the oracle to a library routine
+(torch's float64 scaled_dot_product_attention on the un-paged layout), closed
+forms, invariances and a hand-derived golden example.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "paged_attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {
+    0: "ok",
+    -1: "invalid arguments",
+    -2: "H_q is not a multiple of H_kv",
+    -3: "a sequence length is negative or longer than max_blocks_per_seq * block_size",
+    -4: "a block-table entry in use is outside [0, num_blocks)",
+    -5: "out of host memory",
+}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (-O2, OpenMP, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            lib = ctypes.CDLL(path)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            LL = ctypes.c_longlong
+            F = ctypes.c_float
+            lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F, P, I]
+            lib.oracle_decode.restype = I
+            lib.oracle_decode_pairs.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F, P, I, P, I]
+            lib.oracle_decode_pairs.restype = I
+            lib.oracle_partial_pairs.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F, P, P, I,
+                                                 P, P, P]
+            lib.oracle_partial_pairs.restype = I
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 data as a contiguous uint16 array (torch tensor or uint16 ndarray)."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("numpy inputs must hold bf16 bit patterns as uint16")
+        return np.ascontiguousarray(x)
+    import torch  # only for converting tensors handed in by the tests
+
+    t = x.detach()
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected a bf16 tensor")
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _i32(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.int32)
+    return np.ascontiguousarray(x.detach().cpu().numpy(), dtype=np.int32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Inputs:
+    """Host views of one decode problem in the layout the oracle reads."""
+
+    def __init__(self, q, k_cache, v_cache, block_tables, seq_lens, scale: float):
+        self.q = _bits(q)
+        self.k = _bits(k_cache)
+        self.v = _bits(v_cache)
+        self.bt = _i32(block_tables)
+        self.lens = _i32(seq_lens)
+        if self.q.ndim != 3 or self.k.ndim != 4 or self.k.shape != self.v.shape:
+            raise ValueError("q must be [S,H_q,D] and the caches [NB,H_kv,BS,D]")
+        self.num_seqs, self.H_q, self.D = self.q.shape
+        self.num_blocks, self.H_kv, self.BS, Dk = self.k.shape
+        if Dk != self.D:
+            raise ValueError("head_dim of q and of the caches differ")
+        if self.bt.ndim != 2 or self.bt.shape[0] != self.num_seqs:
+            raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+        if self.lens.shape != (self.num_seqs,):
+            raise ValueError("seq_lens must be [num_seqs]")
+        self.maxb = self.bt.shape[1]
+        self.scale = float(np.float32(scale))
+
+    @classmethod
+    def from_workload(cls, w) -> "Inputs":
+        return cls(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+
+    def _common(self):
+        return (_ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.bt), _ptr(self.lens),
+                self.num_seqs, self.H_q, self.H_kv, self.D, self.maxb, self.BS,
+                self.num_blocks, self.scale)
+
+
+def _as_inputs(x) -> Inputs:
+    return x if isinstance(x, Inputs) else Inputs.from_workload(x)
+
+
+def decode(x, pairs: Optional[Sequence[Sequence[int]]] = None, num_threads: int = 0) -> np.ndarray:
+    """The definition in float64.
+
+    ``x`` is a ``workloads.Workload`` or ``Inputs``.  Without ``pairs`` the
+    result is ``[num_seqs, H_q, D]``; with ``pairs`` (a list of (s, h)) it is
+    ``[len(pairs), D]``.
+    """
+    inp = _as_inputs(x)
+    lib = _load()
+    if pairs is None:
+        out = np.zeros((inp.num_seqs, inp.H_q, inp.D), dtype=np.float64)
+        rc = lib.oracle_decode(*inp._common(), _ptr(out), int(num_threads))
+    else:
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((pr.shape[0], inp.D), dtype=np.float64)
+        rc = lib.oracle_decode_pairs(*inp._common(), _ptr(pr), pr.shape[0], _ptr(out),
+                                     int(num_threads))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return out
+
+
+def pieces(x, pairs, ranges):
+    """Softmax pieces (M, l, o) of rows (s, h) over token ranges [t0, t1)."""
+    inp = _as_inputs(x)
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    rg = np.ascontiguousarray(np.asarray(ranges, dtype=np.int32).reshape(-1, 2))
+    if pr.shape != rg.shape:
+        raise ValueError("one range per pair")
+    n = pr.shape[0]
+    M = np.zeros(n, dtype=np.float64)
+    l = np.zeros(n, dtype=np.float64)
+    o = np.zeros((n, inp.D), dtype=np.float64)
+    rc = _load().oracle_partial_pairs(*inp._common(), _ptr(pr), _ptr(rg), n, _ptr(M), _ptr(l),
+                                      _ptr(o))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return M, l, o
+
+
+def combine(a, b):
+    """Merge two partial states (M, l, o): the binary op of the split-KV design.
+
+    new_M = max(M_a, M_b); each side is weighted by exp(M_side - new_M); a side
+    whose M is -inf (an empty range) gets weight zero.
+    """
+    Ma, la, oa = a
+    Mb, lb, ob = b
+    M = max(Ma, Mb)
+    if M == -np.inf:
+        return (M, 0.0, np.zeros_like(oa))
+    wa = 0.0 if Ma == -np.inf else float(np.exp(Ma - M))
+    wb = 0.0 if Mb == -np.inf else float(np.exp(Mb - M))
+    return (M, wa * la + wb * lb, wa * oa + wb * ob)
+
+
+def finish(state) -> np.ndarray:
+    """Normalise a merged state: o / l (zeros for an empty state)."""
+    M, l, o = state
+    if l == 0.0:
+        return np.zeros_like(o)
+    return o / l

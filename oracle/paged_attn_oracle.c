@@ -1,0 +1,239 @@
+/*
+ * FP64 CPU oracle for single-token paged-KV GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header or constant with the CUDA path.
+ *
+ * What it computes (the definition, written out; not an algorithm):
+ *
+ *   "Paged Attention Kernel Architecture for BI-V100", section 1 (Problem
+ *   Definition): for one decode query, output[h, d] = softmax(Q[h] . K[t]^T
+ *   scaled) . V[t], with K and V stored in pages reached through a block table.
+ *
+ *   The paging layout, the per-sequence length and the GQA head map are the
+ *   ones of the "Add Cuda Kernel" tutorial (RL.cu), include/kernels/
+ *   attention.cuh, "Paged Attention - Decode" and the kernel body that walks
+ *   the block table in src/kernels/attention.cu:
+ *     q            [num_seqs, H_q, D]
+ *     k/v cache    [num_blocks, H_kv, block_size, D]
+ *     block_tables [num_seqs, max_blocks_per_seq]   logical page -> physical block
+ *     seq_lens     [num_seqs]                      tokens t < seq_lens[s] are attended
+ *     kv head      g = h * H_kv / H_q              (integer division)
+ *   and the caller supplies the softmax scale.
+ *
+ *   For each (s, h):
+ *     K_t = k_cache[bt[s, t / BS], g, t % BS, :]      t in [0, L)
+ *     z_t = scale * sum_d q[s,h,d] * K_t[d]
+ *     M   = max_t z_t
+ *     w_t = exp(z_t - M)
+ *     out[s,h,:] = (sum_t w_t V_t) / (sum_t w_t)
+ *
+ *   Every bf16 input is widened exactly to double; all arithmetic is double;
+ *   scale is the float the caller passes, widened to double.  L = 0 gives a
+ *   zero row (the pages never define an empty softmax; this is the reading
+ *   the library documents).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARGS -1
+#define ORACLE_ERR_HEADS -2
+#define ORACLE_ERR_LEN -3
+#define ORACLE_ERR_BLOCK -4
+#define ORACLE_ERR_NOMEM -5
+
+static double widen_bf16(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Validate the sequence lengths and every block-table entry a sequence uses. */
+static int check_inputs(const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q,
+                        int H_kv, int D, int max_blocks, int BS, long long num_blocks) {
+    if (num_seqs < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || max_blocks <= 0 || BS <= 0)
+        return ORACLE_ERR_ARGS;
+    if (H_q % H_kv != 0) return ORACLE_ERR_HEADS;
+    for (int s = 0; s < num_seqs; ++s) {
+        const long long L = seq_lens[s];
+        if (L < 0 || L > (long long)max_blocks * BS) return ORACLE_ERR_LEN;
+        const long long pages = (L + BS - 1) / BS;
+        for (long long p = 0; p < pages; ++p) {
+            const long long b = bt[(size_t)s * max_blocks + p];
+            if (b < 0 || b >= num_blocks) return ORACLE_ERR_BLOCK;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Softmax pieces of one (s, h) row over the token range [t0, t1):
+ *   M = max_t z_t,  l = sum_t exp(z_t - M),  o[d] = sum_t exp(z_t - M) V_t[d].
+ * An empty range gives M = -inf, l = 0, o = 0.  z is scratch of >= t1 - t0 doubles.
+ */
+static void row_pieces(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                       const int32_t* bt, int s, int h, int H_q, int H_kv, int D, int max_blocks,
+                       int BS, double scale, int t0, int t1, double* z, double* M_out,
+                       double* l_out, double* o) {
+    const int g = (int)(((long long)h * H_kv) / H_q);
+    const uint16_t* qrow = q + ((size_t)s * H_q + h) * D;
+
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    *l_out = 0.0;
+    *M_out = -INFINITY;
+    if (t1 <= t0) return;
+
+    /* z_t = scale * q . K_t, K_t reached through the block table */
+    for (int t = t0; t < t1; ++t) {
+        const size_t pb = (size_t)bt[(size_t)s * max_blocks + t / BS];
+        const uint16_t* krow = k_cache + ((pb * H_kv + g) * BS + (size_t)(t % BS)) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += widen_bf16(qrow[d]) * widen_bf16(krow[d]);
+        z[t - t0] = scale * dot;
+    }
+
+    double M = z[0];
+    for (int t = t0 + 1; t < t1; ++t)
+        if (z[t - t0] > M) M = z[t - t0];
+    double l = 0.0;
+    for (int t = t0; t < t1; ++t) {
+        const double w = exp(z[t - t0] - M);
+        l += w;
+        const size_t pb = (size_t)bt[(size_t)s * max_blocks + t / BS];
+        const uint16_t* vrow = v_cache + ((pb * H_kv + g) * BS + (size_t)(t % BS)) * D;
+        for (int d = 0; d < D; ++d) o[d] += w * widen_bf16(vrow[d]);
+    }
+    *M_out = M;
+    *l_out = l;
+}
+
+/* One (s, h) row of the definition: out = o / l over the whole sequence. */
+static void attend_row(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                       const int32_t* bt, const int32_t* seq_lens, int s, int h, int H_q,
+                       int H_kv, int D, int max_blocks, int BS, double scale, double* z,
+                       double* out_row) {
+    double M, l;
+    row_pieces(q, k_cache, v_cache, bt, s, h, H_q, H_kv, D, max_blocks, BS, scale, 0,
+               seq_lens[s], z, &M, &l, out_row);
+    if (l > 0.0)
+        for (int d = 0; d < D; ++d) out_row[d] /= l;
+}
+
+/*
+ * Rows listed in `pairs` ([num_pairs][2] = (s, h)); out is [num_pairs, D].
+ * num_threads <= 0 uses the OpenMP default.  Returns 0 or a negative code.
+ */
+int oracle_decode_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                        int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                        long long num_blocks, float scale, const int32_t* pairs, int num_pairs,
+                        double* out, int num_threads) {
+    int rc = check_inputs(block_tables, seq_lens, num_seqs, H_q, H_kv, D, max_blocks_per_seq,
+                          block_size, num_blocks);
+    if (rc != ORACLE_OK) return rc;
+    for (int i = 0; i < num_pairs; ++i) {
+        if (pairs[2 * i] < 0 || pairs[2 * i] >= num_seqs || pairs[2 * i + 1] < 0 ||
+            pairs[2 * i + 1] >= H_q)
+            return ORACLE_ERR_ARGS;
+    }
+    int Lmax = 1;
+    for (int s = 0; s < num_seqs; ++s)
+        if (seq_lens[s] > Lmax) Lmax = seq_lens[s];
+    const double sc = (double)scale;
+    int failed = 0;
+
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(num_threads)
+#endif
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
+        /* every thread reaches the work-sharing loop; one without scratch skips its rows */
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int i = 0; i < num_pairs; ++i) {
+            if (!z) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                failed = 1;
+                continue;
+            }
+            attend_row(q, k_cache, v_cache, block_tables, seq_lens, pairs[2 * i],
+                       pairs[2 * i + 1], H_q, H_kv, D, max_blocks_per_seq, block_size, sc, z,
+                       out + (size_t)i * D);
+        }
+        free(z);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Every row: out is [num_seqs, H_q, D]. */
+int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                  const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int H_q,
+                  int H_kv, int D, int max_blocks_per_seq, int block_size, long long num_blocks,
+                  float scale, double* out, int num_threads) {
+    if (num_seqs < 0 || H_q <= 0) return ORACLE_ERR_ARGS;
+    const size_t n = (size_t)num_seqs * H_q;
+    int32_t* pairs = (int32_t*)malloc(sizeof(int32_t) * 2 * (n ? n : 1));
+    if (!pairs) return ORACLE_ERR_NOMEM;
+    for (size_t i = 0; i < n; ++i) {
+        pairs[2 * i] = (int32_t)(i / H_q);
+        pairs[2 * i + 1] = (int32_t)(i % H_q);
+    }
+    int rc = oracle_decode_pairs(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                                 D, max_blocks_per_seq, block_size, num_blocks, scale, pairs,
+                                 (int)n, out, num_threads);
+    free(pairs);
+    return rc;
+}
+
+/* Threads the OpenMP runtime would use by default (0 when built without it). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 0;
+#endif
+}
+
+/*
+ * Softmax pieces (M, l, o) of rows (s, h) over token ranges: ranges is
+ * [num_pairs][2] = (t0, t1) with 0 <= t0 <= t1 <= seq_lens[s].  These are the
+ * per-partition states that the split-KV design of "Paged Attention Kernel
+ * Architecture for BI-V100" (section 2, Level 1 and Level 3) merges.
+ */
+int oracle_partial_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                         int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                         long long num_blocks, float scale, const int32_t* pairs,
+                         const int32_t* ranges, int num_pairs, double* M, double* l, double* o) {
+    int rc = check_inputs(block_tables, seq_lens, num_seqs, H_q, H_kv, D, max_blocks_per_seq,
+                          block_size, num_blocks);
+    if (rc != ORACLE_OK) return rc;
+    int Lmax = 1;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int s = pairs[2 * i], h = pairs[2 * i + 1];
+        const int t0 = ranges[2 * i], t1 = ranges[2 * i + 1];
+        if (s < 0 || s >= num_seqs || h < 0 || h >= H_q) return ORACLE_ERR_ARGS;
+        if (t0 < 0 || t1 < t0 || t1 > seq_lens[s]) return ORACLE_ERR_ARGS;
+        if (t1 - t0 > Lmax) Lmax = t1 - t0;
+    }
+    double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
+    if (!z) return ORACLE_ERR_NOMEM;
+    for (int i = 0; i < num_pairs; ++i)
+        row_pieces(q, k_cache, v_cache, block_tables, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv,
+                   D, max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],
+                   ranges[2 * i + 1], z, M + i, l + i, o + (size_t)i * D);
+    free(z);
+    return ORACLE_OK;
+}

@@ -1,0 +1,359 @@
+"""Pins for the FP64 oracle: each test ties it to something other than itself.
+
+* a library routine: torch's float64 scaled_dot_product_attention on the
+  contiguous (un-paged) K/V that the test pages itself;
+* closed forms: one token, constant V rows, zero query / zero scale, and a
+  hand-worked example stored under tests/golden/;
+* invariances: relabelling physical blocks, duplicating KV heads, NaN in every
+  row the definition never reads, scores large enough that exp overflows
+  without the max shift;
+* the split/merge algebra of the split-KV design: merging the pieces of any
+  partition of [0, L) equals the whole-sequence result.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(x: torch.Tensor) -> torch.Tensor:
+    return x.to(torch.bfloat16)
+
+
+def _page(K, V, BS, gen_np, extra_blocks=1, fill=float("nan")):
+    """Scatter contiguous per-sequence K/V ([L_s, H_kv, D] each) into a shuffled pool.
+
+    Returns (k_cache, v_cache, block_tables, seq_lens); unused rows hold ``fill``.
+    """
+    H_kv, D = K[0].shape[1], K[0].shape[2]
+    lens = [k.shape[0] for k in K]
+    pages = [-(-L // BS) for L in lens]
+    maxb = max(1, max(pages))
+    nb = sum(pages) + extra_blocks
+    perm = gen_np.permutation(nb)
+    kc = torch.full((nb, H_kv, BS, D), fill, dtype=torch.bfloat16)
+    vc = torch.full((nb, H_kv, BS, D), fill, dtype=torch.bfloat16)
+    bt = np.full((len(K), maxb), perm[-1], dtype=np.int32)
+    pos = 0
+    for s, L in enumerate(lens):
+        for p in range(pages[s]):
+            b = int(perm[pos])
+            pos += 1
+            bt[s, p] = b
+            t0, t1 = p * BS, min(L, (p + 1) * BS)
+            # cache row order is [block, head, slot, dim]; contiguous is [token, head, dim]
+            kc[b, :, : t1 - t0, :] = K[s][t0:t1].transpose(0, 1)
+            vc[b, :, : t1 - t0, :] = V[s][t0:t1].transpose(0, 1)
+    return kc, vc, torch.from_numpy(bt), torch.tensor(lens, dtype=torch.int32)
+
+
+def _sdpa(q, K, V, scale):
+    """torch float64 SDPA per sequence on contiguous K/V, GQA by repeating KV heads."""
+    outs = []
+    H_q = q.shape[1]
+    for s in range(q.shape[0]):
+        k = K[s].double().transpose(0, 1)  # [H_kv, L, D]
+        v = V[s].double().transpose(0, 1)
+        G = H_q // k.shape[0]
+        k = k.repeat_interleave(G, dim=0)[None]
+        v = v.repeat_interleave(G, dim=0)[None]
+        qq = q[s].double()[None, :, None, :]  # [1, H_q, 1, D]
+        outs.append(F.scaled_dot_product_attention(qq, k, v, scale=scale)[0, :, 0, :])
+    return torch.stack(outs).numpy()
+
+
+def _random_problem(seed, lens, H_q, H_kv, D, BS, kv_std=1.0, extra_blocks=1):
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    q = _bf16(torch.randn(len(lens), H_q, D, generator=g))
+    K = [_bf16(torch.randn(L, H_kv, D, generator=g) * kv_std) for L in lens]
+    V = [_bf16(torch.randn(L, H_kv, D, generator=g) * kv_std) for L in lens]
+    kc, vc, bt, sl = _page(K, V, BS, rng, extra_blocks=extra_blocks)
+    return q, K, V, kc, vc, bt, sl
+
+
+CASES = [
+    # seed, lens, H_q, H_kv, D, BS
+    (1, [37, 100], 4, 2, 64, 16),
+    (2, [1, 16, 17, 33], 8, 8, 32, 16),     # G = 1 (plain multi-head)
+    (3, [5, 64, 129], 6, 1, 128, 32),        # G = 6
+    (4, [31, 2, 48], 16, 2, 16, 8),          # G = 8
+    (5, [200], 3, 1, 8, 4),                  # odd sizes the definition allows
+]
+
+
+@pytest.mark.parametrize("seed,lens,H_q,H_kv,D,BS", CASES)
+def test_matches_torch_sdpa_on_unpaged_kv(seed, lens, H_q, H_kv, D, BS):
+    q, K, V, kc, vc, bt, sl = _random_problem(seed, lens, H_q, H_kv, D, BS)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, scale))
+    ref = _sdpa(q, K, V, scale)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_golden_worked_example():
+    with open(os.path.join(GOLDEN, "paged_decode_worked_example.json")) as f:
+        ex = json.load(f)
+    nb, H_kv, BS, D = ex["num_blocks"], ex["H_kv"], ex["block_size"], ex["D"]
+    kc = torch.full((nb, H_kv, BS, D), float("nan"), dtype=torch.bfloat16)
+    vc = kc.clone()
+    for r in ex["k_rows"]:
+        kc[r["block"], r["head"], r["slot"]] = torch.tensor(r["values"], dtype=torch.bfloat16)
+    for r in ex["v_rows"]:
+        vc[r["block"], r["head"], r["slot"]] = torch.tensor(r["values"], dtype=torch.bfloat16)
+    q = torch.tensor(ex["q"], dtype=torch.bfloat16)
+    bt = torch.tensor(ex["block_tables"], dtype=torch.int32)
+    sl = torch.tensor(ex["seq_lens"], dtype=torch.int32)
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, ex["scale"]))
+
+    def value(expr):
+        # the fixture's closed forms use numbers, e, + - * / and parentheses only
+        if not set(expr) <= set("0123456789.e+-*/() "):
+            raise ValueError(expr)
+        return float(eval(expr, {"__builtins__": {}}, {"e": math.e}))
+
+    for row in ex["expected"]:
+        want = np.array([value(v) for v in row["values"]])
+        np.testing.assert_allclose(got[row["s"], row["h"]], want, rtol=0,
+                                   atol=ex["abs_tolerance"])
+
+
+def test_single_token_returns_its_v_row():
+    q, K, V, kc, vc, bt, sl = _random_problem(11, [1, 1, 1], 4, 2, 64, 16)
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, 0.125))
+    for s in range(3):
+        for h in range(4):
+            want = V[s][0, h // 2].double().numpy()
+            assert np.array_equal(got[s, h], want)
+
+
+def test_constant_v_rows_return_the_constant():
+    lens = [3, 50, 97]
+    q, K, V, kc, vc, bt, sl = _random_problem(12, lens, 4, 2, 32, 16)
+    c = _bf16(torch.randn(2, 32, generator=torch.Generator().manual_seed(5)))
+    V = [c[None].expand(L, 2, 32).clone() for L in lens]
+    kc2, vc2, bt2, sl2 = _page(K, V, 16, np.random.default_rng(12))
+    got = oracle.decode(oracle.Inputs(q, kc2, vc2, bt2, sl2, 0.3))
+    for s in range(3):
+        for h in range(4):
+            np.testing.assert_allclose(got[s, h], c[h // 2].double().numpy(), rtol=1e-15,
+                                       atol=1e-15)
+
+
+@pytest.mark.parametrize("zero", ["query", "scale"])
+def test_uniform_weights_give_the_mean_of_v(zero):
+    lens = [7, 40, 129]
+    q, K, V, kc, vc, bt, sl = _random_problem(13, lens, 6, 3, 64, 16)
+    scale = 0.125
+    if zero == "query":
+        q = torch.zeros_like(q)
+    else:
+        scale = 0.0
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, scale))
+    for s, L in enumerate(lens):
+        mean = V[s].double().mean(dim=0).numpy()  # [H_kv, D]
+        for h in range(6):
+            np.testing.assert_allclose(got[s, h], mean[h // 2], rtol=0, atol=1e-14)
+
+
+def test_block_relabelling_is_invisible():
+    w = workloads.make("tiny", poison="nan")
+    base = oracle.decode(w)
+    rng = np.random.default_rng(99)
+    pi = rng.permutation(w.num_blocks)               # old id -> new id
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[torch.from_numpy(pi)] = w.k_cache
+    v2[torch.from_numpy(pi)] = w.v_cache
+    bt2 = torch.from_numpy(pi[w.block_tables.numpy()].astype(np.int32))
+    got = oracle.decode(oracle.Inputs(w.q, k2, v2, bt2, w.seq_lens, w.scale))
+    assert np.array_equal(got, base)
+
+
+def test_duplicated_kv_heads_give_the_same_rows():
+    w = workloads.make("tiny", poison="nan")
+    G = w.spec.G
+    base = oracle.decode(w)
+    # one KV head per query head, holding the KV head that query head maps to
+    k2 = w.k_cache.repeat_interleave(G, dim=1)
+    v2 = w.v_cache.repeat_interleave(G, dim=1)
+    got = oracle.decode(oracle.Inputs(w.q, k2, v2, w.block_tables, w.seq_lens, w.scale))
+    assert np.array_equal(got, base)
+
+
+def test_unread_rows_never_matter():
+    clean = workloads.make("tiny", poison="none")
+    poisoned = workloads.make("tiny", poison="nan")
+    a = oracle.decode(clean)
+    b = oracle.decode(poisoned)
+    assert np.isfinite(b).all()
+    assert np.array_equal(a, b)
+
+
+def test_large_scores_stay_finite_and_exact():
+    # scores near 1e3 overflow exp() unless the row max is subtracted first
+    q, K, V, kc, vc, bt, sl = _random_problem(14, [20, 70], 2, 1, 64, 16, kv_std=16.0)
+    q = q * 16
+    scale = 1.0
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, scale))
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, _sdpa(q, K, V, scale), rtol=0, atol=1e-12)
+
+
+def _random_partition(rng, L, parts):
+    cuts = np.sort(rng.integers(0, L + 1, size=parts - 1))
+    edges = [0] + [int(c) for c in cuts] + [L]
+    return list(zip(edges[:-1], edges[1:]))  # may contain empty and singleton ranges
+
+
+@pytest.mark.parametrize("parts", [1, 2, 5, 17])
+def test_merging_partition_pieces_equals_whole(parts):
+    w = workloads.make("tiny", poison="nan")
+    inp = oracle.Inputs.from_workload(w)
+    whole = oracle.decode(inp)
+    rng = np.random.default_rng(parts)
+    for s, L in enumerate(w.lens_list):
+        for h in range(w.spec.H_q):
+            rngs = _random_partition(rng, L, parts)
+            M, l, o = oracle.pieces(inp, [(s, h)] * len(rngs), rngs)
+            order = rng.permutation(len(rngs))  # the merge is order-free
+            state = (-np.inf, 0.0, np.zeros(w.spec.D))
+            for i in order:
+                state = oracle.combine(state, (M[i], l[i], o[i]))
+            np.testing.assert_allclose(oracle.finish(state), whole[s, h], rtol=1e-13, atol=1e-15)
+
+
+def test_combine_is_associative_and_commutative():
+    rng = np.random.default_rng(3)
+    st = [(float(rng.normal() * 5), float(rng.uniform(0.5, 9)), rng.normal(size=8))
+          for _ in range(3)]
+    a, b, c = st
+    ab_c = oracle.combine(oracle.combine(a, b), c)
+    a_bc = oracle.combine(a, oracle.combine(b, c))
+    assert ab_c[0] == a_bc[0]
+    np.testing.assert_allclose(ab_c[1], a_bc[1], rtol=1e-14)
+    np.testing.assert_allclose(ab_c[2], a_bc[2], rtol=1e-14)
+    ba = oracle.combine(b, a)
+    ab = oracle.combine(a, b)
+    assert ab[0] == ba[0] and ab[1] == ba[1] and np.array_equal(ab[2], ba[2])
+    empty = (-np.inf, 0.0, np.zeros(8))
+    e_a = oracle.combine(empty, a)
+    assert e_a[0] == a[0] and e_a[1] == a[1] and np.array_equal(e_a[2], a[2])
+
+
+def test_empty_sequence_gives_zero_row():
+    # the pages do not define an empty softmax; the documented reading is a zero row
+    q, K, V, kc, vc, bt, sl = _random_problem(15, [0, 9], 2, 1, 16, 8)
+    got = oracle.decode(oracle.Inputs(q, kc, vc, bt, sl, 0.25))
+    assert np.array_equal(got[0], np.zeros((2, 16)))
+    assert np.isfinite(got[1]).all()
+
+
+def test_rows_subset_matches_full():
+    w = workloads.make("tiny", poison="nan")
+    full = oracle.decode(w)
+    pairs = [(1, 3), (0, 0), (1, 0)]
+    sub = oracle.decode(w, pairs=pairs)
+    for i, (s, h) in enumerate(pairs):
+        assert np.array_equal(sub[i], full[s, h])
+
+
+def test_bad_inputs_are_rejected():
+    w = workloads.make("tiny", poison="nan")
+    inp = oracle.Inputs.from_workload(w)
+    bad_bt = w.block_tables.clone()
+    bad_bt[0, 0] = w.num_blocks
+    with pytest.raises(oracle.OracleError):
+        oracle.decode(oracle.Inputs(w.q, w.k_cache, w.v_cache, bad_bt, w.seq_lens, w.scale))
+    long = w.seq_lens.clone()
+    long[0] = inp.maxb * inp.BS + 1
+    with pytest.raises(oracle.OracleError):
+        oracle.decode(oracle.Inputs(w.q, w.k_cache, w.v_cache, w.block_tables, long, w.scale))
+    q3 = torch.zeros(2, 3, 64, dtype=torch.bfloat16)
+    with pytest.raises(oracle.OracleError):
+        oracle.decode(oracle.Inputs(q3, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, 0.1))
+
+
+MUTANTS = [
+    ("kv head h % H_kv", "(int)(((long long)h * H_kv) / H_q)", "(h % H_kv)"),
+    ("scale dropped", "z[t - t0] = scale * dot;", "z[t - t0] = dot;"),
+    ("page index from t % BS", "bt[(size_t)s * max_blocks + t / BS]", "bt[(size_t)s * max_blocks + t % BS]"),
+    ("slot index from t / BS", "+ (size_t)(t % BS)) * D;", "+ (size_t)(t / BS)) * D;"),
+    ("max not subtracted", "exp(z[t - t0] - M)", "exp(z[t - t0])"),
+    ("softmax sign flipped", "exp(z[t - t0] - M)", "exp(M - z[t - t0])"),
+    ("last token dropped", "for (int t = t0; t < t1; ++t) {\n        const double w",
+     "for (int t = t0; t < t1 - 1; ++t) {\n        const double w"),
+    ("no normalisation", "out_row[d] /= l;", "out_row[d] /= 1.0;"),
+    ("K row reversed", "widen_bf16(qrow[d]) * widen_bf16(krow[d])",
+     "widen_bf16(qrow[d]) * widen_bf16(krow[D - 1 - d])"),
+    ("query head from kv head", "qrow = q + ((size_t)s * H_q + h) * D",
+     "qrow = q + ((size_t)s * H_q + g) * D"),
+]
+
+
+def _pins_pass() -> bool:
+    """The cheap pins, run against whatever library oracle._lib holds."""
+    try:
+        test_matches_torch_sdpa_on_unpaged_kv(*CASES[0])
+        test_matches_torch_sdpa_on_unpaged_kv(*CASES[3])
+        test_golden_worked_example()
+        test_single_token_returns_its_v_row()
+        test_unread_rows_never_matter()
+        test_large_scores_stay_finite_and_exact()
+        test_merging_partition_pieces_equals_whole(5)
+    except (AssertionError, oracle.OracleError, FloatingPointError):
+        return False
+    return True
+
+
+_MUTANT_RUNNER = """
+import ctypes, sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np
+import oracle
+import test_oracle_pins as T
+good = oracle._load()
+lib = ctypes.CDLL({so!r})
+for fn in ("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs"):
+    getattr(lib, fn).argtypes = getattr(good, fn).argtypes
+    getattr(lib, fn).restype = getattr(good, fn).restype
+oracle._lib = lib
+with np.errstate(all="ignore"):
+    print("PINS_PASS" if T._pins_pass() else "PINS_FAIL")
+"""
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistakes(name, old, new, tmp_path):
+    """Plant a plausible mistake in a copy of the oracle's C source, build it, and check
+    that at least one pin fails against the mutant (run in a child process, since a
+    mutant may also read out of bounds and crash, which counts as caught)."""
+    import subprocess
+    import sys
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, name
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _MUTANT_RUNNER.format(root=os.path.dirname(here), tests=here, so=str(so))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    crashed = r.returncode < 0  # killed by a signal: the mutant read out of bounds
+    assert crashed or "PINS_FAIL" in r.stdout, \
+        f"no pin noticed the planted mistake: {name}\n{r.stdout}\n{r.stderr[-2000:]}"
+
+
+def test_unmutated_oracle_passes_the_same_pins():
+    assert _pins_pass()
