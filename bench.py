@@ -1,0 +1,474 @@
+"""Benchmark: paged GQA decode attention on GB300.
+
+One step = one decode-attention call over the whole batch of the workload
+(every (sequence, query head) row), inputs resident in HBM.  Prints ONE JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Default workload: the LLaMA-3-8B-shaped decode batch (32 sequences, H_q 32,
+H_kv 8, head_dim 128, block 16, lengths U[512, 4096], shuffled blocks).
+Throughput counts algorithmic bytes: the K and V rows of every attended token
+once per KV head, plus q, out and the block-table entries in use.  L2: the
+timed calls rotate over replicas of the KV cache whose total size is several
+times the 129 MB L2, so every call streams from HBM.
+
+--impl reference times the FP64 CPU oracle (the reference arm of this
+project) on the host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attn µs/step and KV GB/s (% of GB300 HBM peak), 1 GPU"
+L2_BYTES = 129 * 10**6
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ byte accounting
+
+def algorithmic_bytes(spec, lens) -> dict:
+    """K+V rows once per KV head, q read, out written, block-table entries in use."""
+    D, BS, H_kv, H_q = spec.D, spec.block_size, spec.H_kv, spec.H_q
+    kv = sum(int(L) for L in lens) * H_kv * 4 * D
+    qo = len(lens) * H_q * D * 2 * 2
+    bt = sum(-(-int(L) // BS) for L in lens) * 4
+    return {"kv": kv, "q_out": qo, "block_table": bt, "total": kv + qo + bt}
+
+
+def group_bytes(spec, L: int) -> int:
+    """Algorithmic bytes of one (sequence, KV head) group of G query rows."""
+    return L * 4 * spec.D + spec.G * spec.D * 4 + (-(-L // spec.block_size)) * 4 // spec.H_kv
+
+
+# ------------------------------------------------------------------ environment
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(config_name: str):
+    """DRAM bytes per launch recorded by ncu for this workload, if the kernel
+    sources are unchanged since the capture (else None)."""
+    from paged_kv_gqa_decode_gb300 import build as pbuild
+
+    path = os.path.join(ROOT, "profiles", f"decode_{config_name}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != pbuild.source_digest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device: int):
+        self.samples = []  # (monotonic time, fields)
+        self.proc = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["--id=" + (uuid if uuid.startswith("GPU-") else "GPU-" + uuid)]
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = vis.split(",")[device] if vis else str(device)
+            sel = ["--id=" + idx]
+        cmd = ["nvidia-smi", *sel, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [s for _, s in self.samples]
+            window = "whole run (timed region shorter than 3 samples)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        smax = [num(s[1]) for s in inside if num(s[1]) is not None]
+        reasons = set()
+        for s in inside:
+            for name, v in zip(self.NAMES, s[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_sample_run(w_host, spec, groups, threads):
+    """Run the FP64 oracle on the listed (s, g) groups; returns (seconds, bytes)."""
+    import oracle
+
+    inp = oracle.Inputs.from_workload(w_host)
+    lens = w_host.lens_list
+    pairs = [(s, g * spec.G + r) for (s, g) in groups for r in range(spec.G)]
+    t = time.perf_counter()
+    oracle.decode(inp, pairs=pairs, num_threads=threads)
+    dt = time.perf_counter() - t
+    return dt, sum(group_bytes(spec, lens[s]) for s, _ in groups)
+
+
+def all_groups(spec, lens):
+    return [(s, g) for s in range(len(lens)) for g in range(spec.H_kv) if lens[s] > 0]
+
+
+def oracle_baseline(w_host, spec, budget_s: float, threads: int):
+    """Time the oracle on whole groups in round-robin order for about budget_s seconds."""
+    lens = w_host.lens_list
+    groups = all_groups(spec, lens)
+    done, secs, nbytes, i = 0, 0.0, 0, 0
+    batch = max(1, min(len(groups), 4 * threads))
+    while secs < budget_s and done < 4 * len(groups):
+        chunk = [groups[(i + k) % len(groups)] for k in range(batch)]
+        i += batch
+        dt, b = oracle_sample_run(w_host, spec, chunk, threads)
+        secs += dt
+        nbytes += b
+        done += batch
+    return secs, nbytes, done, len(groups)
+
+
+# ------------------------------------------------------------------ arms
+
+def build_and_load():
+    from paged_kv_gqa_decode_gb300 import build as pbuild
+
+    pbuild.build()
+    import paged_kv_gqa_decode_gb300 as pa
+
+    pa.load()
+    return pa
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def run_ours(args, world, rank, local):
+    pa = build_and_load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = workloads.spec(args.config)
+    seed = workloads.SEEDS[args.config] + rank  # each rank decodes its own batch (weak scaling)
+    w = workloads.make(spec, seed=seed, device=dev, poison="zero")
+    lens = w.lens_list
+    nbytes = algorithmic_bytes(spec, lens)
+    kv_bytes = w.k_cache.numel() * 2 * 2
+    reps = max(1, min(8, math.ceil(4 * L2_BYTES / max(1, kv_bytes))))
+    ks = [w.k_cache] + [w.k_cache.clone() for _ in range(reps - 1)]
+    vs = [w.v_cache] + [w.v_cache.clone() for _ in range(reps - 1)]
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        pa.paged_attn_decode(w.q, ks[i % reps], vs[i % reps], w.block_tables, w.seq_lens,
+                             w.scale, out=out, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # steps: as given, else enough for ~2 s of timed work
+    if args.steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(20):
+            step(i)
+        e1.record(stream)
+        e1.synchronize()
+        per = e0.elapsed_time(e1) / 20 / 1e3
+        steps = int(min(200000, max(50, 2.0 / max(per, 1e-6))))
+    else:
+        steps = args.steps
+
+    clocks = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    time.sleep(0.3 if clocks else 0)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    ev[0].record(stream)
+    for i in range(steps):
+        step(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier(world)
+    elapsed = ev[0].elapsed_time(ev[1]) / 1e3
+    elapsed = reduce_max(elapsed, world)
+    clock_info = None
+    if clocks:
+        clocks.stop()
+        clock_info = clocks.summary(t0, t1)
+    per_step = elapsed / steps
+    launches_per_step = -(-len(lens) // 4096)
+
+    # end to end through the public API: pinned host inputs in, result back to host
+    host_q = w.q.cpu().pin_memory()
+    host_bt = w.block_tables.cpu().pin_memory()
+    host_sl = w.seq_lens.cpu().pin_memory()
+    host_out = torch.empty_like(host_q).pin_memory()
+    dq, dbt, dsl = torch.empty_like(w.q), torch.empty_like(w.block_tables), \
+        torch.empty_like(w.seq_lens)
+    e2e_steps = max(20, min(steps, 2000))
+
+    def e2e_step(i):
+        dq.copy_(host_q, non_blocking=True)
+        dbt.copy_(host_bt, non_blocking=True)
+        dsl.copy_(host_sl, non_blocking=True)
+        pa.paged_attn_decode(dq, ks[i % reps], vs[i % reps], dbt, dsl, w.scale, out=out,
+                             stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    barrier(world)
+    t = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_time = reduce_max((time.perf_counter() - t) / e2e_steps, world)
+    h2d = host_q.numel() * 2 + host_bt.numel() * 4 + host_sl.numel() * 4
+    d2h = host_out.numel() * 2
+
+    result = None
+    if rank == 0:
+        peak, peak_src = measured_peaks()
+        achieved = nbytes["total"] / per_step / 1e9
+        traffic = profile_traffic(args.config)
+        cpu = None
+        if not args.no_cpu_baseline:
+            w_host = workloads.host_copy(w)
+            threads = len(os.sched_getaffinity(0))
+            secs, b, ngroups, total_groups = oracle_baseline(w_host, spec, args.cpu_budget,
+                                                             threads)
+            cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+                   "kind": "oracle",
+                   "sample": f"{ngroups} (sequence, KV head) groups of the {args.config} "
+                             f"workload ({total_groups} per step), round-robin, "
+                             f"{secs:.1f} s of FP64 CPU work"}
+        result = {
+            "metric": METRIC,
+            "value": round(world * nbytes["total"] / per_step / 1e9, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 5),
+            "us_per_step": round(per_step * 1e6, 2),
+            "kv_gbs": round(nbytes["kv"] / per_step / 1e9, 2),
+            "pct_of_hbm_peak": round(100 * achieved / peak, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; see workloads.py)",
+            "config": {
+                "workload": spec.description,
+                "name": args.config,
+                "num_seqs": spec.num_seqs, "H_q": spec.H_q, "H_kv": spec.H_kv,
+                "head_dim": spec.D, "block_size": spec.block_size,
+                "tokens": int(sum(lens)), "seed": seed,
+                "bytes_per_step": nbytes,
+                "l2": f"inputs larger than L2: {reps} KV-cache replicas rotated "
+                      f"({reps * kv_bytes / 1e9:.2f} GB vs 129 MB L2)",
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            },
+            "roofline": {
+                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback 6800 GB/s",
+                "kernel": "paged_decode_kernel (one launch per step, fused combine)",
+            },
+            "e2e": {"value": round(world * nbytes["total"] / e2e_time / 1e9, 2), "unit": "GB/s",
+                    "us_per_step": round(e2e_time * 1e6, 2),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": steps * launches_per_step,
+            "clocks": clock_info,
+        }
+        if cpu:
+            result["cpu_baseline"] = cpu
+    return result
+
+
+def run_reference(args, world, rank):
+    """The FP64 oracle on host cores, each step a bounded sample of the workload."""
+    if rank != 0:
+        return None
+    spec = workloads.spec(args.config)
+    seed = workloads.SEEDS[args.config]
+    w = workloads.make(spec, seed=seed, device="cpu", poison="zero")
+    lens = w.lens_list
+    threads = len(os.sched_getaffinity(0))
+    groups = all_groups(spec, lens)
+    steps = args.steps if args.steps is not None else 20
+    budget_total = args.reference_budget
+    # size each step so warmup + steps stay within the budget
+    per_step_budget = budget_total / max(1, steps + args.warmup)
+    dt1, _ = oracle_sample_run(w, spec, groups[:threads], threads)
+    per_group = dt1 / max(1, min(threads, len(groups)))
+    per_step_groups = int(max(1, min(len(groups), per_step_budget / max(per_group, 1e-9))))
+    i = 0
+
+    def step():
+        nonlocal i
+        chunk = [groups[(i + k) % len(groups)] for k in range(per_step_groups)]
+        i += per_step_groups
+        return oracle_sample_run(w, spec, chunk, threads)
+
+    for _ in range(args.warmup):
+        step()
+    secs = 0.0
+    nbytes = 0
+    for _ in range(steps):
+        dt, b = step()
+        secs += dt
+        nbytes += b
+    value = nbytes / secs / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(secs / steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": spec.description, "name": args.config, "seed": seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{per_step_groups} of {len(groups)} (sequence, KV head) "
+                                   "groups per step, round-robin"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama8b", choices=sorted(workloads.SPECS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--reference-budget", type=float, default=90.0,
+                    help="seconds of oracle work for --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

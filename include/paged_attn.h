@@ -1,0 +1,135 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged-KV GQA decode attention library.
+ *
+ * The operation (every entry point below computes it):
+ *
+ *   "Paged Attention Kernel Architecture for BI-V100", section 1 (Problem
+ *   Definition): for one new query token per sequence,
+ *       out[s, h, :] = softmax_t( scale * q[s, h, :] . K_t ) . V_t,   t < seq_lens[s],
+ *   where K_t / V_t are rows of a paged cache reached through a block table.
+ *   Layout, length meaning and GQA head map follow the "Add Cuda Kernel"
+ *   tutorial (RL.cu), include/kernels/attention.cuh, "Paged Attention - Decode":
+ *       K_t = k_cache[block_tables[s, t / block_size], g, t % block_size, :]
+ *       g   = h * H_kv / H_q          (H_q must be a multiple of H_kv; G = H_q / H_kv)
+ *   The caller passes `scale` (the tutorial's launcher recomputed 1/sqrt(head_dim)
+ *   and ignored its argument; here the argument is used as given).
+ *
+ * Tensors (all DEVICE pointers, owned by the caller, densely packed row-major,
+ * base addresses 16-byte aligned):
+ *   q            [num_seqs, H_q, head_dim]                      bf16   (read)
+ *   k_cache      [num_blocks, H_kv, block_size, head_dim]       bf16   (read)
+ *   v_cache      [num_blocks, H_kv, block_size, head_dim]       bf16   (read)
+ *   out          [num_seqs, H_q, head_dim]                      bf16   (written)
+ *   block_tables [num_seqs, max_blocks_per_seq]                 int32  (read)
+ *   seq_lens     [num_seqs]                                     int32  (read)
+ *
+ * seq_lens[s] is the number of cached tokens the query attends to (the new
+ * token's K/V must already be in the cache).  A length of 0 writes a zero row.
+ * Lengths are clamped to [0, max_blocks_per_seq * block_size].  Only the
+ * first ceil(seq_lens[s] / block_size) entries of a block-table row are read,
+ * and only the rows t < seq_lens[s] of those blocks: slots past the end may
+ * hold anything, NaN included.
+ *
+ * Supported: head_dim in {64, 128, 256}; block_size in {16, 32}; 1 <= G <= 16;
+ * num_seqs >= 0 (0 is a no-op).  Arithmetic: bf16 inputs, fp32 accumulation
+ * (tensor-core products of bf16 operands), bf16 output rounded to nearest even.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream), never synchronises, and never allocates except
+ * where an entry point says so.  Block ids outside the caller's pool are not
+ * detected by paged_attn_decode / paged_attn_decode_ws (the tensor memory
+ * access reads whatever lies at that address); paged_attn_decode_checked
+ * detects them.
+ *
+ * Errors: every entry point returns PAGED_ATTN_OK (0) or a negative
+ * PAGED_ATTN_ERR_* code.  Argument errors are detected on the host before any
+ * CUDA call.  Nothing aborts, throws or exits.
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAGED_ATTN_OK 0
+#define PAGED_ATTN_ERR_POINTER (-1)    /* null or not 16-byte aligned pointer */
+#define PAGED_ATTN_ERR_HEADS (-2)      /* H_kv <= 0, H_q % H_kv != 0, or G > 16 */
+#define PAGED_ATTN_ERR_HEAD_DIM (-3)   /* head_dim not in {64, 128, 256} */
+#define PAGED_ATTN_ERR_BLOCK_SIZE (-4) /* block_size not in {16, 32} */
+#define PAGED_ATTN_ERR_SIZES (-5)      /* num_seqs < 0, max_blocks_per_seq <= 0, or too large */
+#define PAGED_ATTN_ERR_CUDA (-6)       /* a CUDA runtime/driver call failed; see paged_attn_last_cuda_error */
+#define PAGED_ATTN_ERR_WORKSPACE (-7)  /* workspace pointer null/misaligned or smaller than required */
+#define PAGED_ATTN_ERR_SCALE (-8)      /* scale is not finite */
+
+/*
+ * Decode attention (the operation above).
+ *
+ * Scratch: the split-KV partial states live in a per-device workspace that the
+ * library owns.  The first call on a device (and any call that needs a larger
+ * workspace than before) allocates it with cudaMalloc and zero-fills it on
+ * `stream`; later calls allocate nothing.  Because the workspace is shared,
+ * calls that may overlap on the GPU (different streams, same device) race:
+ * give each concurrent stream its own workspace through paged_attn_decode_ws.
+ */
+int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
+                      float scale, void* stream);
+
+/*
+ * Bytes of caller-provided workspace that paged_attn_decode_ws needs for these
+ * sizes on the CURRENT device (it depends on the device's SM count).  Returns 0
+ * for unsupported sizes.
+ */
+size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
+                                  int max_blocks_per_seq, int block_size);
+
+/*
+ * Same operation with a caller-owned device workspace of at least
+ * paged_attn_workspace_bytes(...) bytes, 256-byte aligned.  The workspace
+ * must be zero-filled before its first use; every call that returns
+ * PAGED_ATTN_OK and completes on the GPU leaves its counter region (whose
+ * place depends only on the device) zero again, so the same workspace serves
+ * any later call on the same device that fits in it.  Calls sharing one
+ * workspace must not overlap on the GPU.  Allocates nothing.
+ */
+int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache, void* out,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                         int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
+                         float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Same operation with device-side input checks.  num_blocks is the size of the
+ * caller's block pool.  A block id outside [0, num_blocks) in a used table
+ * entry, or a sequence length outside [0, max_blocks_per_seq * block_size],
+ * sets bit 0 (bad block) or bit 1 (bad length) of *d_status (a device int32
+ * the caller zero-fills); bad blocks read as zero rows, bad lengths are
+ * clamped, and no memory outside the pool is read.  Bit 2 reports that a
+ * pipeline wait in the kernel ran out of its iteration limit (a library
+ * fault, never expected).  Uses the library-owned workspace like
+ * paged_attn_decode.
+ */
+int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
+                              const int32_t* block_tables, const int32_t* seq_lens,
+                              int num_seqs, int H_q, int H_kv, int head_dim,
+                              int max_blocks_per_seq, int block_size, float scale,
+                              long long num_blocks, int32_t* d_status, void* stream);
+
+/* Human-readable text for a PAGED_ATTN_* code (static storage). */
+const char* paged_attn_status_string(int status);
+
+/* The last cudaError_t / CUresult value behind a PAGED_ATTN_ERR_CUDA on this thread. */
+int paged_attn_last_cuda_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int paged_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

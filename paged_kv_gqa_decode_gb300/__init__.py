@@ -1,0 +1,173 @@
+"""GB300 (sm_103a) paged-KV GQA decode attention.
+
+A thin Python binding over the C ABI in ``include/paged_attn.h``: the
+functions here only marshal torch tensors into pointers, sizes and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the compiled library is missing the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "PagedAttnError",
+    "LIB_PATH",
+    "load",
+    "paged_attn_decode",
+    "paged_attn_decode_ws",
+    "paged_attn_decode_checked",
+    "paged_attn_workspace_bytes",
+    "paged_attn_status_string",
+    "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libpaged_kv_gqa_decode.so")
+
+# Every symbol declared in include/paged_attn.h.
+EXPORTED_SYMBOLS = (
+    "paged_attn_decode",
+    "paged_attn_workspace_bytes",
+    "paged_attn_decode_ws",
+    "paged_attn_decode_checked",
+    "paged_attn_status_string",
+    "paged_attn_last_cuda_error",
+    "paged_attn_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"paged_attn status {status}: {message}")
+        self.status = status
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the compiled library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build it with `python -m paged_kv_gqa_decode_gb300.build` "
+                "(needs nvcc from the CUDA 13 toolkit)")
+        lib = ctypes.CDLL(p)
+        P, I, F, LL, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong,
+                           ctypes.c_size_t)
+        common = [P, P, P, P, P, P, I, I, I, I, I, I, F]
+        lib.paged_attn_decode.argtypes = common + [P]
+        lib.paged_attn_decode.restype = I
+        lib.paged_attn_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.paged_attn_workspace_bytes.restype = SZ
+        lib.paged_attn_decode_ws.argtypes = common + [P, SZ, P]
+        lib.paged_attn_decode_ws.restype = I
+        lib.paged_attn_decode_checked.argtypes = common + [LL, P, P]
+        lib.paged_attn_decode_checked.restype = I
+        lib.paged_attn_status_string.argtypes = [I]
+        lib.paged_attn_status_string.restype = ctypes.c_char_p
+        lib.paged_attn_last_cuda_error.argtypes = []
+        lib.paged_attn_last_cuda_error.restype = I
+        lib.paged_attn_version.argtypes = []
+        lib.paged_attn_version.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def paged_attn_status_string(status: int) -> str:
+    return load().paged_attn_status_string(int(status)).decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        lib = load()
+        msg = lib.paged_attn_status_string(status).decode()
+        if status == -6:
+            msg += f" (CUDA error {lib.paged_attn_last_cuda_error()})"
+        raise PagedAttnError(status, msg)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _sizes(q, k_cache, block_tables):
+    num_seqs, H_q, D = (int(x) for x in q.shape)
+    _, H_kv, BS, Dk = (int(x) for x in k_cache.shape)
+    if Dk != D:
+        raise ValueError("q and the caches disagree on head_dim")
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    return num_seqs, H_q, H_kv, D, maxb, BS
+
+
+def _args(q, k_cache, v_cache, out, block_tables, seq_lens, scale):
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out),
+                    ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    num_seqs, H_q, H_kv, D, maxb, BS = _sizes(q, k_cache, block_tables)
+    return (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(block_tables),
+            _ptr(seq_lens), num_seqs, H_q, H_kv, D, maxb, BS, float(scale))
+
+
+def paged_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, scale: float, out=None,
+                      stream=None):
+    """out[s, h] = softmax(scale * q[s, h] . K^T) . V over the paged cache (see paged_attn.h)."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().paged_attn_decode(*_args(q, k_cache, v_cache, out, block_tables, seq_lens,
+                                           scale), _stream(stream)))
+    return out
+
+
+def paged_attn_workspace_bytes(num_seqs: int, H_q: int, H_kv: int, head_dim: int,
+                               max_blocks_per_seq: int, block_size: int) -> int:
+    return int(load().paged_attn_workspace_bytes(num_seqs, H_q, H_kv, head_dim,
+                                                 max_blocks_per_seq, block_size))
+
+
+def paged_attn_decode_ws(q, k_cache, v_cache, block_tables, seq_lens, scale: float, workspace,
+                         out=None, stream=None):
+    """As paged_attn_decode, with a caller-owned zero-initialised uint8 device workspace."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().paged_attn_decode_ws(*_args(q, k_cache, v_cache, out, block_tables, seq_lens,
+                                              scale), _ptr(workspace),
+                                       int(workspace.numel() * workspace.element_size()),
+                                       _stream(stream)))
+    return out
+
+
+def paged_attn_decode_checked(q, k_cache, v_cache, block_tables, seq_lens, scale: float,
+                              status, out=None, stream=None, num_blocks: Optional[int] = None):
+    """As paged_attn_decode, validating block ids and lengths on the device into ``status``
+    (an int32 device tensor of one element that the caller zero-fills)."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(q)
+    nb = int(k_cache.shape[0]) if num_blocks is None else int(num_blocks)
+    _check(load().paged_attn_decode_checked(*_args(q, k_cache, v_cache, out, block_tables,
+                                                   seq_lens, scale), nb, _ptr(status),
+                                            _stream(stream)))
+    return out

@@ -1,0 +1,56 @@
+// Internal interface between the C-ABI layer and the per-head-dim kernel
+// translation units (each instantiates the decode kernel for one head_dim).
+#pragma once
+
+#include <cstddef>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_kernel.cuh"
+
+namespace pagedattn {
+
+// Launches the decode kernel for head_dim D (64, 128 or 256) with the given
+// block size (16 or 32) and query-group class (g16: G > 8).
+cudaError_t launch_decode_d64(int block_size, bool g16, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const DecodeParams& p, int grid,
+                              size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_d128(int block_size, bool g16, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const DecodeParams& p, int grid,
+                               size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_d256(int block_size, bool g16, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const DecodeParams& p, int grid,
+                               size_t smem, cudaStream_t stream);
+
+// Launches one instantiation, first raising its dynamic shared-memory limit on
+// the current device when this launch needs more than was set before (the
+// record is per instantiation and per device).
+template <int D, int BS, bool G16>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                       int grid, size_t smem, cudaStream_t stream) {
+  static int limit_set[64] = {0};
+  auto kernel = paged_decode_kernel<D, BS, G16>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || limit_set[dev] < (int)smem) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) limit_set[dev] = (int)smem;
+  }
+  kernel<<<grid, kThreads, smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_for_dim(int block_size, bool g16, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
+  if (block_size == 16)
+    return g16 ? launch_one<D, 16, true>(tk, tv, p, grid, smem, stream)
+               : launch_one<D, 16, false>(tk, tv, p, grid, smem, stream);
+  return g16 ? launch_one<D, 32, true>(tk, tv, p, grid, smem, stream)
+             : launch_one<D, 32, false>(tk, tv, p, grid, smem, stream);
+}
+
+}  // namespace pagedattn

@@ -1,0 +1,380 @@
+// C ABI of the paged-KV GQA decode library (include/paged_attn.h): argument
+// validation, launch planning (grid, pipeline depth, workspace), TMA tensor
+// maps, and the per-device workspace the plain entry point owns.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "paged_attn.h"
+
+namespace pagedattn {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxSeqsPerLaunch = 4096;
+constexpr size_t kWsAlign = 256;
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int cuda_fail(int err) {
+  g_last_cuda_error = err;
+  return PAGED_ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int validate_sizes(int num_seqs, int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                   int block_size) {
+  if (H_kv <= 0 || H_q <= 0 || H_q % H_kv != 0 || H_q / H_kv > 16) return PAGED_ATTN_ERR_HEADS;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PAGED_ATTN_ERR_HEAD_DIM;
+  if (block_size != 16 && block_size != 32) return PAGED_ATTN_ERR_BLOCK_SIZE;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0) return PAGED_ATTN_ERR_SIZES;
+  // lengths up to max_blocks_per_seq * block_size must fit int32; table rows must be indexable
+  if ((long long)max_blocks_per_seq * block_size > 0x7fffffffLL) return PAGED_ATTN_ERR_SIZES;
+  if ((long long)H_kv * block_size > 0x7fffffffLL) return PAGED_ATTN_ERR_SIZES;
+  return PAGED_ATTN_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem = 0;  // opt-in dynamic shared memory per block
+};
+
+struct OwnedWorkspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_info;
+std::unordered_map<int, OwnedWorkspace> g_ws;
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_info.find(dev);
+  if (it != g_info.end()) {
+    *out = it->second;
+    return PAGED_ATTN_OK;
+  }
+  DeviceInfo di;
+  if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  g_info[dev] = di;
+  *out = di;
+  return PAGED_ATTN_OK;
+}
+
+// Everything a launch needs that depends only on sizes and the device.
+struct Plan {
+  int D, BS, G;
+  bool g16;
+  int chunk;    // sequences per launch
+  int stages;   // pipeline depth
+  size_t smem;  // dynamic shared memory per CTA
+  int grid;     // persistent CTAs
+  size_t off_counters, off_partials, ws_bytes;
+};
+
+template <int D, int BS>
+bool plan_smem(int G, int chunk, int max_smem, int* stages, size_t* smem) {
+  using L = SmemLayout<D, BS>;
+  const L none{0, G, chunk};
+  const long long fixed = none.total() + 2048;  // + alignment slack and static shared memory
+  const long long per_stage = L::kStageBytes + 16;
+  long long st = (max_smem - fixed) / per_stage;
+  if (st > kMaxStages) st = kMaxStages;
+  if (st < 2) return false;
+  const L lay{(int)st, G, chunk};
+  *stages = (int)st;
+  *smem = (size_t)lay.total() + 1024;
+  return true;
+}
+
+bool plan_smem_any(int D, int BS, int G, int chunk, int max_smem, int* stages, size_t* smem) {
+  if (D == 64) return BS == 16 ? plan_smem<64, 16>(G, chunk, max_smem, stages, smem)
+                               : plan_smem<64, 32>(G, chunk, max_smem, stages, smem);
+  if (D == 128) return BS == 16 ? plan_smem<128, 16>(G, chunk, max_smem, stages, smem)
+                                : plan_smem<128, 32>(G, chunk, max_smem, stages, smem);
+  return BS == 16 ? plan_smem<256, 16>(G, chunk, max_smem, stages, smem)
+                  : plan_smem<256, 32>(G, chunk, max_smem, stages, smem);
+}
+
+int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& di, Plan* pl) {
+  pl->D = D;
+  pl->BS = BS;
+  pl->G = H_q / H_kv;
+  pl->g16 = pl->G > 8;
+  pl->grid = di.sms;
+  int chunk = num_seqs < kMaxSeqsPerLaunch ? (num_seqs > 0 ? num_seqs : 1) : kMaxSeqsPerLaunch;
+  // keep at least 4 pipeline stages where possible by launching fewer sequences at a time
+  for (;;) {
+    if (plan_smem_any(D, BS, pl->G, chunk, di.max_smem, &pl->stages, &pl->smem) &&
+        (pl->stages >= 4 || chunk <= 64))
+      break;
+    if (chunk <= 1) return PAGED_ATTN_ERR_SIZES;
+    chunk = (chunk + 1) / 2;
+  }
+  pl->chunk = chunk;
+  // [0, 256): status word; then one combine counter per CTA; then the partial
+  // states.  The counter region depends on the device only, so a workspace
+  // reused by calls of any size always finds it zero.
+  pl->off_counters = kWsAlign;
+  pl->off_partials = pl->off_counters + round_up((size_t)pl->grid * 4, kWsAlign);
+  pl->ws_bytes = pl->off_partials +
+                 round_up((size_t)pl->grid * 2 * pl->G * (size_t)(D + 4) * 4, kWsAlign);
+  return PAGED_ATTN_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  static cudaError_t cached_err = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cached_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                  cudaEnableDefault, &q);
+    if (cached_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      cached = reinterpret_cast<EncodeTiledFn>(p);
+    else if (cached_err == cudaSuccess)
+      cached_err = cudaErrorSymbolNotFound;
+  });
+  if (!cached) return cuda_fail(cached_err);
+  *fn = cached;
+  return PAGED_ATTN_OK;
+}
+
+// 3-D view of a cache: (column, row within a block = kv_head * BS + slot, block id).
+// A page of one KV head is the box {64, BS, 1} at (64 * half, g * BS, block);
+// 128-byte swizzle matches the ldmatrix addressing in the kernel.
+int encode_cache_map(const void* base, int D, int BS, int H_kv, long long num_blocks,
+                     CUtensorMap* map) {
+  EncodeTiledFn enc = nullptr;
+  int rc = get_encoder(&enc);
+  if (rc != PAGED_ATTN_OK) return rc;
+  const cuuint64_t stride1 = (cuuint64_t)D * 2;
+  const cuuint64_t stride2 = stride1 * (cuuint64_t)H_kv * BS;
+  cuuint64_t nb = (cuuint64_t)num_blocks;
+  if (num_blocks <= 0) {
+    // pool size unknown: any non-negative int32 block id is addressable, as long
+    // as the described extent stays below 2^40 bytes
+    nb = ((cuuint64_t)1 << 40) / stride2;
+    if (nb > 0x7fffffffULL) nb = 0x7fffffffULL;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv * BS, nb};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)BS, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail((int)r);
+  return PAGED_ATTN_OK;
+}
+
+cudaError_t launch_dim(int D, int BS, bool g16, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+  if (D == 64) return launch_decode_d64(BS, g16, tk, tv, p, grid, smem, st);
+  if (D == 128) return launch_decode_d128(BS, g16, tk, tv, p, grid, smem, st);
+  return launch_decode_d256(BS, g16, tk, tv, p, grid, smem, st);
+}
+
+int check_pointers(const void* q, const void* k, const void* v, const void* out,
+                   const int32_t* bt, const int32_t* sl) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(bt) ||
+      !aligned16(sl))
+    return PAGED_ATTN_ERR_POINTER;
+  return PAGED_ATTN_OK;
+}
+
+// Runs the whole operation in chunks of plan.chunk sequences on `stream`.
+int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache, void* out,
+        const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
+        int max_blocks_per_seq, float scale, void* ws, int32_t* status, long long num_blocks,
+        cudaStream_t stream) {
+  CUtensorMap tk, tv;
+  int rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk);
+  if (rc != PAGED_ATTN_OK) return rc;
+  rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv);
+  if (rc != PAGED_ATTN_OK) return rc;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  for (int s0 = 0; s0 < num_seqs; s0 += pl.chunk) {
+    const int n = num_seqs - s0 < pl.chunk ? num_seqs - s0 : pl.chunk;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)s0 * H_q * pl.D;
+    p.out = static_cast<__nv_bfloat16*>(out) + (size_t)s0 * H_q * pl.D;
+    p.block_tables = bt + (size_t)s0 * max_blocks_per_seq;
+    p.seq_lens = seq_lens + s0;
+    p.num_seqs = n;
+    p.H_q = H_q;
+    p.H_kv = H_kv;
+    p.G = pl.G;
+    p.maxb = max_blocks_per_seq;
+    p.stages = pl.stages;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = status ? status : reinterpret_cast<int32_t*>(wsb);
+    p.counters = reinterpret_cast<int32_t*>(wsb + pl.off_counters);
+    p.partials = reinterpret_cast<float*>(wsb + pl.off_partials);
+    p.num_blocks = num_blocks;
+    cudaError_t e = launch_dim(pl.D, pl.BS, pl.g16, tk, tv, p, pl.grid, pl.smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PAGED_ATTN_OK;
+}
+
+// The library-owned workspace of the current device, grown to at least `bytes`.
+int owned_workspace(size_t bytes, cudaStream_t stream, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_mu);
+  OwnedWorkspace& w = g_ws[dev];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      // earlier calls on any stream may still use the old buffer
+      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    void* p = nullptr;
+    if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemsetAsync(p, 0, bytes, stream)) != cudaSuccess) {
+      cudaFree(p);
+      return cuda_fail(e);
+    }
+    w.ptr = p;
+    w.bytes = bytes;
+  }
+  *out = w.ptr;
+  return PAGED_ATTN_OK;
+}
+
+int common_checks(const void* q, const void* k, const void* v, const void* out, const int32_t* bt,
+                  const int32_t* sl, int num_seqs, int H_q, int H_kv, int head_dim,
+                  int max_blocks_per_seq, int block_size, float scale) {
+  int rc = validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return PAGED_ATTN_ERR_SCALE;
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  return check_pointers(q, k, v, out, bt, sl);
+}
+
+}  // namespace
+}  // namespace pagedattn
+
+using namespace pagedattn;
+
+extern "C" {
+
+int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
+                      float scale, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
+size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
+                                  int max_blocks_per_seq, int block_size) {
+  if (validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size) !=
+      PAGED_ATTN_OK)
+    return 0;
+  DeviceInfo di;
+  if (device_info(&di) != PAGED_ATTN_OK) return 0;
+  Plan pl;
+  if (make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl) != PAGED_ATTN_OK) return 0;
+  return pl.ws_bytes;
+}
+
+int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache, void* out,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                         int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
+                         float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0)
+    return PAGED_ATTN_ERR_WORKSPACE;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  if (workspace_bytes < pl.ws_bytes) return PAGED_ATTN_ERR_WORKSPACE;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, workspace, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
+                              const int32_t* block_tables, const int32_t* seq_lens,
+                              int num_seqs, int H_q, int H_kv, int head_dim,
+                              int max_blocks_per_seq, int block_size, float scale,
+                              long long num_blocks, int32_t* d_status, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (num_blocks <= 0 || num_blocks > 0x7fffffffLL) return PAGED_ATTN_ERR_SIZES;
+  if (d_status == nullptr || (reinterpret_cast<uintptr_t>(d_status) & 3) != 0)
+    return PAGED_ATTN_ERR_POINTER;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, d_status, num_blocks, st);
+}
+
+const char* paged_attn_status_string(int status) {
+  switch (status) {
+    case PAGED_ATTN_OK: return "ok";
+    case PAGED_ATTN_ERR_POINTER: return "null or misaligned pointer";
+    case PAGED_ATTN_ERR_HEADS: return "H_q must be a positive multiple of H_kv with H_q/H_kv <= 16";
+    case PAGED_ATTN_ERR_HEAD_DIM: return "head_dim must be 64, 128 or 256";
+    case PAGED_ATTN_ERR_BLOCK_SIZE: return "block_size must be 16 or 32";
+    case PAGED_ATTN_ERR_SIZES: return "num_seqs, max_blocks_per_seq or num_blocks out of range";
+    case PAGED_ATTN_ERR_CUDA: return "CUDA call failed (see paged_attn_last_cuda_error)";
+    case PAGED_ATTN_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    case PAGED_ATTN_ERR_SCALE: return "scale is not finite";
+    default: return "unknown status";
+  }
+}
+
+int paged_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int paged_attn_version(void) { return 100; }
+
+}  // extern "C"

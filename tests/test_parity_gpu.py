@@ -1,0 +1,241 @@
+"""GPU parity: the sm_103a kernels against the FP64 oracle, element by element.
+
+Tolerance (bf16 in, fp32 accumulate, bf16 out): max |gpu - oracle| <= 2e-2 and
+mean |gpu - oracle| <= 2e-3 on every workload; outputs must be finite although
+every cache row the definition never reads holds NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pa = pytest.importorskip("paged_kv_gqa_decode_gb300")
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_decode_gb300 import build
+
+    build.build()
+    pa.load()
+
+
+def run_gpu(w, **kw):
+    out = pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale,
+                               **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def errors(out, ref):
+    got = out.detach().float().cpu().double().numpy().reshape(ref.shape)
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - ref)
+    return float(err.max()), float(err.mean())
+
+
+def assert_parity(out, ref, what=""):
+    mx, mean = errors(out, ref)
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max {mx:.3e} mean {mean:.3e}"
+
+
+def reference(w):
+    return oracle.decode(workloads.host_copy(w))
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "qwen100k", "ragged256", "gqa8"])
+def test_published_workloads_full_size(name):
+    w = workloads.make(name, device="cuda", poison="nan")
+    out = run_gpu(w)
+    ref = reference(w)
+    assert_parity(out, ref, name)
+
+
+# The "Add Cuda Kernel" tutorial's paged decode cases (D 128, block 16):
+# (num_seqs, context, H_q, H_kv); here with shuffled tables and NaN-filled tails.
+@pytest.mark.parametrize("num_seqs,ctx,H_q,H_kv",
+                         [(1, 32, 2, 1), (1, 128, 16, 8), (2, 64, 4, 2), (4, 128, 16, 8)])
+def test_tutorial_decode_cases(num_seqs, ctx, H_q, H_kv):
+    sp = workloads.custom_spec("tutorial", num_seqs, H_q, H_kv, 128, 16, [ctx] * num_seqs)
+    w = workloads.make(sp, seed=7, device="cuda")
+    assert_parity(run_gpu(w), reference(w))
+
+
+EDGE_LENS = [0, 1, 15, 16, 17, 31, 32, 33, 100, 257, 1000]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("H_q,H_kv", [(4, 4), (8, 4), (8, 2), (12, 2), (8, 1), (24, 2), (16, 1)])
+def test_shapes_and_ragged_tails(D, BS, H_q, H_kv):
+    sp = workloads.custom_spec(f"sweep", len(EDGE_LENS), H_q, H_kv, D, BS, EDGE_LENS,
+                               max_len=1024)
+    w = workloads.make(sp, seed=D * 1000 + BS * 10 + H_q + H_kv, device="cuda")
+    out = run_gpu(w)
+    ref = reference(w)
+    assert_parity(out, ref, f"D{D} BS{BS} G{H_q // H_kv}")
+    # an empty sequence gives an exact zero row
+    assert torch.count_nonzero(out[0]).item() == 0
+
+
+def test_single_long_sequence_splits_across_all_ctas():
+    sp = workloads.custom_spec("one", 1, 8, 1, 128, 16, [60000])
+    w = workloads.make(sp, seed=3, device="cuda")
+    assert_parity(run_gpu(w), reference(w))
+
+
+def test_many_short_sequences():
+    lens = list(np.random.default_rng(4).integers(0, 40, size=700))
+    sp = workloads.custom_spec("short", len(lens), 8, 2, 128, 16, lens, max_len=48)
+    w = workloads.make(sp, seed=4, device="cuda")
+    assert_parity(run_gpu(w), reference(w))
+
+
+def test_more_sequences_than_one_launch_holds():
+    lens = list(np.random.default_rng(5).integers(1, 70, size=5000))
+    sp = workloads.custom_spec("wide", len(lens), 4, 1, 64, 16, lens, max_len=80)
+    w = workloads.make(sp, seed=5, device="cuda")
+    assert_parity(run_gpu(w), reference(w))
+
+
+def test_all_sequences_empty():
+    sp = workloads.custom_spec("empty", 3, 8, 2, 128, 16, [0, 0, 0], max_len=16)
+    w = workloads.make(sp, seed=6, device="cuda")
+    out = torch.full_like(w.q, float("nan"))
+    run_gpu(w, out=out)
+    assert torch.count_nonzero(out).item() == 0
+
+
+def test_empty_batch():
+    w = workloads.make("tiny", device="cuda")
+    out = pa.paged_attn_decode(w.q[:0], w.k_cache, w.v_cache, w.block_tables[:0],
+                               w.seq_lens[:0], w.scale)
+    assert out.shape[0] == 0
+
+
+def test_lengths_beyond_the_table_are_clamped():
+    sp = workloads.custom_spec("cap", 2, 8, 2, 128, 16, [64, 50], max_len=64)
+    w = workloads.make(sp, seed=8, device="cuda", poison="none")
+    ref = reference(w)
+    w2 = workloads.Workload(**{**w.__dict__, "seq_lens": w.seq_lens + torch.tensor(
+        [100, 0], dtype=torch.int32, device="cuda")})
+    assert_parity(run_gpu(w2), ref)
+
+
+def test_identity_table_and_relabelled_blocks_agree_bitwise():
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    base = run_gpu(w)
+    pi = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1)).cuda()
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[pi] = w.k_cache
+    v2[pi] = w.v_cache
+    bt2 = pi[w.block_tables.long()].int()
+    out = pa.paged_attn_decode(w.q, k2, v2, bt2, w.seq_lens, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), base.view(torch.int16))
+
+
+def test_repeat_calls_are_bitwise_identical():
+    w = workloads.make("ragged256", device="cuda", poison="nan")
+    a = run_gpu(w).clone()
+    b = run_gpu(w)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_caller_workspace_matches_owned_workspace():
+    w = workloads.make("qwen100k", device="cuda", poison="nan")
+    base = run_gpu(w).clone()
+    n = pa.paged_attn_workspace_bytes(4, 24, 4, 256, w.max_blocks_per_seq, 16)
+    assert n > 0
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        out = pa.paged_attn_decode_ws(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                      w.scale, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), base.view(torch.int16))
+    with pytest.raises(pa.PagedAttnError):
+        pa.paged_attn_decode_ws(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale,
+                                ws[: n // 2])
+
+
+def test_checked_variant_flags_bad_inputs_without_faulting():
+    w = workloads.make("tiny", device="cuda", poison="nan")
+    ref = reference(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.paged_attn_decode_checked(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                       w.scale, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert_parity(out, ref)
+    bad_bt = w.block_tables.clone()
+    bad_bt[0, 1] = w.num_blocks + 5     # outside the pool: read as zero rows, flagged
+    bad_bt[1, 0] = -3
+    pa.paged_attn_decode_checked(w.q, w.k_cache, w.v_cache, bad_bt, w.seq_lens, w.scale, status)
+    torch.cuda.synchronize()
+    assert status.item() & 1
+    status.zero_()
+    long = w.seq_lens.clone()
+    long[1] = w.max_blocks_per_seq * 16 + 9
+    out = pa.paged_attn_decode_checked(w.q, w.k_cache, w.v_cache, w.block_tables, long,
+                                       w.scale, status)
+    torch.cuda.synchronize()
+    assert status.item() & 2
+
+
+def test_runs_on_a_side_stream_and_in_a_cuda_graph():
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    ref = run_gpu(w).clone()
+    side = torch.cuda.Stream()
+    out = torch.empty_like(w.q)
+    with torch.cuda.stream(side):
+        pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale,
+                             out=out)
+    side.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    out2 = torch.empty_like(w.q)
+    with torch.cuda.graph(g):
+        pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale,
+                             out=out2)
+    for _ in range(3):
+        out2.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), ref.view(torch.int16))
+
+
+def test_peaked_softmax_rows():
+    # keys scaled so one token dominates each row: stresses the running-max rescale
+    sp = workloads.custom_spec("peak", 8, 16, 2, 128, 16, [3000] * 8, peaked_k_frac=0.002,
+                               peaked_k_gain=16.0)
+    w = workloads.make(sp, seed=9, device="cuda")
+    assert_parity(run_gpu(w), reference(w))
+
+
+def test_one_workspace_serves_calls_of_different_sizes():
+    specs = ["qwen100k", "ragged256", "tiny", "gqa8", "llama8b"]
+    ws_list = [workloads.make(n, device="cuda", poison="nan") for n in specs]
+    need = max(pa.paged_attn_workspace_bytes(w.spec.num_seqs, w.spec.H_q, w.spec.H_kv,
+                                             w.spec.D, w.max_blocks_per_seq,
+                                             w.spec.block_size) for w in ws_list)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    refs = {}
+    for rnd in range(2):
+        for n, w in zip(specs, ws_list):
+            out = pa.paged_attn_decode_ws(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                          w.seq_lens, w.scale, ws)
+            torch.cuda.synchronize()
+            if rnd == 0:
+                refs[n] = reference(w)
+            assert_parity(out, refs[n], f"{n} round {rnd}")
+    del ws_list
