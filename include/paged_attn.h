@@ -109,9 +109,9 @@ int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache
  * sets bit 0 (bad block) or bit 1 (bad length) of *d_status (a device int32
  * the caller zero-fills); bad blocks read as zero rows, bad lengths are
  * clamped, and no memory outside the pool is read.  Bit 2 reports that a
- * pipeline wait in the kernel ran out of its iteration limit (a library
- * fault, never expected).  Uses the library-owned workspace like
- * paged_attn_decode.
+ * pipeline wait in the kernel ran out of its iteration limit and bit 3 that
+ * the kernel rejected its launch configuration (library faults, never
+ * expected).  Uses the library-owned workspace like paged_attn_decode.
  */
 int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
                               const int32_t* block_tables, const int32_t* seq_lens,

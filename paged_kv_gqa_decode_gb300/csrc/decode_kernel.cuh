@@ -8,25 +8,27 @@
 //    fixed 512-token partitions; here the split is re-derived for ragged
 //    batches): the units of work are pages (s, g, p) -- one physical block of
 //    one KV head.  Flattened in (s, g, p) order they are cut into C equal
-//    contiguous ranges, one per persistent CTA (C = number of SMs, reduced so
+//    contiguous ranges, one per persistent CTA (two CTAs per SM, C reduced so
 //    each CTA gets at least kMinPagesPerCta pages).  Every CTA streams the same
 //    number of bytes whatever the length mix, and a range crossing (s, g)
 //    boundaries simply produces one partial softmax state per piece.
 //
-//  * Data movement: one producer warp walks the range, reads the block table
-//    and issues TMA tiled loads (cp.async.bulk.tensor.3d) of each K and V page
-//    into a ring of shared-memory stages, 128-byte swizzled, completing on an
-//    mbarrier per stage.  Each page of one KV head is one contiguous
-//    block_size x head_dim run in HBM; the 3-D tensor map addresses it as
-//    (column, g * block_size, physical block).
+//  * Data movement: a producer warp walks the range, reads the block table
+//    and issues TMA tiled loads (cp.async.bulk.tensor.4d) into a ring of
+//    shared-memory stages, several lanes issuing at once.  One load brings a
+//    whole page of one KV head (block_size x head_dim, contiguous in HBM):
+//    the 4-D tensor map views a row as two-or-more 64-column halves so the
+//    page lands as [half][row][128 B] with the 128-byte swizzle; each stage
+//    holds the K page and the V page and completes on one mbarrier.
 //
-//  * Math: consumer warps take pages round-robin.  The whole GQA group of the
-//    KV head (G <= 16 query heads, zero-padded to 16 rows) is the A operand of
-//    bf16 m16n8k16 tensor-core MMAs: S = Q K^T over the page (K read with
-//    ldmatrix from the swizzled tile), online softmax in fp32 on the
+//  * Math (tensor cores, bf16 m16n8k16, fp32 accumulate), with the page's
+//    tokens as the M dimension and the GQA group as N (8 heads per n-tile):
+//    S^T = K Q^T (K read with ldmatrix from the swizzled tile, Q^T held in
+//    registers for the whole piece), online softmax in fp32 on the
 //    accumulator fragments (BI-V100 design, section 2, Level 1: running max,
-//    exp-sum and weighted V), then O += P V (V read with ldmatrix.trans).  So
-//    every K/V byte leaves HBM once and feeds all G heads.
+//    exp-sum and weighted V), P^T turned into the B operand with movmatrix,
+//    then O^T += V^T P^T (V read with ldmatrix.trans).  Every K/V byte leaves
+//    HBM once and feeds all G heads of its group.
 //
 //  * Merge (BI-V100 design, section 2, Levels 2 and 3): at the end of each
 //    (s, g) piece the consumer warps merge their states through shared
@@ -50,14 +52,24 @@ namespace pagedattn {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
+// Two independent pipelines per SM; the one variant whose accumulators need the
+// whole register file (head_dim 256 with more than 8 heads per group) runs one.
+__host__ __device__ constexpr int ctas_per_sm(int D, bool g16) {
+  return (D >= 256 && g16) ? 1 : 2;
+}
+// The query group is kept in shared memory (read per page with ldmatrix)
+// where holding it in registers would push the kernel past its register budget.
+__host__ __device__ constexpr bool q_in_smem(int D, bool g16) { return D >= 256 || g16; }
 constexpr int kMinPagesPerCta = 8;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 16;  // ring depth; always a multiple of kConsumerWarps
+constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
 constexpr int kConsumerBarrier = 1;
 
 // Status bits written to the workspace / caller status word.
 constexpr int kStatusBadBlock = 1;
 constexpr int kStatusBadLength = 2;
 constexpr int kStatusTimeout = 4;
+constexpr int kStatusConfig = 8;
 
 struct DecodeParams {
   const __nv_bfloat16* q;       // [num_seqs, H_q, D]
@@ -84,7 +96,7 @@ struct SmemLayout {
   static constexpr int kTileBytes = BS * 128;         // one half of one page
   static constexpr int kPageBytes = kHalves * kTileBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  static constexpr int kRowStride = D + 8;            // padded fp32 row in the merge buffer
+  static constexpr int kRowStride = D + 4;            // padded fp32 row in the merge buffer
 
   int stages, G, num_seqs;
   __host__ __device__ int bars() const { return stages * kStageBytes; }
@@ -93,9 +105,10 @@ struct SmemLayout {
   __host__ __device__ int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   __host__ __device__ int flag() const { return final_ml() + 32 * 4; }
   __host__ __device__ int merge_o() const { return flag() + 16; }
-  __host__ __device__ int prefix() const {
+  __host__ __device__ int qtile() const {  // [16 heads][D] bf16, 16-byte chunks swizzled
     return merge_o() + kConsumerWarps * G * kRowStride * 4;
   }
+  __host__ __device__ int prefix() const { return qtile() + 16 * D * 2; }
   __host__ __device__ int lens() const { return prefix() + (num_seqs + 1) * 4; }
   __host__ __device__ int total() const { return lens() + num_seqs * 4; }
 };
@@ -142,7 +155,7 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
 }
 
 template <int D, int BS, bool G16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using L = SmemLayout<D, BS>;
@@ -151,9 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStageBytes = L::kStageBytes;
   constexpr int kRowStride = L::kRowStride;
   constexpr int kPartialRow = D + 4;  // [M, L, pad, pad, o[0..D)]
-  constexpr int kNT = D / 8;          // n8 tiles across head_dim
-  constexpr int kKT = D / 16;         // k16 steps across head_dim
-  constexpr int kST = BS / 8;         // n8 token tiles per page
+  constexpr int kNH = G16 ? 2 : 1;    // n8 tiles of query heads
+  constexpr int kDT = D / 16;         // 16-wide tiles of head_dim
+  constexpr int kTG = BS / 16;        // 16-token groups per page
+  constexpr bool kQSmem = q_in_smem(D, G16);
+  constexpr int kQRegs = kQSmem ? 1 : kDT;  // register copy of Q^T (unused when in smem)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -166,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sm_final = reinterpret_cast<float*>(smem + lay.final_ml());  // [0,16) M, [16,32) L
   int* sm_flag = reinterpret_cast<int*>(smem + lay.flag());
   float* sm_o = reinterpret_cast<float*>(smem + lay.merge_o());
+  uint8_t* sm_q = smem + lay.qtile();
   int* sm_prefix = reinterpret_cast<int*>(smem + lay.prefix());
   int* sm_len = reinterpret_cast<int*>(smem + lay.lens());
 
@@ -192,8 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm_len[s] = len;
       local += (len + BS - 1) / BS;
     }
-    // block-wide exclusive scan of `local`
-    int incl = local;
+    int incl = local;  // block-wide exclusive scan of `local`
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -222,6 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const long long W = (long long)sm_prefix[N] * H_kv;
   if (W == 0) return;
+  // Each ring slot must belong to one consumer warp (see the host plan).
+  if (p.stages <= 0 || p.stages % kConsumerWarps != 0) {
+    if (tid == 0) atomicOr(p.status, kStatusConfig);
+    return;
+  }
   const long long C =
       min((long long)gridDim.x, max(1LL, (W + kMinPagesPerCta - 1) / kMinPagesPerCta));
   if ((long long)blockIdx.x >= C) return;
@@ -245,6 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
     }
     const uint64_t policy = l2_evict_first_policy();
+    // Lanes issue loads for consecutive units together; never more lanes than
+    // stages, so the lanes of one wave always wait on distinct slots.
+    const int issue_lanes = min(kMaxIssueLanes, p.stages);
     Walker wk;
     if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_kv);
     auto fetch = [&](long long u) -> int2 {
@@ -256,10 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return make_int2(pb, wk.g);
     };
     int2 cur = fetch(u0 + lane);
-    int stage = 0;
-    uint32_t phase = 0;
     bool abort = false;
-    long long issued = 0;
     for (long long ub = u0; ub < u1 && !abort; ub += 32) {
       // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
@@ -268,42 +288,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt = fetch(ub + 32 + lane);
       }
       const int cnt = (int)min(32LL, u1 - ub);
-      for (int j = 0; j < cnt; ++j) {
+      for (int j0 = 0; j0 < cnt && !abort; j0 += issue_lanes) {
+        const int j = j0 + (lane < issue_lanes ? lane : 0);
         const int pb = __shfl_sync(0xffffffffu, cur.x, j);
         const int g = __shfl_sync(0xffffffffu, cur.y, j);
-        if (lane == 0 && !abort) {
+        bool bad = false;
+        if (lane < issue_lanes && j0 + lane < cnt) {
+          const long long i = ub - u0 + j;  // unit index within this CTA
+          const int stage = (int)(i % p.stages);
+          const uint32_t phase = (uint32_t)((i / p.stages) & 1);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
             atomicOr(p.status, kStatusTimeout);
-            abort = true;
+            bad = true;
           } else {
             mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
             uint8_t* st = smem + stage * kStageBytes;
-#pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
-              tma_load_3d(st + hh * kTileBytes, &tm_k, &full_bar[stage], hh * 64, g * BS, pb,
-                          policy);
-#pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
-              tma_load_3d(st + kPageBytes + hh * kTileBytes, &tm_v, &full_bar[stage], hh * 64,
-                          g * BS, pb, policy);
-            ++issued;
+            tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
+            tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
           }
         }
-        abort = __shfl_sync(0xffffffffu, abort, 0);
-        if (++stage == p.stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        abort = __any_sync(0xffffffffu, bad);
       }
       cur = nxt;
     }
-    // Drain: make sure no tensor copy issued by this CTA is still in flight when it exits.
-    if (lane == 0 && issued > 0) {
-      const long long first = issued > p.stages ? issued - p.stages : 0;
-      for (long long i = first; i < issued; ++i) {
-        const int st = (int)(i % p.stages);
-        const uint32_t ph = (uint32_t)((i / p.stages) & 1);
-        if (!mbar_wait(&full_bar[st], ph)) {
+    // Drain: no tensor copy issued by this CTA may still be in flight when it exits.
+    if (lane == 0) {
+      const long long n = u1 - u0;
+      for (long long i = n > p.stages ? n - p.stages : 0; i < n; ++i) {
+        if (!mbar_wait(&full_bar[i % p.stages], (uint32_t)((i / p.stages) & 1))) {
           atomicOr(p.status, kStatusTimeout);
           break;
         }
@@ -313,199 +325,269 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ===================================================================== consumers
-  const int r0 = lane >> 2;       // accumulator row (query head within the group)
-  const int cq = 2 * (lane & 3);  // column pair within an n8 tile
-  const int ctid = tid;           // 0 .. kConsumerThreads-1
+  // Fragment ownership (m16n8k16): lane holds tokens / head_dim rows lane/4 and
+  // lane/4 + 8, and query heads 8 * nh + 2 * (lane % 4) + {0, 1}.
+  const int quad = lane & 3;
+  const int row = lane >> 2;
+  const int ctid = tid;  // 0 .. kConsumerThreads-1
 
-  uint32_t qa[kKT][G16 ? 4 : 2];  // A fragments of the query group
-  float o_acc[kNT][G16 ? 4 : 2];  // output accumulator fragments
-  float m_run[2], l_run[2];       // per accumulator row: running max (log2 domain) and sum
+  uint32_t qb[kQRegs][kNH][2];  // B operand Q^T of the query group (register variant)
+  float o_acc[kDT][kNH][4];   // O^T accumulators
+  float m_run[kNH][2];        // running max per owned head (log2 domain)
+  float l_run[kNH][2];        // running sum per owned head (this lane's tokens)
 
+  // Query group of piece (s, g): registers, or the shared tile [head][chunk ^ (head % 8)].
+  // Callers hold the consumer barrier after a shared-tile load before any page.
   auto load_q = [&](int s, int g) {
-    const __nv_bfloat16* qb = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
+    const __nv_bfloat16* qg = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
+    if constexpr (kQSmem) {
+      for (int i = ctid; i < 16 * (D / 8); i += kConsumerThreads) {
+        const int h = i / (D / 8);
+        const int c = i - h * (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (h < G) v = __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D) + c);
+        const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
+        *reinterpret_cast<uint4*>(sm_q + h * (D * 2) + pc * 16) = v;
+      }
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < kKT; ++kk) {
-      const int c = kk * 16 + cq;
-      const uint32_t* r0p = reinterpret_cast<const uint32_t*>(qb + (size_t)r0 * D + c);
-      qa[kk][0] = r0 < G ? __ldg(r0p) : 0u;
-      qa[kk][1] = r0 < G ? __ldg(r0p + 4) : 0u;
-      if constexpr (G16) {
-        const uint32_t* r1p = reinterpret_cast<const uint32_t*>(qb + (size_t)(r0 + 8) * D + c);
-        qa[kk][2] = r0 + 8 < G ? __ldg(r1p) : 0u;
-        qa[kk][3] = r0 + 8 < G ? __ldg(r1p + 4) : 0u;
+      for (int nh = 0; nh < kNH; ++nh) {
+        const int h = 8 * nh + row;
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + (size_t)h * D + 2 * quad);
+#pragma unroll
+        for (int kk = 0; kk < kQRegs; ++kk) {
+          qb[kk][nh][0] = h < G ? __ldg(qr + 8 * kk) : 0u;
+          qb[kk][nh][1] = h < G ? __ldg(qr + 8 * kk + 4) : 0u;
+        }
       }
     }
   };
   auto reset = [&]() {
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
+    for (int dt = 0; dt < kDT; ++dt)
 #pragma unroll
-      for (int e = 0; e < (G16 ? 4 : 2); ++e) o_acc[nt][e] = 0.f;
-    m_run[0] = m_run[1] = -INFINITY;
-    l_run[0] = l_run[1] = 0.f;
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_acc[dt][nh][e] = 0.f;
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        m_run[nh][e] = -INFINITY;
+        l_run[nh][e] = 0.f;
+      }
   };
 
-  // One page: S = Q K^T, online softmax, O += P V.
+  // One page: S^T = K Q^T, online softmax, O^T += V^T P^T.
   auto process_page = [&](const uint8_t* kt, const uint8_t* vt, int valid) {
     const uint32_t kbase = smem_addr(kt);
     const uint32_t vbase = smem_addr(vt);
-    float s_acc[kST][4];
+    const int li = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix.x4
+    // Two accumulator sets (even / odd 16-column steps) halve the dependent MMA chain.
+    float s_acc[kTG][kNH][4], s_odd[kTG][kNH][4];
 #pragma unroll
-    for (int j = 0; j < kST; ++j) s_acc[j][0] = s_acc[j][1] = s_acc[j][2] = s_acc[j][3] = 0.f;
+    for (int tg = 0; tg < kTG; ++tg)
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s_acc[tg][nh][e] = s_odd[tg][nh][e] = 0.f;
 
-    // ---- S = Q K^T: B operand rows are tokens, 16-byte chunks of head_dim, swizzled
+    // ---- S^T = K Q^T: A operand = 16 tokens x 16 columns of the swizzled K tile
 #pragma unroll
-    for (int kq = 0; kq < D / 32; ++kq) {
-      const int chunk = 4 * kq + (lane >> 3);
-      const uint32_t koff = (uint32_t)((chunk >> 3) * kTileBytes +
-                                       ((((chunk & 7) ^ (lane & 7))) << 4));
+    for (int kq = 0; kq < kDT / 2; ++kq) {
+      uint32_t qf[2][kNH][2];  // B fragments for column steps 2kq, 2kq+1
+      if constexpr (kQSmem) {
+        const int chunk = 4 * kq + li;
 #pragma unroll
-      for (int j = 0; j < kST; ++j) {
-        const uint32_t addr = kbase + koff + (uint32_t)((8 * j + (lane & 7)) * 128);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(addr, b0, b1, b2, b3);
-        if constexpr (G16) {
-          mma_bf16_16816(s_acc[j], qa[2 * kq][0], qa[2 * kq][2], qa[2 * kq][1], qa[2 * kq][3],
-                         b0, b1);
-          mma_bf16_16816(s_acc[j], qa[2 * kq + 1][0], qa[2 * kq + 1][2], qa[2 * kq + 1][1],
-                         qa[2 * kq + 1][3], b2, b3);
-        } else {
-          mma_bf16_16816_top(s_acc[j][0], s_acc[j][1], qa[2 * kq][0], qa[2 * kq][1], b0, b1);
-          mma_bf16_16816_top(s_acc[j][0], s_acc[j][1], qa[2 * kq + 1][0], qa[2 * kq + 1][1], b2,
-                             b3);
+        for (int nh = 0; nh < kNH; ++nh) {
+          const int h = 8 * nh + (lane & 7);
+          const int pc = (chunk & ~7) | ((chunk & 7) ^ (lane & 7));
+          ldmatrix_x4(smem_addr(sm_q + h * (D * 2) + pc * 16), qf[0][nh][0], qf[0][nh][1],
+                      qf[1][nh][0], qf[1][nh][1]);
+        }
+      } else {
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            qf[x][nh][0] = qb[kQSmem ? 0 : 2 * kq + x][nh][0];
+            qf[x][nh][1] = qb[kQSmem ? 0 : 2 * kq + x][nh][1];
+          }
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int kk = 2 * kq + x;
+        const int chunk = 2 * kk + (li >> 1);
+        const uint32_t coff =
+            (uint32_t)((chunk >> 3) * kTileBytes + (((chunk & 7) ^ (lane & 7)) << 4));
+#pragma unroll
+        for (int tg = 0; tg < kTG; ++tg) {
+          const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(kbase + coff + (uint32_t)(tok * 128), a0, a1, a2, a3);
+#pragma unroll
+          for (int nh = 0; nh < kNH; ++nh)
+            mma_bf16_16816(x ? s_odd[tg][nh] : s_acc[tg][nh], a0, a1, a2, a3, qf[x][nh][0],
+                           qf[x][nh][1]);
         }
       }
     }
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg)
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s_acc[tg][nh][e] += s_odd[tg][nh][e];
 
-    // ---- online softmax (log2 domain); masked tokens are selected out
-    float mx[2] = {-INFINITY, -INFINITY};
+    // ---- online softmax per head (log2 domain); masked tokens are selected out
+    float mx[kNH][2];
 #pragma unroll
-    for (int j = 0; j < kST; ++j)
+    for (int nh = 0; nh < kNH; ++nh) mx[nh][0] = mx[nh][1] = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < (G16 ? 4 : 2); ++e) {
-        const int tok = 8 * j + cq + (e & 1);
-        const float x = tok < valid ? s_acc[j][e] * p.scale_log2 : -INFINITY;
-        s_acc[j][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    float alpha[2];
+    for (int tg = 0; tg < kTG; ++tg)
 #pragma unroll
-    for (int h = 0; h < (G16 ? 2 : 1); ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-      const float m_new = fmaxf(m_run[h], mx[h]);
-      alpha[h] = fast_exp2(m_run[h] - m_new);
-      m_run[h] = m_new;
-    }
-    uint32_t pk[kST][2];  // P as packed bf16 pairs: [tile][row half]
-    float psum[2] = {0.f, 0.f};
+      for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
-    for (int j = 0; j < kST; ++j)
-#pragma unroll
-      for (int h = 0; h < (G16 ? 2 : 1); ++h) {
-        const float e0 = fast_exp2(s_acc[j][2 * h] - m_run[h]);
-        const float e1 = fast_exp2(s_acc[j][2 * h + 1] - m_run[h]);
-        const uint32_t pr = pack_bf16x2(e0, e1);
-        pk[j][h] = pr;
-        psum[h] += bf16lo_to_f32(pr) + bf16hi_to_f32(pr);
-      }
-#pragma unroll
-    for (int h = 0; h < (G16 ? 2 : 1); ++h) l_run[h] = l_run[h] * alpha[h] + psum[h];
-    const bool rescale = G16 ? __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)
-                             : __any_sync(0xffffffffu, alpha[0] != 1.f);
-    if (rescale) {
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        o_acc[nt][0] *= alpha[0];
-        o_acc[nt][1] *= alpha[0];
-        if constexpr (G16) {
-          o_acc[nt][2] *= alpha[1];
-          o_acc[nt][3] *= alpha[1];
+        for (int e = 0; e < 4; ++e) {
+          const int tok = 16 * tg + row + ((e >> 1) << 3);
+          const float x = tok < valid ? s_acc[tg][nh][e] * p.scale_log2 : -INFINITY;
+          s_acc[tg][nh][e] = x;
+          mx[nh][e & 1] = fmaxf(mx[nh][e & 1], x);
         }
+    float alpha[kNH][2];
+    bool changed = false;
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = mx[nh][e];
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const float m_new = fmaxf(m_run[nh][e], v);
+        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_new);
+        changed |= m_new != m_run[nh][e];
+        m_run[nh][e] = m_new;
       }
+    uint32_t pb0[kTG][kNH], pb1[kTG][kNH];  // B operand P^T (tokens 0-7 / 8-15 of a group)
+    float psum[kNH][2];
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) psum[nh][0] = psum[nh][1] = 0.f;
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg)
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh) {
+        const float e0 = fast_exp2(s_acc[tg][nh][0] - m_run[nh][0]);
+        const float e1 = fast_exp2(s_acc[tg][nh][1] - m_run[nh][1]);
+        const float e2 = fast_exp2(s_acc[tg][nh][2] - m_run[nh][0]);
+        const float e3 = fast_exp2(s_acc[tg][nh][3] - m_run[nh][1]);
+        const uint32_t lo = pack_bf16x2(e0, e1);  // tokens row,   heads 2q, 2q+1
+        const uint32_t hi = pack_bf16x2(e2, e3);  // tokens row+8, heads 2q, 2q+1
+        psum[nh][0] += bf16lo_to_f32(lo) + bf16lo_to_f32(hi);
+        psum[nh][1] += bf16hi_to_f32(lo) + bf16hi_to_f32(hi);
+        pb0[tg][nh] = movmatrix_trans(lo);  // tokens 2q, 2q+1 of head `row`
+        pb1[tg][nh] = movmatrix_trans(hi);
+      }
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) l_run[nh][e] = l_run[nh][e] * alpha[nh][e] + psum[nh][e];
+    if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt)
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o_acc[dt][nh][e] *= alpha[nh][e & 1];
     }
 
-    // ---- O += P V: B operand from V rows (tokens) with a transposing ldmatrix
+    // ---- O^T += V^T P^T: A operand = 16 columns x 16 tokens via transposing ldmatrix
     const bool tail = valid < BS;
 #pragma unroll
-    for (int jj = 0; jj < BS / 16; ++jj) {
-      const uint32_t a0 = pk[2 * jj][0];
-      const uint32_t a2 = pk[2 * jj + 1][0];
-      const uint32_t a1 = G16 ? pk[2 * jj][1] : 0u;
-      const uint32_t a3 = G16 ? pk[2 * jj + 1][1] : 0u;
-      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+    for (int tg = 0; tg < kTG; ++tg) {
+      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
       if (tail) {  // rows past the sequence may hold anything: zero them in the fragment
-        const int t0 = 16 * jj + cq;
-        vmask_lo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-        vmask_hi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+        const int t0 = 16 * tg + 2 * quad;
+        mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+        mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
       }
-      const int i = lane >> 3;
-      const int trow = 16 * jj + (lane & 7) + ((i & 1) << 3);
+      const int tok = 16 * tg + (lane & 7) + ((li >> 1) << 3);
 #pragma unroll
-      for (int n2 = 0; n2 < D / 16; ++n2) {
-        const int chunk = 2 * n2 + (i >> 1);
-        const uint32_t addr = vbase + (uint32_t)((chunk >> 3) * kTileBytes + trow * 128 +
+      for (int dt = 0; dt < kDT; ++dt) {
+        const int chunk = 2 * dt + (li & 1);
+        const uint32_t addr = vbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
                                                  (((chunk & 7) ^ (lane & 7)) << 4));
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-        b0 &= vmask_lo;
-        b1 &= vmask_hi;
-        b2 &= vmask_lo;
-        b3 &= vmask_hi;
-        if constexpr (G16) {
-          mma_bf16_16816(o_acc[2 * n2], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(o_acc[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
-        } else {
-          mma_bf16_16816_top(o_acc[2 * n2][0], o_acc[2 * n2][1], a0, a2, b0, b1);
-          mma_bf16_16816_top(o_acc[2 * n2 + 1][0], o_acc[2 * n2 + 1][1], a0, a2, b2, b3);
-        }
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        a0 &= mlo;
+        a1 &= mlo;
+        a2 &= mhi;
+        a3 &= mhi;
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh)
+          mma_bf16_16816(o_acc[dt][nh], a0, a1, a2, a3, pb0[tg][nh], pb1[tg][nh]);
       }
     }
   };
 
-  // Merge the consumer warps' states for (s, g) and emit the output row block
+  // Merge the consumer warps' states for (s, g) and emit the output rows
   // (whole piece) or a partial state (split piece; the last piece combines).
   auto finish_piece = [&](int s, int g, long long sb, long long se) {
     const bool split = sb < u0 || se > u1;
 #pragma unroll
-    for (int h = 0; h < (G16 ? 2 : 1); ++h) {
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-    }
-    if ((lane & 3) == 0) {
-      sm_m[warp * 16 + r0] = m_run[0];
-      sm_l[warp * 16 + r0] = l_run[0];
-      if constexpr (G16) {
-        sm_m[warp * 16 + r0 + 8] = m_run[1];
-        sm_l[warp * 16 + r0 + 8] = l_run[1];
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = l_run[nh][e];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l_run[nh][e] = v;
       }
+    if (row == 0) {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 8 * nh + 2 * quad + e;
+          sm_m[warp * 16 + h] = m_run[nh][e];
+          sm_l[warp * 16 + h] = l_run[nh][e];
+        }
     }
+    __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
+    float f[kNH][2];
 #pragma unroll
-    for (int h = 0; h < (G16 ? 2 : 1); ++h) {
-      const int r = r0 + 8 * h;
-      float M = -INFINITY;
+    for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 16 + r]);
-      float Lsum = 0.f;
+      for (int e = 0; e < 2; ++e) {
+        const int h = 8 * nh + 2 * quad + e;
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = sm_m[w * 16 + r];
-        if (mw != -INFINITY) Lsum += sm_l[w * 16 + r] * fast_exp2(mw - M);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 16 + h]);
+        float Lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = sm_m[w * 16 + h];
+          if (mw != -INFINITY) Lsum += sm_l[w * 16 + h] * fast_exp2(mw - M);
+        }
+        f[nh][e] = m_run[nh][e] == -INFINITY ? 0.f : fast_exp2(m_run[nh][e] - M);
+        if (warp == 0 && row == 0) {
+          sm_final[h] = M;
+          sm_final[16 + h] = Lsum;
+        }
       }
-      const float f = m_run[h] == -INFINITY ? 0.f : fast_exp2(m_run[h] - M);
-      if (r < G) {
-        float* row = sm_o + (warp * G + r) * kRowStride + cq;
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          *reinterpret_cast<float2*>(row + 8 * nt) =
-              make_float2(o_acc[nt][2 * h] * f, o_acc[nt][2 * h + 1] * f);
-      }
-      if (warp == 0 && (lane & 3) == 0) {
-        sm_final[r] = M;
-        sm_final[16 + r] = Lsum;
-      }
-    }
+    for (int dt = 0; dt < kDT; ++dt)
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = 8 * nh + 2 * quad + (e & 1);
+          const int d = 16 * dt + row + ((e >> 1) << 3);
+          if (h < G) sm_o[(warp * G + h) * kRowStride + d] = o_acc[dt][nh][e] * f[nh][e & 1];
+        }
+    __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
 
     const long long C_ = C;
@@ -529,13 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D + d) =
             pack_bf16x2(acc.x * inv, acc.y * inv);
       } else {
-        float* row = mine + r * kPartialRow;
-        *reinterpret_cast<float2*>(row + 4 + d) = acc;
-        if (d == 0) *reinterpret_cast<float2*>(row) = make_float2(sm_final[r], sm_final[16 + r]);
+        float* prow = mine + r * kPartialRow;
+        *reinterpret_cast<float2*>(prow + 4 + d) = acc;
+        if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(sm_final[r], sm_final[16 + r]);
       }
     }
     if (split) {
       __threadfence();
+      __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
       const int c_first = cta_of(sb, W, C_);
       const int c_last = cta_of(se - 1, W, C_);
@@ -545,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int old = atomicAdd(p.counters + c_first, 1);
         *sm_flag = (old == c_last - c_first) ? 1 : 0;
       }
+      __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
       if (*sm_flag) {
         __threadfence();
@@ -559,9 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           float den = 0.f, nx = 0.f, ny = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
             const int slot = 2 * c + (sb <= range_begin(c, W, C_) ? 0 : 1);
-            const float* row = p.partials + ((size_t)slot * G + r) * kPartialRow;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(row));
-            const float2 o = __ldcg(reinterpret_cast<const float2*>(row + 4 + d));
+            const float* prow = p.partials + ((size_t)slot * G + r) * kPartialRow;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(prow));
+            const float2 o = __ldcg(reinterpret_cast<const float2*>(prow + 4 + d));
             const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
             den += wgt * ml.y;
             nx += wgt * o.x;
@@ -574,12 +658,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ctid == 0) p.counters[c_first] = 0;  // ready for the next call
       }
     }
+    __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
   };
 
   Walker wk;
   wk.start(u0, sm_prefix, N, H_kv);
   load_q(wk.s, wk.g);
+  if constexpr (kQSmem) {
+    __syncwarp();
+    named_barrier(kConsumerBarrier, kConsumerThreads);
+  }
   reset();
   int stage = 0;
   uint32_t phase = 0;
@@ -587,7 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool abort = false;
   for (long long u = u0; u < u1; ++u) {
     if (owner == warp && !abort) {
-      if (!mbar_wait(&full_bar[stage], phase)) {
+      // Lanes poll the barrier independently; the vote both reconverges the warp
+      // before the warp-collective ldmatrix / movmatrix / mma and makes the
+      // outcome uniform.
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase));
+      if (!ready) {
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
         abort = true;
       } else {
@@ -610,7 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
       finish_piece(s, g, sb, sb + n);
       if (!last) {
-        load_q(wk.s, wk.g);
+        load_q(wk.s, wk.g);  // finish_piece ended on a consumer barrier: the tile is free
+        if constexpr (kQSmem) {
+          __syncwarp();
+          named_barrier(kConsumerBarrier, kConsumerThreads);
+        }
         reset();
       }
     }

@@ -44,7 +44,8 @@ int validate_sizes(int num_seqs, int H_q, int H_kv, int head_dim, int max_blocks
 
 struct DeviceInfo {
   int sms = 0;
-  int max_smem = 0;  // opt-in dynamic shared memory per block
+  int max_smem = 0;     // opt-in dynamic shared memory per block
+  int smem_per_sm = 0;  // shared memory per multiprocessor
 };
 
 struct OwnedWorkspace {
@@ -72,6 +73,9 @@ int device_info(DeviceInfo* out) {
   if ((e = cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
       cudaSuccess)
     return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                  dev)) != cudaSuccess)
+    return cuda_fail(e);
   g_info[dev] = di;
   *out = di;
   return PAGED_ATTN_OK;
@@ -96,7 +100,11 @@ bool plan_smem(int G, int chunk, int max_smem, int* stages, size_t* smem) {
   const long long per_stage = L::kStageBytes + 16;
   long long st = (max_smem - fixed) / per_stage;
   if (st > kMaxStages) st = kMaxStages;
-  if (st < 2) return false;
+  // Ring slot i % stages is consumed by warp i % kConsumerWarps; a multiple keeps
+  // every slot with one warp, so its uses are waited on strictly in order (an
+  // mbarrier parity wait cannot tell phase k from phase k - 2).
+  st -= st % kConsumerWarps;
+  if (st < kConsumerWarps) return false;
   const L lay{(int)st, G, chunk};
   *stages = (int)st;
   *smem = (size_t)lay.total() + 1024;
@@ -117,16 +125,29 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
   pl->BS = BS;
   pl->G = H_q / H_kv;
   pl->g16 = pl->G > 8;
-  pl->grid = di.sms;
-  int chunk = num_seqs < kMaxSeqsPerLaunch ? (num_seqs > 0 ? num_seqs : 1) : kMaxSeqsPerLaunch;
-  // keep at least 4 pipeline stages where possible by launching fewer sequences at a time
-  for (;;) {
-    if (plan_smem_any(D, BS, pl->G, chunk, di.max_smem, &pl->stages, &pl->smem) &&
-        (pl->stages >= 4 || chunk <= 64))
-      break;
-    if (chunk <= 1) return PAGED_ATTN_ERR_SIZES;
-    chunk = (chunk + 1) / 2;
+  const int chunk0 =
+      num_seqs < kMaxSeqsPerLaunch ? (num_seqs > 0 ? num_seqs : 1) : kMaxSeqsPerLaunch;
+  // Two CTAs per SM (two independent pipelines) when their shared memory fits,
+  // else one.  Keep at least 4 pipeline stages where possible by launching
+  // fewer sequences at a time.
+  bool ok = false;
+  int chunk = chunk0;
+  for (int occ = ctas_per_sm(D, pl->g16); occ >= 1 && !ok; --occ) {
+    int budget = di.smem_per_sm / occ - 1024;  // 1 KB per CTA is reserved by the system
+    if (budget > di.max_smem) budget = di.max_smem;
+    chunk = chunk0;
+    for (;;) {
+      if (plan_smem_any(D, BS, pl->G, chunk, budget, &pl->stages, &pl->smem) &&
+          (pl->stages >= 4 || chunk <= 64)) {
+        ok = true;
+        pl->grid = di.sms * occ;
+        break;
+      }
+      if (chunk <= 1) break;
+      chunk = (chunk + 1) / 2;
+    }
   }
+  if (!ok) return PAGED_ATTN_ERR_SIZES;
   pl->chunk = chunk;
   // [0, 256): status word; then one combine counter per CTA; then the partial
   // states.  The counter region depends on the device only, so a workspace
@@ -162,28 +183,30 @@ int get_encoder(EncodeTiledFn* fn) {
   return PAGED_ATTN_OK;
 }
 
-// 3-D view of a cache: (column, row within a block = kv_head * BS + slot, block id).
-// A page of one KV head is the box {64, BS, 1} at (64 * half, g * BS, block);
-// 128-byte swizzle matches the ldmatrix addressing in the kernel.
+// 4-D view of a cache: (column within a 64-column half, row within a block =
+// kv_head * BS + slot, half, block id).  A page of one KV head is the box
+// {64, BS, D / 64, 1} at (0, g * BS, 0, block); it lands in shared memory as
+// [half][row][128 bytes] with the 128-byte swizzle the kernel's ldmatrix
+// addressing expects.
 int encode_cache_map(const void* base, int D, int BS, int H_kv, long long num_blocks,
                      CUtensorMap* map) {
   EncodeTiledFn enc = nullptr;
   int rc = get_encoder(&enc);
   if (rc != PAGED_ATTN_OK) return rc;
-  const cuuint64_t stride1 = (cuuint64_t)D * 2;
-  const cuuint64_t stride2 = stride1 * (cuuint64_t)H_kv * BS;
+  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  const cuuint64_t block_bytes = row_bytes * (cuuint64_t)H_kv * BS;
   cuuint64_t nb = (cuuint64_t)num_blocks;
   if (num_blocks <= 0) {
     // pool size unknown: any non-negative int32 block id is addressable, as long
     // as the described extent stays below 2^40 bytes
-    nb = ((cuuint64_t)1 << 40) / stride2;
+    nb = ((cuuint64_t)1 << 40) / block_bytes;
     if (nb > 0x7fffffffULL) nb = 0x7fffffffULL;
   }
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv * BS, nb};
-  const cuuint64_t strides[2] = {stride1, stride2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)BS, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  const cuuint64_t dims[4] = {64, (cuuint64_t)H_kv * BS, (cuuint64_t)D / 64, nb};
+  const cuuint64_t strides[3] = {row_bytes, 128, block_bytes};
+  const cuuint32_t box[4] = {64, (cuuint32_t)BS, (cuuint32_t)D / 64, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail((int)r);
