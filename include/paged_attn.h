@@ -64,6 +64,7 @@ extern "C" {
 #define PAGED_ATTN_ERR_CUDA (-6)       /* a CUDA runtime/driver call failed; see paged_attn_last_cuda_error */
 #define PAGED_ATTN_ERR_WORKSPACE (-7)  /* workspace pointer null/misaligned or smaller than required */
 #define PAGED_ATTN_ERR_SCALE (-8)      /* scale is not finite */
+#define PAGED_ATTN_ERR_STATIC_SCRATCH (-9) /* sizes exceed paged_attn_decode_static's scratch */
 
 /*
  * Decode attention (the operation above).
@@ -118,6 +119,33 @@ int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_
                               int num_seqs, int H_q, int H_kv, int head_dim,
                               int max_blocks_per_seq, int block_size, float scale,
                               long long num_blocks, int32_t* d_status, void* stream);
+
+/*
+ * Same operation for callers that cannot allocate device memory.  There is no
+ * counterpart in the reference pages; this entry point exists for callers whose
+ * host framework owns all device memory -- a serving engine that reserves the
+ * whole HBM for its KV-cache pool, or a plugin host that forbids allocation --
+ * and for decode loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  It calls no cudaMalloc, cudaFree or allocating library
+ * routine: its scratch (split-KV partial states and combine counters) is a
+ * fixed 4 MiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.  Sizes whose scratch would exceed
+ * 4 MiB (those for which paged_attn_workspace_bytes() reports more) return
+ * PAGED_ATTN_ERR_STATIC_SCRATCH before anything is launched; on a 152-SM
+ * GB300 that excludes head_dim 256 with G = 7 or 8 and head_dim 128 or 256
+ * with G >= 14, and admits every other supported shape.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it, so make that first call before any
+ * stream capture.  Every call clears the array's status and counter region
+ * on `stream` (a memset, not an allocation) and then shares the array: calls
+ * that may overlap on the GPU (several streams, several host threads) race
+ * on it and must be serialised by the caller.
+ */
+int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
+                             const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                             int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                             int block_size, float scale, void* stream);
 
 /* Human-readable text for a PAGED_ATTN_* code (static storage). */
 const char* paged_attn_status_string(int status);

@@ -20,6 +20,7 @@ __all__ = [
     "paged_attn_decode",
     "paged_attn_decode_ws",
     "paged_attn_decode_checked",
+    "paged_attn_decode_static",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "EXPORTED_SYMBOLS",
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "paged_attn_workspace_bytes",
     "paged_attn_decode_ws",
     "paged_attn_decode_checked",
+    "paged_attn_decode_static",
     "paged_attn_status_string",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
@@ -72,6 +74,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_decode_ws.restype = I
         lib.paged_attn_decode_checked.argtypes = common + [LL, P, P]
         lib.paged_attn_decode_checked.restype = I
+        lib.paged_attn_decode_static.argtypes = common + [P]
+        lib.paged_attn_decode_static.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -170,4 +174,19 @@ def paged_attn_decode_checked(q, k_cache, v_cache, block_tables, seq_lens, scale
     _check(load().paged_attn_decode_checked(*_args(q, k_cache, v_cache, out, block_tables,
                                                    seq_lens, scale), nb, _ptr(status),
                                             _stream(stream)))
+    return out
+
+
+def paged_attn_decode_static(q, k_cache, v_cache, block_tables, seq_lens, scale: float,
+                             out=None, stream=None):
+    """As paged_attn_decode, for callers that must not allocate device memory: the
+    library's fixed 4 MiB scratch array stands in for the workspace (see paged_attn.h;
+    calls that overlap on the GPU race on that array).  ``out`` should be passed in by
+    such callers, since creating it here would allocate."""
+    import torch
+
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().paged_attn_decode_static(*_args(q, k_cache, v_cache, out, block_tables,
+                                                  seq_lens, scale), _stream(stream)))
     return out

@@ -291,6 +291,32 @@ int owned_workspace(size_t bytes, cudaStream_t stream, void** out) {
   return PAGED_ATTN_OK;
 }
 
+// Scratch for paged_attn_decode_static: a fixed array every GPU that loads the
+// library holds until the process exits, so that entry point never allocates.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::unordered_map<int, void*> g_static_scratch_ptr;  // device -> address of the array
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (in host code the array's name is only a stand-in, not an address).
+int static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_static_scratch_ptr.find(dev);
+  if (it != g_static_scratch_ptr.end()) {
+    *out = it->second;
+    return PAGED_ATTN_OK;
+  }
+  void* ptr = nullptr;
+  if ((e = cudaGetSymbolAddress(&ptr, g_static_scratch)) != cudaSuccess) return cuda_fail(e);
+  g_static_scratch_ptr[dev] = ptr;
+  *out = ptr;
+  return PAGED_ATTN_OK;
+}
+
 int common_checks(const void* q, const void* k, const void* v, const void* out, const int32_t* bt,
                   const int32_t* sl, int num_seqs, int H_q, int H_kv, int head_dim,
                   int max_blocks_per_seq, int block_size, float scale) {
@@ -381,6 +407,30 @@ int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_
              max_blocks_per_seq, scale, ws, d_status, num_blocks, st);
 }
 
+int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
+                             const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                             int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                             int block_size, float scale, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  if (pl.ws_bytes > kStaticScratchBytes) return PAGED_ATTN_ERR_STATIC_SCRATCH;
+  void* ws = nullptr;
+  if ((rc = static_scratch_address(&ws)) != PAGED_ATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps whatever the previous call left; the status word and the
+  // combine counters must start at zero.
+  cudaError_t e = cudaMemsetAsync(ws, 0, pl.off_partials, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
 const char* paged_attn_status_string(int status) {
   switch (status) {
     case PAGED_ATTN_OK: return "ok";
@@ -392,6 +442,8 @@ const char* paged_attn_status_string(int status) {
     case PAGED_ATTN_ERR_CUDA: return "CUDA call failed (see paged_attn_last_cuda_error)";
     case PAGED_ATTN_ERR_WORKSPACE: return "workspace null, misaligned or too small";
     case PAGED_ATTN_ERR_SCALE: return "scale is not finite";
+    case PAGED_ATTN_ERR_STATIC_SCRATCH:
+      return "sizes need more scratch than paged_attn_decode_static's fixed 4 MiB array";
     default: return "unknown status";
   }
 }
