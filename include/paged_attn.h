@@ -131,9 +131,9 @@ int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_
  * fixed 4 MiB array compiled into the library, which every GPU that loads the
  * library holds until the process exits.  Sizes whose scratch would exceed
  * 4 MiB (those for which paged_attn_workspace_bytes() reports more) return
- * PAGED_ATTN_ERR_STATIC_SCRATCH before anything is launched; on a 152-SM
- * GB300 that excludes head_dim 256 with G = 7 or 8 and head_dim 128 or 256
- * with G >= 14, and admits every other supported shape.
+ * PAGED_ATTN_ERR_STATIC_SCRATCH before anything is launched (on a 152-SM
+ * GB300 that is, for instance, head_dim 128 with 16 query heads per KV head;
+ * the LLaMA-3-8B-, Qwen- and GQA-8-shaped decode batches all fit).
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it, so make that first call before any

@@ -57,9 +57,6 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 __host__ __device__ constexpr int ctas_per_sm(int D, bool g16) {
   return (D >= 256 && g16) ? 1 : 2;
 }
-// The query group is kept in shared memory (read per page with ldmatrix)
-// where holding it in registers would push the kernel past its register budget.
-__host__ __device__ constexpr bool q_in_smem(int D, bool g16) { return D >= 256 || g16; }
 constexpr int kMinPagesPerCta = 8;
 constexpr int kMaxStages = 16;  // ring depth; always a multiple of kConsumerWarps
 constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
@@ -105,10 +102,10 @@ struct SmemLayout {
   __host__ __device__ int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   __host__ __device__ int flag() const { return final_ml() + 32 * 4; }
   __host__ __device__ int merge_o() const { return flag() + 16; }
-  __host__ __device__ int qtile() const {  // [16 heads][D] bf16, 16-byte chunks swizzled
+  __host__ __device__ int qtile() const {  // 2 x [16 heads][D] bf16, 16-byte chunks swizzled
     return merge_o() + kConsumerWarps * G * kRowStride * 4;
   }
-  __host__ __device__ int prefix() const { return qtile() + 16 * D * 2; }
+  __host__ __device__ int prefix() const { return qtile() + 2 * 16 * D * 2; }
   __host__ __device__ int lens() const { return prefix() + (num_seqs + 1) * 4; }
   __host__ __device__ int total() const { return lens() + num_seqs * 4; }
 };
@@ -167,8 +164,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   constexpr int kNH = G16 ? 2 : 1;    // n8 tiles of query heads
   constexpr int kDT = D / 16;         // 16-wide tiles of head_dim
   constexpr int kTG = BS / 16;        // 16-token groups per page
-  constexpr bool kQSmem = q_in_smem(D, G16);
-  constexpr int kQRegs = kQSmem ? 1 : kDT;  // register copy of Q^T (unused when in smem)
+  constexpr int kQTileBytes = 16 * D * 2;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -331,36 +327,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const int row = lane >> 2;
   const int ctid = tid;  // 0 .. kConsumerThreads-1
 
-  uint32_t qb[kQRegs][kNH][2];  // B operand Q^T of the query group (register variant)
   float o_acc[kDT][kNH][4];   // O^T accumulators
   float m_run[kNH][2];        // running max per owned head (log2 domain)
   float l_run[kNH][2];        // running sum per owned head (this lane's tokens)
 
-  // Query group of piece (s, g): registers, or the shared tile [head][chunk ^ (head % 8)].
-  // Callers hold the consumer barrier after a shared-tile load before any page.
-  auto load_q = [&](int s, int g) {
+  // The query group of a piece lives in one of two shared tiles
+  // [16 heads][D] (16-byte chunk c of head h at c ^ (h % 8) within each 128
+  // bytes; heads >= G are zero) and is fetched one piece ahead with cp.async.
+  auto prefetch_q = [&](int buf, int s, int g) {
     const __nv_bfloat16* qg = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
-    if constexpr (kQSmem) {
-      for (int i = ctid; i < 16 * (D / 8); i += kConsumerThreads) {
-        const int h = i / (D / 8);
-        const int c = i - h * (D / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (h < G) v = __ldg(reinterpret_cast<const uint4*>(qg + (size_t)h * D) + c);
-        const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
-        *reinterpret_cast<uint4*>(sm_q + h * (D * 2) + pc * 16) = v;
-      }
-    } else {
-#pragma unroll
-      for (int nh = 0; nh < kNH; ++nh) {
-        const int h = 8 * nh + row;
-        const uint32_t* qr = reinterpret_cast<const uint32_t*>(qg + (size_t)h * D + 2 * quad);
-#pragma unroll
-        for (int kk = 0; kk < kQRegs; ++kk) {
-          qb[kk][nh][0] = h < G ? __ldg(qr + 8 * kk) : 0u;
-          qb[kk][nh][1] = h < G ? __ldg(qr + 8 * kk + 4) : 0u;
-        }
-      }
+    uint8_t* tile = sm_q + buf * kQTileBytes;
+    for (int i = ctid; i < 16 * (D / 8); i += kConsumerThreads) {
+      const int h = i / (D / 8);
+      const int c = i - h * (D / 8);
+      const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
+      const bool live = h < G;
+      cp_async_16(tile + h * (D * 2) + pc * 16,
+                  live ? static_cast<const void*>(qg + (size_t)h * D + c * 8)
+                       : static_cast<const void*>(p.q),
+                  live ? 16 : 0);
     }
+    cp_async_commit();
   };
   auto reset = [&]() {
 #pragma unroll
@@ -379,9 +366,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   };
 
   // One page: S^T = K Q^T, online softmax, O^T += V^T P^T.
-  auto process_page = [&](const uint8_t* kt, const uint8_t* vt, int valid) {
+  auto process_page = [&](const uint8_t* kt, const uint8_t* vt, const uint8_t* qtile,
+                          int valid) {
     const uint32_t kbase = smem_addr(kt);
     const uint32_t vbase = smem_addr(vt);
+    const uint32_t qbase = smem_addr(qtile);
     const int li = lane >> 3;  // which 8x8 matrix this lane addresses in ldmatrix.x4
     // Two accumulator sets (even / odd 16-column steps) halve the dependent MMA chain.
     float s_acc[kTG][kNH][4], s_odd[kTG][kNH][4];
@@ -392,27 +381,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
         for (int e = 0; e < 4; ++e) s_acc[tg][nh][e] = s_odd[tg][nh][e] = 0.f;
 
-    // ---- S^T = K Q^T: A operand = 16 tokens x 16 columns of the swizzled K tile
+    // ---- S^T = K Q^T: A operand = 16 tokens x 16 columns of the swizzled K tile,
+    //      B operand Q^T from the query tile
 #pragma unroll
     for (int kq = 0; kq < kDT / 2; ++kq) {
       uint32_t qf[2][kNH][2];  // B fragments for column steps 2kq, 2kq+1
-      if constexpr (kQSmem) {
+      {
         const int chunk = 4 * kq + li;
-#pragma unroll
-        for (int nh = 0; nh < kNH; ++nh) {
-          const int h = 8 * nh + (lane & 7);
-          const int pc = (chunk & ~7) | ((chunk & 7) ^ (lane & 7));
-          ldmatrix_x4(smem_addr(sm_q + h * (D * 2) + pc * 16), qf[0][nh][0], qf[0][nh][1],
-                      qf[1][nh][0], qf[1][nh][1]);
-        }
-      } else {
+        const int pc = (chunk & ~7) | ((chunk & 7) ^ (lane & 7));
 #pragma unroll
         for (int nh = 0; nh < kNH; ++nh)
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            qf[x][nh][0] = qb[kQSmem ? 0 : 2 * kq + x][nh][0];
-            qf[x][nh][1] = qb[kQSmem ? 0 : 2 * kq + x][nh][1];
-          }
+          ldmatrix_x4(qbase + (uint32_t)((8 * nh + (lane & 7)) * (D * 2) + pc * 16),
+                      qf[0][nh][0], qf[0][nh][1], qf[1][nh][0], qf[1][nh][1]);
       }
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
@@ -530,6 +510,111 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
   };
 
+  // Partial state slot of CTA c for the split (s, g) whose units begin at sb.
+  auto slot_of = [&](int c, long long sb) -> int {
+    return 2 * c + (sb <= range_begin(c, W, C) ? 0 : 1);
+  };
+
+  // Last-arriving CTA of a split (s, g): merge the partials of CTAs c_first..c_last
+  // (BI-V100 design, section 2, Level 3) in CTA order and store the bf16 rows.
+  auto combine_split = [&](int s, int g, long long sb, int c_first, int c_last) {
+    // (1) row maxima and denominators: 8 threads per query head
+    {
+      const int r = ctid >> 3, t8 = ctid & 7;
+      float M = -INFINITY;
+      if (r < G)
+        for (int c = c_first + t8; c <= c_last; c += 8)
+          M = fmaxf(M, __ldcg(p.partials + ((size_t)slot_of(c, sb) * G + r) * kPartialRow));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+      float den = 0.f;
+      if (r < G)
+        for (int c = c_first + t8; c <= c_last; c += 8) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+              p.partials + ((size_t)slot_of(c, sb) * G + r) * kPartialRow));
+          if (ml.x != -INFINITY) den += fast_exp2(ml.x - M) * ml.y;
+        }
+      den += __shfl_xor_sync(0xffffffffu, den, 1);
+      den += __shfl_xor_sync(0xffffffffu, den, 2);
+      den += __shfl_xor_sync(0xffffffffu, den, 4);
+      if (t8 == 0 && r < G) {
+        sm_final[r] = M;
+        sm_final[16 + r] = den;
+      }
+    }
+    __syncwarp();
+    named_barrier(kConsumerBarrier, kConsumerThreads);
+    // (2) weighted sums, parts taken in chunks whose weights fit in the merge buffer
+    constexpr int kSlots = (8 * kNH * (D / 4) + kConsumerThreads - 1) / kConsumerThreads;
+    float4 acc[kSlots];
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float* wts = sm_o;                                          // [chunk][G] weights
+    const int cap = (kConsumerWarps * G * kRowStride) / (G + 1);
+    int* slots = reinterpret_cast<int*>(sm_o + cap * G);        // [chunk] slot ids
+    for (int cb = c_first; cb <= c_last; cb += cap) {
+      const int nc = min(cap, c_last + 1 - cb);
+      for (int i = ctid; i < nc * G; i += kConsumerThreads) {
+        const int c = cb + i / G, r = i % G;
+        const int sl = slot_of(c, sb);
+        const float m = __ldcg(p.partials + ((size_t)sl * G + r) * kPartialRow);
+        wts[i] = m == -INFINITY ? 0.f : fast_exp2(m - sm_final[r]);
+        if (r == 0) slots[i / G] = sl;
+      }
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k) {
+        const int v = ctid + k * kConsumerThreads;  // float4 index within [G][D/4]
+        if (v < G * (D / 4)) {
+          const int r = v / (D / 4), d4 = v - r * (D / 4);
+          int j = 0;
+          for (; j + 4 <= nc; j += 4) {  // four independent loads in flight
+            float4 o4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              o4[x] = __ldcg(reinterpret_cast<const float4*>(
+                  p.partials + ((size_t)slots[j + x] * G + r) * kPartialRow + 4 + 4 * d4));
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float wgt = wts[(j + x) * G + r];
+              acc[k].x += wgt * o4[x].x;
+              acc[k].y += wgt * o4[x].y;
+              acc[k].z += wgt * o4[x].z;
+              acc[k].w += wgt * o4[x].w;
+            }
+          }
+          for (; j < nc; ++j) {
+            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(
+                p.partials + ((size_t)slots[j] * G + r) * kPartialRow + 4 + 4 * d4));
+            const float wgt = wts[j * G + r];
+            acc[k].x += wgt * o4.x;
+            acc[k].y += wgt * o4.y;
+            acc[k].z += wgt * o4.z;
+            acc[k].w += wgt * o4.w;
+          }
+        }
+      }
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+    }
+    // (3) normalise and store
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      const int v = ctid + k * kConsumerThreads;
+      if (v < G * (D / 4)) {
+        const int r = v / (D / 4), d4 = v - r * (D / 4);
+        const float inv = 1.f / sm_final[16 + r];
+        uint2 packed;
+        packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+        packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<uint2*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D +
+                                  4 * d4) = packed;
+      }
+    }
+  };
+
   // Merge the consumer warps' states for (s, g) and emit the output rows
   // (whole piece) or a partial state (split piece; the last piece combines).
   auto finish_piece = [&](int s, int g, long long sb, long long se) {
@@ -590,29 +675,30 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
 
-    const long long C_ = C;
     float* mine = nullptr;
-    if (split) {
-      const int slot = 2 * blockIdx.x + (sb <= u0 ? 0 : 1);
-      mine = p.partials + (size_t)slot * G * kPartialRow;
-    }
-    for (int i = ctid; i < G * (D / 2); i += kConsumerThreads) {
-      const int r = i / (D / 2);
-      const int d = 2 * (i - r * (D / 2));
-      float2 acc = make_float2(0.f, 0.f);
+    if (split) mine = p.partials + (size_t)slot_of(blockIdx.x, sb) * G * kPartialRow;
+    for (int i = ctid; i < G * (D / 4); i += kConsumerThreads) {
+      const int r = i / (D / 4);
+      const int d = 4 * (i - r * (D / 4));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float2 v = *reinterpret_cast<const float2*>(sm_o + (w * G + r) * kRowStride + d);
+        const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * G + r) * kRowStride + d);
         acc.x += v.x;
         acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
       }
       if (!split) {
         const float inv = 1.f / sm_final[16 + r];
-        *reinterpret_cast<uint32_t*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D + d) =
-            pack_bf16x2(acc.x * inv, acc.y * inv);
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D + d) =
+            packed;
       } else {
         float* prow = mine + r * kPartialRow;
-        *reinterpret_cast<float2*>(prow + 4 + d) = acc;
+        *reinterpret_cast<float4*>(prow + 4 + d) = acc;
         if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(sm_final[r], sm_final[16 + r]);
       }
     }
@@ -620,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       __threadfence();
       __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
-      const int c_first = cta_of(sb, W, C_);
-      const int c_last = cta_of(se - 1, W, C_);
+      const int c_first = cta_of(sb, W, C);
+      const int c_last = cta_of(se - 1, W, C);
       if (ctid == 0) {
         // A split (s, g) is identified by the first CTA holding a piece of it: only
         // that CTA's last piece can run past its range, so the index is unique.
@@ -632,43 +718,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       named_barrier(kConsumerBarrier, kConsumerThreads);
       if (*sm_flag) {
         __threadfence();
-        for (int i = ctid; i < G * (D / 2); i += kConsumerThreads) {
-          const int r = i / (D / 2);
-          const int d = 2 * (i - r * (D / 2));
-          float M = -INFINITY;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int slot = 2 * c + (sb <= range_begin(c, W, C_) ? 0 : 1);
-            M = fmaxf(M, __ldcg(p.partials + ((size_t)slot * G + r) * kPartialRow));
-          }
-          float den = 0.f, nx = 0.f, ny = 0.f;
-          for (int c = c_first; c <= c_last; ++c) {
-            const int slot = 2 * c + (sb <= range_begin(c, W, C_) ? 0 : 1);
-            const float* prow = p.partials + ((size_t)slot * G + r) * kPartialRow;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(prow));
-            const float2 o = __ldcg(reinterpret_cast<const float2*>(prow + 4 + d));
-            const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-            den += wgt * ml.y;
-            nx += wgt * o.x;
-            ny += wgt * o.y;
-          }
-          const float inv = 1.f / den;
-          *reinterpret_cast<uint32_t*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D +
-                                       d) = pack_bf16x2(nx * inv, ny * inv);
-        }
+        combine_split(s, g, sb, c_first, c_last);
         if (ctid == 0) p.counters[c_first] = 0;  // ready for the next call
       }
     }
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
+  };
+
+  // Pieces of this CTA's range in order: (s, g) and where its units begin.
+  struct Piece {
+    int s, g;
+    long long sb;  // first unit of the whole (s, g)
+  };
+  auto next_piece = [&](Piece pc) -> Piece {
+    const int n = sm_prefix[pc.s + 1] - sm_prefix[pc.s];
+    if (++pc.g == H_kv) {
+      pc.g = 0;
+      do {
+        ++pc.s;
+      } while (pc.s < N && sm_prefix[pc.s + 1] == sm_prefix[pc.s]);
+    }
+    pc.sb = pc.s < N ? (long long)sm_prefix[pc.s] * H_kv +
+                           (long long)pc.g * (sm_prefix[pc.s + 1] - sm_prefix[pc.s])
+                     : pc.sb + n;
+    return pc;
   };
 
   Walker wk;
   wk.start(u0, sm_prefix, N, H_kv);
-  load_q(wk.s, wk.g);
-  if constexpr (kQSmem) {
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-  }
+  Piece ahead{wk.s, wk.g, 0};  // the next piece whose query group gets prefetched
+  int qbuf = 0;
+  prefetch_q(0, wk.s, wk.g);
+  ahead = next_piece(ahead);
+  cp_async_wait_all();
+  __syncwarp();
+  named_barrier(kConsumerBarrier, kConsumerThreads);
+  if (ahead.s < N && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
   reset();
   int stage = 0;
   uint32_t phase = 0;
@@ -686,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       } else {
         const int valid = min(BS, sm_len[wk.s] - wk.p * BS);
         const uint8_t* st = smem + stage * kStageBytes;
-        process_page(st, st + kPageBytes, valid);
+        process_page(st, st + kPageBytes, sm_q + qbuf * kQTileBytes, valid);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
       }
@@ -703,15 +787,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
       finish_piece(s, g, sb, sb + n);
       if (!last) {
-        load_q(wk.s, wk.g);  // finish_piece ended on a consumer barrier: the tile is free
-        if constexpr (kQSmem) {
-          __syncwarp();
-          named_barrier(kConsumerBarrier, kConsumerThreads);
-        }
+        // The next piece's query group was prefetched into the other tile: make
+        // every thread's copies visible, then prefetch the piece after it into
+        // the tile just freed.
+        cp_async_wait_all();
+        __syncwarp();
+        named_barrier(kConsumerBarrier, kConsumerThreads);
+        qbuf ^= 1;
+        ahead = next_piece(ahead);
+        if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
         reset();
       }
     }
   }
+  cp_async_wait_all();
 }
 
 }  // namespace pagedattn

@@ -48,7 +48,7 @@ def _c_call(lib, fn, w, out, stream):
         ctypes.c_float(w.scale), ctypes.c_void_p(stream.cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama8b", "qwen100k", "gqa8"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "qwen100k", "ragged256", "gqa8"])
 def test_static_scratch_matches_the_allocating_entry_point(lib, name):
     w = workloads.make(name, device="cuda", poison="nan")
     stream = torch.cuda.current_stream()
@@ -67,13 +67,23 @@ def test_static_scratch_matches_the_allocating_entry_point(lib, name):
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit(lib):
-    # head_dim 256 with 8 query heads per KV head needs about 5 MB of split-KV
-    # state on a 152-SM GB300, more than the fixed 4 MiB array.
-    sp = workloads.custom_spec("too_big", 4, 64, 8, 256, 16, [64] * 4)
+    # Find a supported shape whose split-KV state needs more than the 4 MiB array
+    # on this device (on a 152-SM GB300: head_dim 128 with 16 query heads per KV
+    # head), and check that the call is refused before anything is launched.
+    shape = None
+    for D in (128, 256, 64):
+        for G in (16, 12, 8):
+            need = lib.paged_attn_workspace_bytes(4, 2 * G, 2, D, 4, 16)
+            if need > 4 << 20:
+                shape = (D, G)
+                break
+        if shape:
+            break
+    if shape is None:
+        pytest.skip("every supported shape fits in 4 MiB on this device")
+    D, G = shape
+    sp = workloads.custom_spec("too_big", 4, 2 * G, 2, D, 16, [64] * 4)
     w = workloads.make(sp, seed=3, device="cuda")
-    need = lib.paged_attn_workspace_bytes(4, 64, 8, 256, w.block_tables.shape[1], 16)
-    if need <= 4 << 20:
-        pytest.skip("this device needs no more than 4 MiB for the case")
     out = torch.zeros_like(w.q)
     rc = _c_call(lib, "paged_attn_decode_static", w, out, torch.cuda.current_stream())
     assert rc == STATIC_SCRATCH_ERROR
