@@ -46,10 +46,10 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "smem_layout.h"
 
 namespace pagedattn {
 
-constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 // Two independent pipelines per SM; the one variant whose accumulators need the
@@ -84,30 +84,6 @@ struct DecodeParams {
   int32_t* counters;    // [gridDim.x], zero between calls (one per split piece's first CTA)
   float* partials;      // [gridDim.x * 2][G][D + 4]
   long long num_blocks; // > 0: checked mode (validate block ids against it)
-};
-
-// Shared-memory layout, in bytes from a 1024-aligned base.
-template <int D, int BS>
-struct SmemLayout {
-  static constexpr int kHalves = D / 64;              // 128-byte column halves of a row
-  static constexpr int kTileBytes = BS * 128;         // one half of one page
-  static constexpr int kPageBytes = kHalves * kTileBytes;
-  static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  static constexpr int kRowStride = D + 4;            // padded fp32 row in the merge buffer
-
-  int stages, G, num_seqs;
-  __host__ __device__ int bars() const { return stages * kStageBytes; }
-  __host__ __device__ int merge_m() const { return bars() + 2 * stages * 8; }
-  __host__ __device__ int merge_l() const { return merge_m() + kConsumerWarps * 16 * 4; }
-  __host__ __device__ int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
-  __host__ __device__ int flag() const { return final_ml() + 32 * 4; }
-  __host__ __device__ int merge_o() const { return flag() + 16; }
-  __host__ __device__ int qtile() const {  // 2 x [16 heads][D] bf16, 16-byte chunks swizzled
-    return merge_o() + kConsumerWarps * G * kRowStride * 4;
-  }
-  __host__ __device__ int prefix() const { return qtile() + 2 * 16 * D * 2; }
-  __host__ __device__ int lens() const { return prefix() + (num_seqs + 1) * 4; }
-  __host__ __device__ int total() const { return lens() + num_seqs * 4; }
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -164,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   constexpr int kNH = G16 ? 2 : 1;    // n8 tiles of query heads
   constexpr int kDT = D / 16;         // 16-wide tiles of head_dim
   constexpr int kTG = BS / 16;        // 16-token groups per page
-  constexpr int kQTileBytes = 16 * D * 2;
+  constexpr int kQTileBytes = L::kQTileBytes;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(

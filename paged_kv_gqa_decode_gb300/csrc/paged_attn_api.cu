@@ -108,7 +108,7 @@ bool plan_smem(int G, int chunk, int max_smem, int* stages, size_t* smem) {
   const L lay{(int)st, G, chunk};
   *stages = (int)st;
   *smem = (size_t)lay.total() + 1024;
-  return true;
+  return *smem + 256 <= (size_t)max_smem;  // + the kernel's static shared memory
 }
 
 bool plan_smem_any(int D, int BS, int G, int chunk, int max_smem, int* stages, size_t* smem) {

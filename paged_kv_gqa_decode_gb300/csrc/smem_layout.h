@@ -1,0 +1,48 @@
+// Shared-memory layout of the decode kernel, as plain C++ so the host plan, the
+// kernel and a host-only alignment check all use the same arithmetic.
+//
+// The pipeline ring starts the (1024-byte aligned) dynamic shared memory, as the
+// 128-byte TMA swizzle requires; every later region starts on a 128-byte
+// boundary, so mbarriers (8 bytes), ldmatrix rows and cp.async chunks (16) and
+// the float4 merge buffer (16) are aligned whatever the ring depth, the group
+// size or the batch.
+#pragma once
+
+#if defined(__CUDACC__)
+#define PAGEDATTN_HD __host__ __device__
+#else
+#define PAGEDATTN_HD
+#endif
+
+namespace pagedattn {
+
+constexpr int kConsumerWarps = 4;
+
+PAGEDATTN_HD constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int D, int BS>
+struct SmemLayout {
+  static constexpr int kHalves = D / 64;              // 128-byte column halves of a row
+  static constexpr int kTileBytes = BS * 128;         // one half of one page
+  static constexpr int kPageBytes = kHalves * kTileBytes;
+  static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
+  static constexpr int kQTileBytes = 16 * D * 2;      // query group, up to 16 heads
+  static constexpr int kRowStride = D + 4;            // padded fp32 row in the merge buffer
+
+  int stages, G, num_seqs;
+  // [0, bars): the ring of `stages` K/V pages; then full[stages], empty[stages]
+  PAGEDATTN_HD int bars() const { return stages * kStageBytes; }
+  PAGEDATTN_HD int merge_m() const { return align_up(bars() + 2 * stages * 8, 128); }
+  PAGEDATTN_HD int merge_l() const { return merge_m() + kConsumerWarps * 16 * 4; }
+  PAGEDATTN_HD int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
+  PAGEDATTN_HD int flag() const { return final_ml() + 32 * 4; }  // a few ints
+  PAGEDATTN_HD int merge_o() const { return flag() + 128; }
+  PAGEDATTN_HD int qtile() const {  // two query tiles
+    return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
+  }
+  PAGEDATTN_HD int prefix() const { return qtile() + 2 * kQTileBytes; }
+  PAGEDATTN_HD int lens() const { return prefix() + align_up((num_seqs + 1) * 4, 128); }
+  PAGEDATTN_HD int total() const { return lens() + num_seqs * 4; }
+};
+
+}  // namespace pagedattn
