@@ -55,6 +55,15 @@
 extern "C" {
 #endif
 
+/* Only the entry points below are exported from the shared library (it is built
+ * with hidden default visibility), so several copies of it -- say, two versions
+ * -- can live in one process without sharing any internal state. */
+#if defined(__GNUC__)
+#define PAGED_ATTN_API __attribute__((visibility("default")))
+#else
+#define PAGED_ATTN_API
+#endif
+
 #define PAGED_ATTN_OK 0
 #define PAGED_ATTN_ERR_POINTER (-1)    /* null or not 16-byte aligned pointer */
 #define PAGED_ATTN_ERR_HEADS (-2)      /* H_kv <= 0, H_q % H_kv != 0, or G > 16 */
@@ -76,7 +85,7 @@ extern "C" {
  * calls that may overlap on the GPU (different streams, same device) race:
  * give each concurrent stream its own workspace through paged_attn_decode_ws.
  */
-int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+PAGED_ATTN_API int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                       int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
                       float scale, void* stream);
@@ -86,7 +95,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
  * sizes on the CURRENT device (it depends on the device's SM count).  Returns 0
  * for unsupported sizes.
  */
-size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
+PAGED_ATTN_API size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
                                   int max_blocks_per_seq, int block_size);
 
 /*
@@ -98,7 +107,7 @@ size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
  * any later call on the same device that fits in it.  Calls sharing one
  * workspace must not overlap on the GPU.  Allocates nothing.
  */
-int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache, void* out,
+PAGED_ATTN_API int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache, void* out,
                          const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                          int H_q, int H_kv, int head_dim, int max_blocks_per_seq, int block_size,
                          float scale, void* workspace, size_t workspace_bytes, void* stream);
@@ -114,7 +123,7 @@ int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache
  * the kernel rejected its launch configuration (library faults, never
  * expected).  Uses the library-owned workspace like paged_attn_decode.
  */
-int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
+PAGED_ATTN_API int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
                               const int32_t* block_tables, const int32_t* seq_lens,
                               int num_seqs, int H_q, int H_kv, int head_dim,
                               int max_blocks_per_seq, int block_size, float scale,
@@ -142,19 +151,19 @@ int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_
  * that may overlap on the GPU (several streams, several host threads) race
  * on it and must be serialised by the caller.
  */
-int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
+PAGED_ATTN_API int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                              int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
                              int block_size, float scale, void* stream);
 
 /* Human-readable text for a PAGED_ATTN_* code (static storage). */
-const char* paged_attn_status_string(int status);
+PAGED_ATTN_API const char* paged_attn_status_string(int status);
 
 /* The last cudaError_t / CUresult value behind a PAGED_ATTN_ERR_CUDA on this thread. */
-int paged_attn_last_cuda_error(void);
+PAGED_ATTN_API int paged_attn_last_cuda_error(void);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
-int paged_attn_version(void);
+PAGED_ATTN_API int paged_attn_version(void);
 
 #ifdef __cplusplus
 }

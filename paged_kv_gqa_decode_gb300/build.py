@@ -32,7 +32,11 @@ def nvcc() -> str:
 
 
 def _flags():
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+    # hidden default visibility: only the C ABI (marked in paged_attn.h) is exported,
+    # so nothing internal (e.g. a template's static locals) is shared between two
+    # copies of the library loaded into one process
+    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler",
+                   "-fPIC,-O2,-fvisibility=hidden,-fvisibility-inlines-hidden",
                    "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", "-Xptxas", "-v"]
 
 

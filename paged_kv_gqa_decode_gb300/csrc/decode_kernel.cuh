@@ -61,6 +61,8 @@ constexpr int kMinPagesPerCta = 8;
 constexpr int kMaxStages = 16;  // ring depth; always a multiple of kConsumerWarps
 constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
 constexpr int kConsumerBarrier = 1;
+// Block tables up to this size are prefetched into L2 at kernel entry.
+constexpr size_t kBlockTablePrefetchBytes = size_t(4) << 20;
 
 // Status bits written to the workspace / caller status word.
 constexpr int kStatusBadBlock = 1;
@@ -116,6 +118,26 @@ struct Walker {
     } while (s < N && prefix[s + 1] == prefix[s]);
     n = s < N ? prefix[s + 1] - prefix[s] : 0;
   }
+
+  // k units further on (the target unit must exist); one step per piece crossed.
+  __device__ void advance(int k, const int* prefix, int N, int H_kv) {
+    p += k;
+    while (p >= n) {
+      p -= n;
+      if (++g == H_kv) {
+        g = 0;
+        do {
+          ++s;
+        } while (s < N && prefix[s + 1] == prefix[s]);
+        if (s >= N) {
+          n = 0;
+          p = 0;
+          return;
+        }
+        n = prefix[s + 1] - prefix[s];
+      }
+    }
+  }
 };
 
 // The CTA whose range contains unit u, for ranges [floor(c W / C), floor((c+1) W / C)).
@@ -148,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const L lay{p.stages, p.G, p.num_seqs};
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
+  uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
   float* sm_m = reinterpret_cast<float*>(smem + lay.merge_m());
   float* sm_l = reinterpret_cast<float*>(smem + lay.merge_l());
   float* sm_final = reinterpret_cast<float*>(smem + lay.final_ml());  // [0,16) M, [16,32) L
@@ -164,6 +187,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const int H_kv = p.H_kv;
   const int G = p.G;
   const int cap = p.maxb * BS;
+
+  // ---- 0. start the cold fetches that only depend on the arguments: the tensor
+  // maps (for the first tensor copy) and, spread over the grid, the block table
+  // (read right after the prefix below), so neither waits behind the lengths.
+  if (tid == kThreads - 32) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  {
+    const size_t bt_bytes = (size_t)N * p.maxb * sizeof(int32_t);
+    if (bt_bytes <= kBlockTablePrefetchBytes) {
+      const char* bt = reinterpret_cast<const char*>(p.block_tables);
+      for (size_t off = ((size_t)blockIdx.x * kThreads + tid) * 128; off < bt_bytes;
+           off += (size_t)gridDim.x * kThreads * 128)
+        prefetch_l2(bt + off);
+    }
+  }
 
   // ---- 1. clamped lengths and the exclusive prefix of pages per sequence
   {
@@ -226,16 +266,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
+    mbar_init(comb_bar, 1);
     fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == kConsumerWarps) {
     // =================================================================== producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
     const uint64_t policy = l2_evict_first_policy();
     // Lanes issue loads for consecutive units together; never more lanes than
     // stages, so the lanes of one wave always wait on distinct slots.
@@ -256,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
       if (ub + 32 + lane < u1) {
-        for (int k = 0; k < 32; ++k) wk.next(sm_prefix, N, H_kv);
+        wk.advance(32, sm_prefix, N, H_kv);
         nxt = fetch(ub + 32 + lane);
       }
       const int cnt = (int)min(32LL, u1 - ub);
@@ -302,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const int quad = lane & 3;
   const int row = lane >> 2;
   const int ctid = tid;  // 0 .. kConsumerThreads-1
+  bool abort = false;    // this warp gave up waiting for a page (status reports it)
+  int first_old = -1;    // thread 0: counter value its first piece's arrival saw
 
   float o_acc[kDT][kNH][4];   // O^T accumulators
   float m_run[kNH][2];        // running max per owned head (log2 domain)
@@ -486,113 +525,139 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
   };
 
-  // Partial state slot of CTA c for the split (s, g) whose units begin at sb.
-  auto slot_of = [&](int c, long long sb) -> int {
-    return 2 * c + (sb <= range_begin(c, W, C) ? 0 : 1);
+  // Partial state slot this CTA writes for a split piece beginning at sb: slot 0
+  // for its first piece (begun at or before u0), slot 1 for its last.
+  auto my_slot = [&](long long sb) -> int { return 2 * (int)blockIdx.x + (sb <= u0 ? 0 : 1); };
+
+  // A split (s, g): the CTAs c_first..c_last hold its pieces; c_first's piece
+  // sits in slot_first, every later CTA's in its slot 0 (its first piece).
+  struct Split {
+    int s, g, c_first, c_last, slot_first;
+  };
+  auto make_split = [&](int s, int g, long long sb, long long se) -> Split {
+    Split x;
+    x.s = s;
+    x.g = g;
+    x.c_first = cta_of(sb, W, C);
+    x.c_last = cta_of(se - 1, W, C);
+    x.slot_first = 2 * x.c_first + (sb == range_begin(x.c_first, W, C) ? 0 : 1);
+    return x;
   };
 
-  // Last-arriving CTA of a split (s, g): merge the partials of CTAs c_first..c_last
-  // (BI-V100 design, section 2, Level 3) in CTA order and store the bf16 rows.
-  auto combine_split = [&](int s, int g, long long sb, int c_first, int c_last) {
-    // (1) row maxima and denominators: 8 threads per query head
-    {
-      const int r = ctid >> 3, t8 = ctid & 7;
-      float M = -INFINITY;
-      if (r < G)
-        for (int c = c_first + t8; c <= c_last; c += 8)
-          M = fmaxf(M, __ldcg(p.partials + ((size_t)slot_of(c, sb) * G + r) * kPartialRow));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-      float den = 0.f;
-      if (r < G)
-        for (int c = c_first + t8; c <= c_last; c += 8) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-              p.partials + ((size_t)slot_of(c, sb) * G + r) * kPartialRow));
-          if (ml.x != -INFINITY) den += fast_exp2(ml.x - M) * ml.y;
-        }
-      den += __shfl_xor_sync(0xffffffffu, den, 1);
-      den += __shfl_xor_sync(0xffffffffu, den, 2);
-      den += __shfl_xor_sync(0xffffffffu, den, 4);
-      if (t8 == 0 && r < G) {
-        sm_final[r] = M;
-        sm_final[16 + r] = den;
+  // The combine (BI-V100 design, section 2, Level 3) run by the last CTA to
+  // arrive for a split: the partial states of c_first..c_last are merged in CTA
+  // order and the bf16 rows stored.  Partials are brought into the (now idle)
+  // pipeline ring with bulk copies, as many per round as the ring holds (the
+  // parts of both splits a CTA may combine share rounds), and folded in online
+  // by threads owning float4 slices of the output rows.
+  constexpr int kSlots = (8 * kNH * (D / 4) + kConsumerThreads - 1) / kConsumerThreads;
+  auto fold = [&](const float* parts, int nc, float4 (&acc)[kSlots], float (&m_acc)[kSlots],
+                  float (&l_acc)[kSlots]) {
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      const int v = ctid + k * kConsumerThreads;  // float4 index within [G][D/4]
+      if (v >= G * (D / 4)) continue;
+      const int r = v / (D / 4), d4 = v - r * (D / 4);
+      float m_new = m_acc[k];
+#pragma unroll 4
+      for (int j = 0; j < nc; ++j) m_new = fmaxf(m_new, parts[(j * G + r) * kPartialRow]);
+      if (m_new == -INFINITY) continue;
+      const float sc = m_acc[k] == -INFINITY ? 0.f : fast_exp2(m_acc[k] - m_new);
+      float4 a = make_float4(acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc);
+      float l = l_acc[k] * sc;
+#pragma unroll 4
+      for (int j = 0; j < nc; ++j) {
+        const float* prow = parts + (j * G + r) * kPartialRow;
+        const float2 ml = *reinterpret_cast<const float2*>(prow);
+        const float4 o4 = *reinterpret_cast<const float4*>(prow + 4 + 4 * d4);
+        const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - m_new);
+        a.x += wgt * o4.x;
+        a.y += wgt * o4.y;
+        a.z += wgt * o4.z;
+        a.w += wgt * o4.w;
+        l += wgt * ml.y;
       }
+      acc[k] = a;
+      l_acc[k] = l;
+      m_acc[k] = m_new;
     }
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-    // (2) weighted sums, parts taken in chunks whose weights fit in the merge buffer
-    constexpr int kSlots = (8 * kNH * (D / 4) + kConsumerThreads - 1) / kConsumerThreads;
-    float4 acc[kSlots];
-#pragma unroll
-    for (int k = 0; k < kSlots; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float* wts = sm_o;                                          // [chunk][G] weights
-    const int cap = (kConsumerWarps * G * kRowStride) / (G + 1);
-    int* slots = reinterpret_cast<int*>(sm_o + cap * G);        // [chunk] slot ids
-    for (int cb = c_first; cb <= c_last; cb += cap) {
-      const int nc = min(cap, c_last + 1 - cb);
-      for (int i = ctid; i < nc * G; i += kConsumerThreads) {
-        const int c = cb + i / G, r = i % G;
-        const int sl = slot_of(c, sb);
-        const float m = __ldcg(p.partials + ((size_t)sl * G + r) * kPartialRow);
-        wts[i] = m == -INFINITY ? 0.f : fast_exp2(m - sm_final[r]);
-        if (r == 0) slots[i / G] = sl;
-      }
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-#pragma unroll
-      for (int k = 0; k < kSlots; ++k) {
-        const int v = ctid + k * kConsumerThreads;  // float4 index within [G][D/4]
-        if (v < G * (D / 4)) {
-          const int r = v / (D / 4), d4 = v - r * (D / 4);
-          int j = 0;
-          for (; j + 4 <= nc; j += 4) {  // four independent loads in flight
-            float4 o4[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-              o4[x] = __ldcg(reinterpret_cast<const float4*>(
-                  p.partials + ((size_t)slots[j + x] * G + r) * kPartialRow + 4 + 4 * d4));
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float wgt = wts[(j + x) * G + r];
-              acc[k].x += wgt * o4[x].x;
-              acc[k].y += wgt * o4[x].y;
-              acc[k].z += wgt * o4[x].z;
-              acc[k].w += wgt * o4[x].w;
-            }
-          }
-          for (; j < nc; ++j) {
-            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(
-                p.partials + ((size_t)slots[j] * G + r) * kPartialRow + 4 + 4 * d4));
-            const float wgt = wts[j * G + r];
-            acc[k].x += wgt * o4.x;
-            acc[k].y += wgt * o4.y;
-            acc[k].z += wgt * o4.z;
-            acc[k].w += wgt * o4.w;
-          }
-        }
-      }
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-    }
-    // (3) normalise and store
+  };
+  auto store_rows = [&](const Split& x, const float4 (&acc)[kSlots], const float (&l_acc)[kSlots]) {
 #pragma unroll
     for (int k = 0; k < kSlots; ++k) {
       const int v = ctid + k * kConsumerThreads;
-      if (v < G * (D / 4)) {
-        const int r = v / (D / 4), d4 = v - r * (D / 4);
-        const float inv = 1.f / sm_final[16 + r];
-        uint2 packed;
-        packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
-        packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<uint2*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D +
-                                  4 * d4) = packed;
+      if (v >= G * (D / 4)) continue;
+      const int r = v / (D / 4), d4 = v - r * (D / 4);
+      const float inv = 1.f / l_acc[k];
+      uint2 packed;
+      packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+      packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+      *reinterpret_cast<uint2*>(p.out + ((size_t)x.s * p.H_q + (size_t)x.g * G + r) * D +
+                                4 * d4) = packed;
+    }
+  };
+  uint32_t comb_phase = 0;
+  auto combine = [&](const Split& x0, const Split& x1, int njobs) {
+    const int part_bytes = G * kPartialRow * 4;
+    const int per_round = (p.stages * kStageBytes) / part_bytes;  // >= 3 for ring >= 4 stages
+    if (per_round < 1) {
+      if (ctid == 0) atomicOr(p.status, kStatusConfig);
+      return;
+    }
+    const int n0 = x0.c_last - x0.c_first + 1;
+    const int total = n0 + (njobs > 1 ? x1.c_last - x1.c_first + 1 : 0);
+    float4 acc[kSlots];
+    float m_acc[kSlots], l_acc[kSlots];
+    auto reset_acc = [&]() {
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k) {
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        m_acc[k] = -INFINITY;
+        l_acc[k] = 0.f;
+      }
+    };
+    reset_acc();
+    for (int t0 = 0; t0 < total; t0 += per_round) {
+      const int nt = min(per_round, total - t0);
+      if (ctid == 0) {
+        fence_proxy_async_all();  // earlier reads of the ring; the acquired partials
+        mbar_arrive_expect_tx(comb_bar, (uint32_t)(nt * part_bytes));
+        for (int t = t0; t < t0 + nt; ++t) {
+          const Split& x = t < n0 ? x0 : x1;
+          const int c = x.c_first + (t < n0 ? t : t - n0);
+          const int slot = c == x.c_first ? x.slot_first : 2 * c;
+          bulk_load(smem + (t - t0) * part_bytes, p.partials + (size_t)slot * G * kPartialRow,
+                    (uint32_t)part_bytes, comb_bar);
+        }
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(comb_bar, comb_phase & 1u));
+      ++comb_phase;
+      // one verdict for all consumer warps, so they leave (or go on) together
+      if (named_barrier_or(kConsumerBarrier, kConsumerThreads, !ok)) {
+        if (ctid == 0) atomicOr(p.status, kStatusTimeout);
+        return;
+      }
+      for (int t = t0; t < t0 + nt;) {
+        const int job_end = t < n0 ? n0 : total;
+        const int cnt = min(t0 + nt, job_end) - t;
+        fold(reinterpret_cast<const float*>(smem + (t - t0) * part_bytes), cnt, acc, m_acc,
+             l_acc);
+        t += cnt;
+        if (t == job_end) {
+          store_rows(t == n0 ? x0 : x1, acc, l_acc);
+          reset_acc();
+        }
+      }
+      if (t0 + nt < total) {
+        __syncwarp();
+        named_barrier(kConsumerBarrier, kConsumerThreads);  // the ring may be refilled
       }
     }
   };
 
   // Merge the consumer warps' states for (s, g) and emit the output rows
-  // (whole piece) or a partial state (split piece; the last piece combines).
+  // (whole piece) or a partial state (split piece; its arrival comes at the end
+  // of the range).
   auto finish_piece = [&](int s, int g, long long sb, long long se) {
     const bool split = sb < u0 || se > u1;
 #pragma unroll
@@ -652,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     named_barrier(kConsumerBarrier, kConsumerThreads);
 
     float* mine = nullptr;
-    if (split) mine = p.partials + (size_t)slot_of(blockIdx.x, sb) * G * kPartialRow;
+    if (split) mine = p.partials + (size_t)my_slot(sb) * G * kPartialRow;
     for (int i = ctid; i < G * (D / 4); i += kConsumerThreads) {
       const int r = i / (D / 4);
       const int d = 4 * (i - r * (D / 4));
@@ -678,26 +743,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(sm_final[r], sm_final[16 + r]);
       }
     }
-    if (split) {
-      __threadfence();
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      const int c_first = cta_of(sb, W, C);
-      const int c_last = cta_of(se - 1, W, C);
-      if (ctid == 0) {
-        // A split (s, g) is identified by the first CTA holding a piece of it: only
-        // that CTA's last piece can run past its range, so the index is unique.
-        const int old = atomicAdd(p.counters + c_first, 1);
-        *sm_flag = (old == c_last - c_first) ? 1 : 0;
-      }
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      if (*sm_flag) {
-        __threadfence();
-        combine_split(s, g, sb, c_first, c_last);
-        if (ctid == 0) p.counters[c_first] = 0;  // ready for the next call
-      }
-    }
   };
 
   // Pieces of this CTA's range in order: (s, g) and where its units begin.
@@ -721,6 +766,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 
   Walker wk;
   wk.start(u0, sm_prefix, N, H_kv);
+  // the CTA's first piece (split when it began in an earlier CTA's range)
+  const int first_s = wk.s, first_g = wk.g;
+  const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
+  const long long first_se = first_sb + wk.n;
   Piece ahead{wk.s, wk.g, 0};  // the next piece whose query group gets prefetched
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
@@ -733,7 +782,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   int stage = 0;
   uint32_t phase = 0;
   int owner = 0;  // which consumer warp takes the current unit
-  bool abort = false;
   for (long long u = u0; u < u1; ++u) {
     if (owner == warp && !abort) {
       // Lanes poll the barrier independently; the vote both reconverges the warp
@@ -769,10 +817,50 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         cp_async_wait_all();
         __syncwarp();
         named_barrier(kConsumerBarrier, kConsumerThreads);
+        // A split piece that is not the range's last is its first: arrive on its
+        // counter now (the barrier above ordered every thread's partial stores
+        // before this release); the old value is read at the end of the range.
+        if (ctid == 0 && sb < u0) first_old = atom_add_release_gpu(p.counters + cta_of(sb, W, C), 1);
         qbuf ^= 1;
         ahead = next_piece(ahead);
         if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
         reset();
+      } else {
+        // Arrival for the last piece (if split) and, when this CTA arrived last
+        // for either split piece, the combine.  The barrier orders every
+        // thread's partial stores before thread 0's release.
+        const bool last_split = sb < u0 || sb + n > u1;
+        const bool first_pending = first_sb < u0 && first_sb != sb;
+        __syncwarp();
+        const bool failed = named_barrier_or(kConsumerBarrier, kConsumerThreads, abort);
+        if (!failed && (last_split || first_pending)) {
+          if (ctid == 0) {
+            bool cf = false, cl = false;
+            if (first_pending)
+              cf = first_old == cta_of(first_se - 1, W, C) - cta_of(first_sb, W, C);
+            if (last_split) {
+              const int c_first = cta_of(sb, W, C);
+              const int old = atom_add_acq_rel_gpu(p.counters + c_first, 1);
+              cl = old == cta_of(sb + n - 1, W, C) - c_first;
+            }
+            // the first piece's counter was read with a release-only add: acquire now
+            if (cf) fence_acq_rel_gpu();
+            sm_flag[0] = cf ? 1 : 0;
+            sm_flag[1] = cl ? 1 : 0;
+          }
+          __syncwarp();
+          named_barrier(kConsumerBarrier, kConsumerThreads);
+          const bool cf = sm_flag[0] != 0, cl = sm_flag[1] != 0;
+          if (cf || cl) {
+            const Split xf = make_split(first_s, first_g, first_sb, first_se);
+            const Split xl = make_split(s, g, sb, sb + n);
+            combine(cf ? xf : xl, xl, cf && cl ? 2 : 1);
+            if (ctid == 0) {  // ready for the next call
+              if (cf) p.counters[xf.c_first] = 0;
+              if (cl) p.counters[xl.c_first] = 0;
+            }
+          }
+        }
       }
     }
   }

@@ -5,7 +5,6 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
-#include <unordered_map>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -53,18 +52,28 @@ struct OwnedWorkspace {
   size_t bytes = 0;
 };
 
+// Per-device state, indexed by device ordinal (guarded by g_mu).
+constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-std::unordered_map<int, DeviceInfo> g_info;
-std::unordered_map<int, OwnedWorkspace> g_ws;
+DeviceInfo g_info[kMaxDevices];
+OwnedWorkspace g_ws[kMaxDevices];
+void* g_static_scratch_ptr[kMaxDevices];  // address of the static scratch array
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (*dev < 0 || *dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+  return PAGED_ATTN_OK;
+}
 
 int device_info(DeviceInfo* out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
+  int rc = current_device(&dev);
+  if (rc != PAGED_ATTN_OK) return rc;
+  cudaError_t e;
   std::lock_guard<std::mutex> lk(g_mu);
-  auto it = g_info.find(dev);
-  if (it != g_info.end()) {
-    *out = it->second;
+  if (g_info[dev].sms > 0) {
+    *out = g_info[dev];
     return PAGED_ATTN_OK;
   }
   DeviceInfo di;
@@ -266,8 +275,9 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
 // The library-owned workspace of the current device, grown to at least `bytes`.
 int owned_workspace(size_t bytes, cudaStream_t stream, void** out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
+  int rc = current_device(&dev);
+  if (rc != PAGED_ATTN_OK) return rc;
+  cudaError_t e;
   std::lock_guard<std::mutex> lk(g_mu);
   OwnedWorkspace& w = g_ws[dev];
   if (w.bytes < bytes) {
@@ -296,22 +306,20 @@ int owned_workspace(size_t bytes, cudaStream_t stream, void** out) {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::unordered_map<int, void*> g_static_scratch_ptr;  // device -> address of the array
-
 // Device address of g_static_scratch on the current device, looked up once per
 // device (in host code the array's name is only a stand-in, not an address).
 int static_scratch_address(void** out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
+  int rc = current_device(&dev);
+  if (rc != PAGED_ATTN_OK) return rc;
   std::lock_guard<std::mutex> lk(g_mu);
-  auto it = g_static_scratch_ptr.find(dev);
-  if (it != g_static_scratch_ptr.end()) {
-    *out = it->second;
+  if (g_static_scratch_ptr[dev] != nullptr) {
+    *out = g_static_scratch_ptr[dev];
     return PAGED_ATTN_OK;
   }
   void* ptr = nullptr;
-  if ((e = cudaGetSymbolAddress(&ptr, g_static_scratch)) != cudaSuccess) return cuda_fail(e);
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
   g_static_scratch_ptr[dev] = ptr;
   *out = ptr;
   return PAGED_ATTN_OK;

@@ -40,6 +40,21 @@ def test_every_declared_symbol_is_exported(lib):
         assert getattr(lib, name) is not None
 
 
+def test_library_exports_only_the_c_abi(lib):
+    # Anything else exported -- a C++ helper, a template's static local (a GNU
+    # "unique" symbol, shared by every library in the process) -- would let two
+    # copies of the library loaded side by side interfere with each other.
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    allowed = set(declared_functions()) | {"_init", "_fini", "__bss_start", "_edata", "_end"}
+    extra = []
+    for line in out.splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and parts[-1] not in allowed:
+            extra.append(line)
+    assert not extra, extra
+
+
 def test_build_targets_sm103a_only():
     assert pbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -152,6 +152,28 @@ def test_repeat_calls_are_bitwise_identical():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_two_copies_of_the_library_in_one_process(tmp_path):
+    # Each copy keeps its own per-device state (shared-memory limits, workspace):
+    # a launch through one copy must not make the other skip its own setup.
+    import shutil
+
+    other = tmp_path / "libpaged_kv_gqa_decode_copy.so"
+    shutil.copy(pa.LIB_PATH, other)
+    lib2 = pa.load(str(other))
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    a = run_gpu(w).clone()  # the first copy sets up this kernel first
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        rc = lib2.paged_attn_decode(*pa._args(w.q, w.k_cache, w.v_cache, out, w.block_tables,
+                                              w.seq_lens, w.scale), stream)
+        assert rc == 0, lib2.paged_attn_status_string(rc).decode()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), a.view(torch.int16))
+    b = run_gpu(w)
+    assert torch.equal(b.view(torch.int16), a.view(torch.int16))
+
+
 def test_caller_workspace_matches_owned_workspace():
     w = workloads.make("qwen100k", device="cuda", poison="nan")
     base = run_gpu(w).clone()
