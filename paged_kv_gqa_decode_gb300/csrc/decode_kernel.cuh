@@ -188,13 +188,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const int G = p.G;
   const int cap = p.maxb * BS;
 
-  // ---- 0. start the cold fetches that only depend on the arguments: the tensor
-  // maps (for the first tensor copy) and, spread over the grid, the block table
-  // (read right after the prefix below), so neither waits behind the lengths.
+  // ---- 0. Programmatic dependent launch: let the next kernel in the stream be
+  // scheduled as this grid's CTAs retire, and wait for the previous kernel
+  // (which may write any of the inputs) to complete before touching global
+  // memory.  Both are no-ops for a launch without the programmatic attribute.
+  griddep_launch_dependents();
+  // Start the cold fetches that only depend on the arguments: the tensor maps
+  // (kernel parameters, safe before the wait; needed by the first tensor copy)
+  // and, spread over the grid, the block table (read right after the prefix
+  // below), so neither waits behind the lengths.
   if (tid == kThreads - 32) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  griddep_wait();
   {
     const size_t bt_bytes = (size_t)N * p.maxb * sizeof(int32_t);
     if (bt_bytes <= kBlockTablePrefetchBytes) {

@@ -39,8 +39,20 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) limit_set[dev] = (int)smem;
   }
-  kernel<<<grid, kThreads, smem, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  // Programmatic stream serialization: this launch may begin while the previous
+  // kernel in the stream finishes; the kernel waits for it (griddepcontrol.wait)
+  // before reading any input, so results are those of plain stream order.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
 }
 
 template <int D>

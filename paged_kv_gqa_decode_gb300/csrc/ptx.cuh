@@ -131,6 +131,21 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Blocks until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory operations are visible; returns at once
+// when the launch had no such dependency.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allows the dependent grid to be scheduled once every CTA of this grid has
+// executed this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- global atomics
 
 // atomicAdd with release semantics at GPU scope: this thread's earlier memory
