@@ -58,7 +58,7 @@ __host__ __device__ constexpr int ctas_per_sm(int D, bool g16) {
   return (D >= 256 && g16) ? 1 : 2;
 }
 constexpr int kMinPagesPerCta = 8;
-constexpr int kMaxStages = 16;  // ring depth; always a multiple of kConsumerWarps
+constexpr int kMaxStages = 16;  // ring depth cap (slot s belongs to consumer warp s % 4)
 constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
 constexpr int kConsumerBarrier = 1;
 // Block tables up to this size are prefetched into L2 at kernel entry.
@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   constexpr int kNH = G16 ? 2 : 1;    // n8 tiles of query heads
   constexpr int kDT = D / 16;         // 16-wide tiles of head_dim
   constexpr int kTG = BS / 16;        // 16-token groups per page
-  constexpr int kQTileBytes = L::kQTileBytes;
+  constexpr int kQRows = 8 * kNH;                 // query rows one tile holds
+  constexpr int kQTileBytes = kQRows * D * 2;     // = lay.q_tile_bytes()
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -256,8 +257,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 
   const long long W = (long long)sm_prefix[N] * H_kv;
   if (W == 0) return;
-  // Each ring slot must belong to one consumer warp (see the host plan).
-  if (p.stages <= 0 || p.stages % kConsumerWarps != 0) {
+  if (p.stages < kConsumerWarps) {  // the host plan never launches fewer
     if (tid == 0) atomicOr(p.status, kStatusConfig);
     return;
   }
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   auto prefetch_q = [&](int buf, int s, int g) {
     const __nv_bfloat16* qg = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
     uint8_t* tile = sm_q + buf * kQTileBytes;
-    for (int i = ctid; i < 16 * (D / 8); i += kConsumerThreads) {
+    for (int i = ctid; i < kQRows * (D / 8); i += kConsumerThreads) {
       const int h = i / (D / 8);
       const int c = i - h * (D / 8);
       const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
@@ -788,9 +788,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   reset();
   int stage = 0;
   uint32_t phase = 0;
-  int owner = 0;  // which consumer warp takes the current unit
   for (long long u = u0; u < u1; ++u) {
-    if (owner == warp && !abort) {
+    // Ring slot `stage` always belongs to consumer warp stage % 4, so each warp
+    // waits on its slots' phases strictly in order (a parity wait cannot tell
+    // phase k from phase k - 2) whatever the ring depth.
+    if (stage % kConsumerWarps == warp && !abort) {
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.
@@ -806,7 +808,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
       }
     }
-    if (++owner == kConsumerWarps) owner = 0;
     if (++stage == p.stages) {
       stage = 0;
       phase ^= 1u;

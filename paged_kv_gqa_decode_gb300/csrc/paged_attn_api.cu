@@ -19,6 +19,8 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr size_t kWsAlign = 256;
+constexpr long long kRingBytesPerSm = 128 << 10;            // K/V rings of one SM, few pieces per CTA
+constexpr long long kRingBytesPerSmManyPieces = 160 << 10;  // ... two or more pieces per CTA
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -102,17 +104,15 @@ struct Plan {
 };
 
 template <int D, int BS>
-bool plan_smem(int G, int chunk, int max_smem, int* stages, size_t* smem) {
+bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int* stages, size_t* smem) {
   using L = SmemLayout<D, BS>;
   const L none{0, G, chunk};
   const long long fixed = none.total() + 2048;  // + alignment slack and static shared memory
   const long long per_stage = L::kStageBytes + 16;
   long long st = (max_smem - fixed) / per_stage;
   if (st > kMaxStages) st = kMaxStages;
-  // Ring slot i % stages is consumed by warp i % kConsumerWarps; a multiple keeps
-  // every slot with one warp, so its uses are waited on strictly in order (an
-  // mbarrier parity wait cannot tell phase k from phase k - 2).
-  st -= st % kConsumerWarps;
+  if (st > ring_cap / L::kStageBytes) st = ring_cap / L::kStageBytes;
+  // At least one slot per consumer warp (slot s belongs to warp s % 4).
   if (st < kConsumerWarps) return false;
   const L lay{(int)st, G, chunk};
   *stages = (int)st;
@@ -120,13 +120,16 @@ bool plan_smem(int G, int chunk, int max_smem, int* stages, size_t* smem) {
   return *smem + 256 <= (size_t)max_smem;  // + the kernel's static shared memory
 }
 
-bool plan_smem_any(int D, int BS, int G, int chunk, int max_smem, int* stages, size_t* smem) {
-  if (D == 64) return BS == 16 ? plan_smem<64, 16>(G, chunk, max_smem, stages, smem)
-                               : plan_smem<64, 32>(G, chunk, max_smem, stages, smem);
-  if (D == 128) return BS == 16 ? plan_smem<128, 16>(G, chunk, max_smem, stages, smem)
-                                : plan_smem<128, 32>(G, chunk, max_smem, stages, smem);
-  return BS == 16 ? plan_smem<256, 16>(G, chunk, max_smem, stages, smem)
-                  : plan_smem<256, 32>(G, chunk, max_smem, stages, smem);
+bool plan_smem_any(int D, int BS, int G, int chunk, int max_smem, long long ring_cap,
+                   int* stages, size_t* smem) {
+  if (D == 64)
+    return BS == 16 ? plan_smem<64, 16>(G, chunk, max_smem, ring_cap, stages, smem)
+                    : plan_smem<64, 32>(G, chunk, max_smem, ring_cap, stages, smem);
+  if (D == 128)
+    return BS == 16 ? plan_smem<128, 16>(G, chunk, max_smem, ring_cap, stages, smem)
+                    : plan_smem<128, 32>(G, chunk, max_smem, ring_cap, stages, smem);
+  return BS == 16 ? plan_smem<256, 16>(G, chunk, max_smem, ring_cap, stages, smem)
+                  : plan_smem<256, 32>(G, chunk, max_smem, ring_cap, stages, smem);
 }
 
 int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& di, Plan* pl) {
@@ -146,7 +149,15 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
     if (budget > di.max_smem) budget = di.max_smem;
     chunk = chunk0;
     for (;;) {
-      if (plan_smem_any(D, BS, pl->G, chunk, budget, &pl->stages, &pl->smem) &&
+      // Bytes in flight per SM: past about 128 KB the memory system delivers no
+      // more and a deeper ring measured slower (LLaMA-shaped batch, 8 KB pages, two
+      // CTAs per SM: 8 stages 51.4 us, 10 52.2, 12 53.3); CTAs that cross many
+      // (s, g) pieces gain from a deeper ring that absorbs the stall at each
+      // piece end (ragged 256-sequence batch: 8 stages 617 us, 10 608).
+      const long long pieces = (long long)chunk * H_kv;
+      const long long ring_cap =
+          (pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces : kRingBytesPerSm) / occ;
+      if (plan_smem_any(D, BS, pl->G, chunk, budget, ring_cap, &pl->stages, &pl->smem) &&
           (pl->stages >= 4 || chunk <= 64)) {
         ok = true;
         pl->grid = di.sms * occ;

@@ -26,7 +26,6 @@ struct SmemLayout {
   static constexpr int kTileBytes = BS * 128;         // one half of one page
   static constexpr int kPageBytes = kHalves * kTileBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
-  static constexpr int kQTileBytes = 16 * D * 2;      // query group, up to 16 heads
   static constexpr int kRowStride = D + 4;            // padded fp32 row in the merge buffer
 
   int stages, G, num_seqs;
@@ -39,10 +38,12 @@ struct SmemLayout {
   PAGEDATTN_HD int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int flag() const { return final_ml() + 32 * 4; }  // a few ints
   PAGEDATTN_HD int merge_o() const { return flag() + 128; }
+  // one query tile: the group's rows padded to 8 (G <= 8) or 16 heads
+  PAGEDATTN_HD int q_tile_bytes() const { return (G > 8 ? 16 : 8) * D * 2; }
   PAGEDATTN_HD int qtile() const {  // two query tiles
     return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
   }
-  PAGEDATTN_HD int prefix() const { return qtile() + 2 * kQTileBytes; }
+  PAGEDATTN_HD int prefix() const { return qtile() + 2 * q_tile_bytes(); }
   PAGEDATTN_HD int lens() const { return prefix() + align_up((num_seqs + 1) * 4, 128); }
   PAGEDATTN_HD int total() const { return lens() + num_seqs * 4; }
 };

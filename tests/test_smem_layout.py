@@ -29,7 +29,7 @@ template <int D, int BS>
 void run() {
   using L = SmemLayout<D, BS>;
   const int ns[] = {1, 2, 3, 5, 7, 31, 32, 33, 255, 256, 257, 1000, 4095, 4096};
-  for (int st = 4; st <= 16; st += 4)
+  for (int st = 4; st <= 16; ++st)
     for (int G = 1; G <= 16; ++G)
       for (int n : ns) {
         const L l{st, G, n};
@@ -45,7 +45,8 @@ void run() {
         CHECK(l.flag() - l.final_ml() >= 32 * 4, "final size\n");
         CHECK(l.merge_o() - l.flag() >= 4 * 4, "flag size\n");
         CHECK(l.qtile() - l.merge_o() >= kConsumerWarps * G * L::kRowStride * 4, "merge_o size\n");
-        CHECK(l.prefix() - l.qtile() >= 2 * 16 * D * 2, "qtile size\n");
+        CHECK(l.prefix() - l.qtile() >= 2 * (G > 8 ? 16 : 8) * D * 2, "qtile size\n");
+        CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
         CHECK(l.lens() - l.prefix() >= (n + 1) * 4, "prefix size\n");
         CHECK(l.total() - l.lens() >= n * 4, "lens size\n");
