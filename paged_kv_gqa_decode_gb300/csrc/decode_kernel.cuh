@@ -604,7 +604,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
   };
   uint32_t comb_phase = 0;
-  auto combine = [&](const Split& x0, const Split& x1, int njobs) {
+  // x0 (and x1 when njobs == 2), parts in CTA order.  When local_t >= 0, x0's
+  // part number local_t (this CTA's) is not read back from the workspace: its
+  // merged state already sits in the ring at that place of the first round.
+  auto combine = [&](const Split& x0, const Split& x1, int njobs, int local_t) {
     const int part_bytes = G * kPartialRow * 4;
     const int per_round = (p.stages * kStageBytes) / part_bytes;  // >= 3 for ring >= 4 stages
     if (per_round < 1) {
@@ -627,9 +630,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     for (int t0 = 0; t0 < total; t0 += per_round) {
       const int nt = min(per_round, total - t0);
       if (ctid == 0) {
-        fence_proxy_async_all();  // earlier reads of the ring; the acquired partials
-        mbar_arrive_expect_tx(comb_bar, (uint32_t)(nt * part_bytes));
+        fence_proxy_async_all();  // earlier accesses of the ring; the acquired partials
+        const bool has_local = local_t >= t0 && local_t < t0 + nt;
+        mbar_arrive_expect_tx(comb_bar, (uint32_t)((nt - (has_local ? 1 : 0)) * part_bytes));
         for (int t = t0; t < t0 + nt; ++t) {
+          if (t == local_t) continue;  // already in place
           const Split& x = t < n0 ? x0 : x1;
           const int c = x.c_first + (t < n0 ? t : t - n0);
           const int slot = c == x.c_first ? x.slot_first : 2 * c;
@@ -662,11 +667,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
   };
 
-  // Merge the consumer warps' states for (s, g) and emit the output rows
-  // (whole piece) or a partial state (split piece; its arrival comes at the end
-  // of the range).
-  auto finish_piece = [&](int s, int g, long long sb, long long se) {
-    const bool split = sb < u0 || se > u1;
+  // Merge the four consumer warps' states of a piece through shared memory
+  // (BI-V100 design, section 2, Level 2): afterwards sm_final holds each head's
+  // (M, L) and sm_o each warp's o rescaled to M.  When `arrive` is given,
+  // thread 0 arrives on that split counter (a relaxed add: nothing is published
+  // yet) as soon as every warp is done with the piece's pages, so the add's
+  // round trip overlaps the merge; its old value lands in *old.
+  auto merge_warps = [&](int* arrive, int* old) {
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
@@ -689,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
     __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
+    if (arrive != nullptr && ctid == 0) *old = atomicAdd(arrive, 1);
     float f[kNH][2];
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh)
@@ -722,9 +730,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         }
     __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
+  };
 
-    float* mine = nullptr;
-    if (split) mine = p.partials + (size_t)my_slot(sb) * G * kPartialRow;
+  // Sum the warps' rescaled o and write the piece's merged state: normalised
+  // bf16 rows of (s, g) (whole piece), or a partial row set [M, L, -, -, o]
+  // at `dst` (a workspace slot, or part 0 of the ring).
+  auto emit = [&](int s, int g, float* dst) {
     for (int i = ctid; i < G * (D / 4); i += kConsumerThreads) {
       const int r = i / (D / 4);
       const int d = 4 * (i - r * (D / 4));
@@ -737,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         acc.z += v.z;
         acc.w += v.w;
       }
-      if (!split) {
+      if (dst == nullptr) {
         const float inv = 1.f / sm_final[16 + r];
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -745,11 +756,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         *reinterpret_cast<uint2*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D + d) =
             packed;
       } else {
-        float* prow = mine + r * kPartialRow;
+        float* prow = dst + r * kPartialRow;
         *reinterpret_cast<float4*>(prow + 4 + d) = acc;
         if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(sm_final[r], sm_final[16 + r]);
       }
     }
+  };
+
+  // Thread 0: waits (bounded) until the published count (high half) of a split
+  // counter reaches `want`, with acquire ordering.  Only CTAs that have already
+  // arrived are waited for, and they publish without waiting on anyone.
+  auto wait_published = [&](const int* word, int want) -> bool {
+    for (uint32_t k = 0; k < (1u << 22); ++k) {
+      if ((ld_acquire_gpu(word) >> 16) >= want) return true;
+      __nanosleep(64);
+    }
+    return false;
   };
 
   // Pieces of this CTA's range in order: (s, g) and where its units begin.
@@ -773,10 +795,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 
   Walker wk;
   wk.start(u0, sm_prefix, N, H_kv);
-  // the CTA's first piece (split when it began in an earlier CTA's range)
-  const int first_s = wk.s, first_g = wk.g;
-  const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
-  const long long first_se = first_sb + wk.n;
+  // The range's first and last pieces (the only ones that can be split) and
+  // their split descriptors, worked out now by thread 0 (off the critical path
+  // at the end) and kept in shared memory, not in registers, through the loop.
+  Split* const sm_split = reinterpret_cast<Split*>(sm_flag + 4);  // [0] first, [1] last
+  int* const sm_split_flags = sm_flag + 4 + 2 * (int)(sizeof(Split) / sizeof(int));
+  if (ctid == 0) {
+    const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
+    Walker wl;
+    wl.start(u1 - 1, sm_prefix, N, H_kv);
+    const long long last_sb = (long long)sm_prefix[wl.s] * H_kv + (long long)wl.g * wl.n;
+    sm_split[0] = make_split(wk.s, wk.g, first_sb, first_sb + wk.n);
+    sm_split[1] = make_split(wl.s, wl.g, last_sb, last_sb + wl.n);
+    sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
+    sm_split_flags[1] = last_sb < u0 || last_sb + wl.n > u1;
+  }
   Piece ahead{wk.s, wk.g, 0};  // the next piece whose query group gets prefetched
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
@@ -815,61 +848,85 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     const int s = wk.s, g = wk.g, n = wk.n;
     const bool last = u + 1 == u1;
     wk.next(sm_prefix, N, H_kv);
-    if (last || wk.g != g || wk.s != s) {
-      const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
-      finish_piece(s, g, sb, sb + n);
-      if (!last) {
-        // The next piece's query group was prefetched into the other tile: make
-        // every thread's copies visible, then prefetch the piece after it into
-        // the tile just freed.
-        cp_async_wait_all();
-        __syncwarp();
-        named_barrier(kConsumerBarrier, kConsumerThreads);
-        // A split piece that is not the range's last is its first: arrive on its
-        // counter now (the barrier above ordered every thread's partial stores
-        // before this release); the old value is read at the end of the range.
-        if (ctid == 0 && sb < u0) first_old = atom_add_release_gpu(p.counters + cta_of(sb, W, C), 1);
-        qbuf ^= 1;
-        ahead = next_piece(ahead);
-        if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
-        reset();
-      } else {
-        // Arrival for the last piece (if split) and, when this CTA arrived last
-        // for either split piece, the combine.  The barrier orders every
-        // thread's partial stores before thread 0's release.
-        const bool last_split = sb < u0 || sb + n > u1;
-        const bool first_pending = first_sb < u0 && first_sb != sb;
-        __syncwarp();
-        const bool failed = named_barrier_or(kConsumerBarrier, kConsumerThreads, abort);
-        if (!failed && (last_split || first_pending)) {
-          if (ctid == 0) {
-            bool cf = false, cl = false;
-            if (first_pending)
-              cf = first_old == cta_of(first_se - 1, W, C) - cta_of(first_sb, W, C);
-            if (last_split) {
-              const int c_first = cta_of(sb, W, C);
-              const int old = atom_add_acq_rel_gpu(p.counters + c_first, 1);
-              cl = old == cta_of(sb + n - 1, W, C) - c_first;
-            }
-            // the first piece's counter was read with a release-only add: acquire now
-            if (cf) fence_acq_rel_gpu();
-            sm_flag[0] = cf ? 1 : 0;
-            sm_flag[1] = cl ? 1 : 0;
-          }
-          __syncwarp();
-          named_barrier(kConsumerBarrier, kConsumerThreads);
-          const bool cf = sm_flag[0] != 0, cl = sm_flag[1] != 0;
-          if (cf || cl) {
-            const Split xf = make_split(first_s, first_g, first_sb, first_se);
-            const Split xl = make_split(s, g, sb, sb + n);
-            combine(cf ? xf : xl, xl, cf && cl ? 2 : 1);
-            if (ctid == 0) {  // ready for the next call
-              if (cf) p.counters[xf.c_first] = 0;
-              if (cl) p.counters[xl.c_first] = 0;
-            }
-          }
-        }
+    if (!last && wk.g == g && wk.s == s) continue;
+    const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
+    if (!last) {
+      // A split piece that is not the range's last is its first: store its
+      // partial, then arrive and publish at once with a release add (the
+      // barrier below orders every thread's stores before it); the old value
+      // is only read at the end of the range.
+      const bool split = sb < u0;
+      merge_warps(nullptr, nullptr);
+      emit(s, g, split ? p.partials + (size_t)my_slot(sb) * G * kPartialRow : nullptr);
+      // The next piece's query group was prefetched into the other tile: make
+      // every thread's copies visible, then prefetch the piece after it into
+      // the tile just freed.
+      cp_async_wait_all();
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      if (ctid == 0 && split)
+        first_old = atom_add_release_gpu(p.counters + sm_split[0].c_first, 1 + (1 << 16));
+      qbuf ^= 1;
+      ahead = next_piece(ahead);
+      if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
+      reset();
+      continue;
+    }
+    // ---- the range's last piece.  When it is split, thread 0 arrives as soon
+    // as the pages are done (before anything is stored); the last CTA to arrive
+    // combines, keeping its own merged state in shared memory, while the
+    // others store theirs and publish it.
+    const Split xf = sm_split[0], xl = sm_split[1];
+    const bool first_split = sm_split_flags[0] != 0, last_split = sm_split_flags[1] != 0;
+    int* const word_f = p.counters + xf.c_first;  // [15:0] arrived, [31:16] published
+    int* const word_l = p.counters + xl.c_first;
+    const int n_f = xf.c_last - xf.c_first + 1;   // contributors
+    const int n_l = xl.c_last - xl.c_first + 1;
+    int old_l = 0;
+    merge_warps(last_split ? word_l : nullptr, &old_l);
+    if (!last_split) emit(s, g, nullptr);
+    if (ctid == 0) {
+      sm_flag[0] = first_split && (first_old & 0xffff) == n_f - 1 ? 1 : 0;
+      sm_flag[1] = last_split && (old_l & 0xffff) == n_l - 1 ? 1 : 0;
+    }
+    __syncwarp();
+    if (named_barrier_or(kConsumerBarrier, kConsumerThreads, abort)) break;
+    const bool cf = sm_flag[0] != 0, cl = sm_flag[1] != 0;
+    // this CTA's part of the last piece: its place among the split's parts, and
+    // whether the combine can take it from the ring instead of the workspace
+    const int local_t = (int)blockIdx.x - xl.c_first;
+    const int part_bytes = G * kPartialRow * 4;
+    const bool local = cl && local_t < (p.stages * kStageBytes) / part_bytes;
+    if (last_split && !local) {
+      emit(s, g, p.partials + (size_t)my_slot(sb) * G * kPartialRow);
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      if (ctid == 0) {
+        if (!cl)
+          atom_add_release_gpu(word_l, 1 << 16);  // publish
+        else
+          __threadfence();  // this CTA's stores, read back by its own bulk copies
       }
+    }
+    if (local) emit(s, g, reinterpret_cast<float*>(smem + local_t * part_bytes));
+    if (!cf && !cl) break;
+    if (ctid == 0) {
+      bool ok = true;
+      if (cl) ok = wait_published(word_l, n_l - 1);  // every other part
+      if (cf && ok) ok = wait_published(word_f, n_f);
+      if (!ok) atomicOr(p.status, kStatusTimeout);
+      sm_flag[2] = ok ? 1 : 0;
+    }
+    __syncwarp();
+    named_barrier(kConsumerBarrier, kConsumerThreads);  // also orders the ring writes
+    if (sm_flag[2] == 0) break;
+    if (cl)
+      combine(xl, xf, cf ? 2 : 1, local ? local_t : -1);
+    else
+      combine(xf, xf, 1, -1);
+    if (ctid == 0) {  // ready for the next call
+      if (cf) *word_f = 0;
+      if (cl) *word_l = 0;
     }
   }
   cp_async_wait_all();
