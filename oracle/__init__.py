@@ -8,6 +8,8 @@ imports this package, and this package imports nothing from it.
                       layout) for every (s, h) row or for a list of rows; the C
                       source ``paged_attn_oracle.c`` states it in full.
 * ``pieces``       -- the per-range softmax pieces (M, l, o) of rows.
+* ``append``       -- the cache write of each sequence's new token (the step
+                      before the decode).
 * ``combine`` / ``finish`` -- the merge of two partial softmax states and the
                       final normalisation, as "Paged Attention Kernel
                       Architecture for BI-V100" (section 2, Level 1: the
@@ -21,6 +23,7 @@ forms, invariances and a hand-derived golden example.
 """
 from __future__ import annotations
 
+import copy
 import ctypes
 import os
 import subprocess
@@ -204,6 +207,45 @@ def combine(a, b):
     wa = 0.0 if Ma == -np.inf else float(np.exp(Ma - M))
     wb = 0.0 if Mb == -np.inf else float(np.exp(Mb - M))
     return (M, wa * la + wb * lb, wa * oa + wb * ob)
+
+
+def append(x, k_new, v_new) -> Inputs:
+    """Cache append ("reshape and cache") of one new token per sequence.
+
+    The paged-decode layout of the "Add Cuda Kernel" tutorial
+    (include/kernels/attention.cuh, "Paged Attention - Decode") counts the new
+    token in seq_lens, so its K and V must already sit in the cache when the
+    decode runs; AstrAI's CUDA-kernels page (Backend Layer) has the backend own
+    that write.  The new token of sequence s is position t = L_s - 1, and for
+    every KV head g
+
+        k_cache[bt[s, t // BS], g, t % BS, :] = k_new[s, g, :]   (v likewise).
+
+    A sequence with L_s = 0 has no token and writes nothing.  ``k_new`` and
+    ``v_new`` are [num_seqs, H_kv, D] bf16.  Returns new Inputs whose caches
+    are copies with those rows written (the input is not modified).
+    """
+    inp = _as_inputs(x)
+    kn = _bits(k_new)
+    vn = _bits(v_new)
+    if kn.shape != (inp.num_seqs, inp.H_kv, inp.D) or vn.shape != kn.shape:
+        raise ValueError("k_new and v_new must be [num_seqs, H_kv, D]")
+    out = copy.copy(inp)
+    out.k = inp.k.copy()
+    out.v = inp.v.copy()
+    for s in range(inp.num_seqs):
+        L = int(inp.lens[s])
+        if L <= 0:
+            continue
+        if L > inp.maxb * inp.BS:
+            raise OracleError(f"oracle rejected the input: {ERRORS[-3]}")
+        t = L - 1
+        b = int(inp.bt[s, t // inp.BS])
+        if not 0 <= b < inp.num_blocks:
+            raise OracleError(f"oracle rejected the input: {ERRORS[-4]}")
+        out.k[b, :, t % inp.BS, :] = kn[s]
+        out.v[b, :, t % inp.BS, :] = vn[s]
+    return out
 
 
 def finish(state) -> np.ndarray:

@@ -357,3 +357,132 @@ def test_pins_catch_planted_mistakes(name, old, new, tmp_path):
 
 def test_unmutated_oracle_passes_the_same_pins():
     assert _pins_pass()
+
+
+# ---------------------------------------------------------------- cache append
+
+def _last_rows(inp):
+    """Each sequence's newest cached K and V rows, [num_seqs, H_kv, D] (zeros when L = 0).
+
+    Read through the un-paged view (the table maps logical page i of s to its block),
+    so these tests do not restate the append's own indexing."""
+    k = np.zeros((inp.num_seqs, inp.H_kv, inp.D), dtype=np.uint16)
+    v = np.zeros_like(k)
+    for s in range(inp.num_seqs):
+        L = int(inp.lens[s])
+        if L == 0:
+            continue
+        pages = [inp.bt[s, i] for i in range(-(-L // inp.BS))]
+        flat_k = np.concatenate([inp.k[b] for b in pages], axis=1)  # [H_kv, pages*BS, D]
+        flat_v = np.concatenate([inp.v[b] for b in pages], axis=1)
+        k[s] = flat_k[:, L - 1]
+        v[s] = flat_v[:, L - 1]
+    return k, v
+
+
+def _append_pins_pass(append) -> bool:
+    """The cache-append pins, against a given append function."""
+    try:
+        _round_trip(append, "tiny")
+        _round_trip(append, "ragged_small")
+        test_append_changes_only_the_new_token_rows(append)
+        test_append_of_a_one_token_sequence_is_its_output(append)
+    except (AssertionError, oracle.OracleError, IndexError, ValueError):
+        return False
+    return True
+
+
+@pytest.fixture
+def append():
+    return oracle.append
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_small"])
+def test_append_round_trip_restores_cache_and_decode(append, name):
+    _round_trip(append, name)
+
+
+def _round_trip(append, name):
+    """Take every sequence's newest row out of the cache, poison it, append it back:
+    the caches and the decode come back bit for bit."""
+    if name == "ragged_small":
+        spec = workloads.custom_spec("ragged_small", 9, 8, 2, 64, 16,
+                                     [1, 15, 16, 17, 31, 32, 33, 0, 48])
+        w = workloads.make(spec, seed=7, poison="nan")
+    else:
+        w = workloads.make(name, poison="nan")
+    inp = oracle.Inputs.from_workload(w)
+    k_new, v_new = _last_rows(inp)
+    hole = oracle.Inputs.from_workload(w)
+    hole.k, hole.v = hole.k.copy(), hole.v.copy()  # the views share the workload's memory
+    for s in range(hole.num_seqs):  # poison the newest row of every sequence
+        L = int(hole.lens[s])
+        if L == 0:
+            continue
+        pages = -(-L // hole.BS)
+        b = int(hole.bt[s, pages - 1])
+        slot = (L - 1) - (pages - 1) * hole.BS
+        hole.k[b, :, slot, :] = 0x7FC0
+        hole.v[b, :, slot, :] = 0x7FC0
+    back = append(hole, k_new, v_new)
+    assert np.array_equal(back.k, inp.k) and np.array_equal(back.v, inp.v)
+    assert np.array_equal(oracle.decode(back), oracle.decode(inp))
+
+
+def test_append_changes_only_the_new_token_rows(append):
+    """Random new rows: exactly H_kv * D values per non-empty sequence change in each cache,
+    and the input problem itself is left untouched."""
+    spec = workloads.custom_spec("app", 5, 4, 2, 64, 16, [3, 16, 0, 17, 40])
+    w = workloads.make(spec, seed=11, poison="zero")
+    inp = oracle.Inputs.from_workload(w)
+    k0, v0 = inp.k.copy(), inp.v.copy()
+    rng = np.random.default_rng(3)
+    # magnitudes 32768..65535, which the N(0, 1) cache never holds: every written value changes
+    k_new = rng.integers(0x4700, 0x4780, size=(5, 2, 64), dtype=np.uint16)
+    v_new = rng.integers(0xC700, 0xC780, size=(5, 2, 64), dtype=np.uint16)
+    out = append(inp, k_new, v_new)
+    assert np.array_equal(inp.k, k0) and np.array_equal(inp.v, v0)
+    nonempty = sum(1 for L in [3, 16, 0, 17, 40] if L > 0)
+    assert int((out.k != k0).sum()) == nonempty * 2 * 64
+    assert int((out.v != v0).sum()) == nonempty * 2 * 64
+    kl, vl = _last_rows(out)
+    for s, L in enumerate([3, 16, 0, 17, 40]):
+        if L:
+            assert np.array_equal(kl[s], k_new[s]) and np.array_equal(vl[s], v_new[s])
+
+
+def test_append_of_a_one_token_sequence_is_its_output(append):
+    """A sequence whose only token is the new one attends to it alone: out = v_new."""
+    spec = workloads.custom_spec("one", 3, 4, 2, 64, 16, [1, 1, 1])
+    w = workloads.make(spec, seed=5, poison="nan")
+    rng = np.random.default_rng(9)
+    k_new = rng.integers(0x3C00, 0x4000, size=(3, 2, 64), dtype=np.uint16)
+    v_new = rng.integers(0x3C00, 0x4000, size=(3, 2, 64), dtype=np.uint16)
+    out = oracle.decode(append(oracle.Inputs.from_workload(w), k_new, v_new))
+    vf = (v_new.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for s in range(3):
+        for h in range(4):
+            assert np.array_equal(out[s, h], vf[s, h // 2])
+
+
+APPEND_MUTANTS = [
+    ("slot from L", "t % inp.BS, :] = kn[s]", "L % inp.BS, :] = kn[s]"),
+    ("page from L", "b = int(inp.bt[s, t // inp.BS])", "b = int(inp.bt[s, L // inp.BS])"),
+    ("k and v swapped", "out.v[b, :, t % inp.BS, :] = vn[s]", "out.v[b, :, t % inp.BS, :] = kn[s]"),
+    ("kv head dropped", "out.k[b, :, t % inp.BS, :] = kn[s]", "out.k[b, :, t % inp.BS, :] = kn[s, 0]"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", APPEND_MUTANTS, ids=[m[0] for m in APPEND_MUTANTS])
+def test_append_pins_catch_planted_mistakes(name, old, new):
+    import inspect
+
+    src = inspect.getsource(oracle.append)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    assert not _append_pins_pass(ns["append"]), f"no pin noticed: {name}"
+
+
+def test_unmutated_append_passes_the_same_pins():
+    assert _append_pins_pass(oracle.append)
