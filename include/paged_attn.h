@@ -156,6 +156,47 @@ PAGED_ATTN_API int paged_attn_decode_static(const void* q, const void* k_cache, 
                              int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
                              int block_size, float scale, void* stream);
 
+/*
+ * Cache append ("reshape and cache") of one new token per sequence, the write
+ * that precedes the decode: the paged-decode layout above counts the new token
+ * in seq_lens ("context length including the new token"), so its K and V must
+ * be in the cache when the decode runs; AstrAI's CUDA-kernels page (Backend
+ * Layer) has the backend own that write.  For every sequence s with
+ * L = seq_lens[s] >= 1 and every KV head g, with t = L - 1:
+ *
+ *   k_cache[block_tables[s, t / block_size], g, t % block_size, :] = k_new[s, g, :]
+ *   v_cache[...same place...]                                      = v_new[s, g, :]
+ *
+ *   k_new, v_new  [num_seqs, H_kv, head_dim]  bf16  (read; device, 16-byte aligned)
+ *   k_cache, v_cache                          bf16  (written at those rows only)
+ *
+ * Sequences with L = 0 or L > max_blocks_per_seq * block_size write nothing.
+ * The block ids are not checked.  Sizes follow paged_attn_decode's rules
+ * (head_dim 64/128/256, block_size 16/32); errors as above.  Asynchronous on
+ * `stream`; allocates nothing.
+ */
+PAGED_ATTN_API int paged_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                                   void* v_cache, const int32_t* block_tables,
+                                   const int32_t* seq_lens, int num_seqs, int H_kv, int head_dim,
+                                   int max_blocks_per_seq, int block_size, void* stream);
+
+/*
+ * paged_kv_append followed by paged_attn_decode, fused into the decode launch:
+ * the CTA that reads the page holding a sequence's new token writes that
+ * token's K and V rows first (while its first pages are in flight), so the
+ * append costs no extra launch and no extra pass over the cache.  The blocks
+ * that receive the new tokens must not also be read by another sequence of
+ * the same call (no copy-on-write sharing of a partly filled block).  Same
+ * arguments, workspace and errors as paged_attn_decode, plus k_new / v_new
+ * ([num_seqs, H_kv, head_dim] bf16, 16-byte aligned).
+ */
+PAGED_ATTN_API int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new,
+                                            void* k_cache, void* v_cache, void* out,
+                                            const int32_t* block_tables, const int32_t* seq_lens,
+                                            int num_seqs, int H_q, int H_kv, int head_dim,
+                                            int max_blocks_per_seq, int block_size, float scale,
+                                            void* stream);
+
 /* Human-readable text for a PAGED_ATTN_* code (static storage). */
 PAGED_ATTN_API const char* paged_attn_status_string(int status);
 

@@ -21,6 +21,8 @@ __all__ = [
     "paged_attn_decode_ws",
     "paged_attn_decode_checked",
     "paged_attn_decode_static",
+    "paged_attn_append_decode",
+    "paged_kv_append",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "EXPORTED_SYMBOLS",
@@ -36,6 +38,8 @@ EXPORTED_SYMBOLS = (
     "paged_attn_decode_ws",
     "paged_attn_decode_checked",
     "paged_attn_decode_static",
+    "paged_kv_append",
+    "paged_attn_append_decode",
     "paged_attn_status_string",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
@@ -76,6 +80,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_decode_checked.restype = I
         lib.paged_attn_decode_static.argtypes = common + [P]
         lib.paged_attn_decode_static.restype = I
+        lib.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
+        lib.paged_kv_append.restype = I
+        lib.paged_attn_append_decode.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.paged_attn_append_decode.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -189,4 +197,41 @@ def paged_attn_decode_static(q, k_cache, v_cache, block_tables, seq_lens, scale:
         out = torch.empty_like(q)
     _check(load().paged_attn_decode_static(*_args(q, k_cache, v_cache, out, block_tables,
                                                   seq_lens, scale), _stream(stream)))
+    return out
+
+
+def _check_rows(k_new, v_new, q_or_none, k_cache):
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _, H_kv, _, D = (int(x) for x in k_cache.shape)
+    if tuple(k_new.shape[1:]) != (H_kv, D) or k_new.shape != v_new.shape:
+        raise ValueError("k_new and v_new must be [num_seqs, H_kv, head_dim]")
+    if q_or_none is not None and int(k_new.shape[0]) != int(q_or_none.shape[0]):
+        raise ValueError("k_new must have one row set per sequence of q")
+
+
+def paged_kv_append(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, stream=None):
+    """Write each sequence's new token (position seq_lens[s] - 1) into the paged caches
+    (see paged_attn.h).  k_new, v_new: [num_seqs, H_kv, head_dim] bf16."""
+    _check_rows(k_new, v_new, None, k_cache)
+    num_blocks, H_kv, BS, D = (int(x) for x in k_cache.shape)
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(load().paged_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_tables), _ptr(seq_lens), int(k_new.shape[0]), H_kv,
+                                  D, maxb, BS, _stream(stream)))
+
+
+def paged_attn_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                             scale: float, out=None, stream=None):
+    """paged_kv_append then paged_attn_decode, fused into one launch (see paged_attn.h)."""
+    import torch
+
+    _check_rows(k_new, v_new, q, k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    a = _args(q, k_cache, v_cache, out, block_tables, seq_lens, scale)
+    # (q, k_new, v_new, k_cache, v_cache, out, tables, lens, sizes..., scale)
+    _check(load().paged_attn_append_decode(a[0], _ptr(k_new), _ptr(v_new), a[1], a[2], a[3],
+                                           *a[4:], _stream(stream)))
     return out

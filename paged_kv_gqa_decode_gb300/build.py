@@ -21,7 +21,8 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libpaged_kv_gqa_decode.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["paged_attn_api.cu", "decode_d64.cu", "decode_d128.cu", "decode_d256.cu"]
+SOURCES = ["paged_attn_api.cu", "append.cu", "decode_d64.cu", "decode_d128.cu",
+           "decode_d256.cu"]
 
 
 def nvcc() -> str:

@@ -86,6 +86,12 @@ struct DecodeParams {
   int32_t* counters;    // [gridDim.x], zero between calls (one per split piece's first CTA)
   float* partials;      // [gridDim.x * 2][G][D + 4]
   long long num_blocks; // > 0: checked mode (validate block ids against it)
+  // Fused cache append (null k_new: none): the new token's rows, written into
+  // the caches before the pages holding them are read.
+  const __nv_bfloat16* k_new;  // [num_seqs, H_kv, D]
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache;      // [num_blocks, H_kv, BS, D]
+  __nv_bfloat16* v_cache;
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -172,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
+  uint64_t* append_bar = comb_bar + 1;         // the fused append's rows are written
   float* sm_m = reinterpret_cast<float*>(smem + lay.merge_m());
   float* sm_l = reinterpret_cast<float*>(smem + lay.merge_l());
   float* sm_final = reinterpret_cast<float*>(smem + lay.final_ml());  // [0,16) M, [16,32) L
@@ -274,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       mbar_init(&empty_bar[i], 1);
     }
     mbar_init(comb_bar, 1);
+    mbar_init(append_bar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -286,19 +294,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     const int issue_lanes = min(kMaxIssueLanes, p.stages);
     Walker wk;
     if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_kv);
-    auto fetch = [&](long long u) -> int2 {
-      // physical block and KV head of this lane's unit (block -1 past the range)
-      if (u >= u1) return make_int2(-1, 0);
+    auto fetch = [&](long long u) -> int3 {
+      // physical block and KV head of this lane's unit (block -1 past the range),
+      // and whether the unit is the last page of its (s, g)
+      if (u >= u1) return make_int3(-1, 0, 0);
       int pb = __ldg(p.block_tables + (size_t)wk.s * p.maxb + wk.p);
       if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
         atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
-      return make_int2(pb, wk.g);
+      return make_int3(pb, wk.g, wk.p == wk.n - 1 ? 1 : 0);
     };
-    int2 cur = fetch(u0 + lane);
+    // With a fused append, the last page of a piece may only be read once the
+    // consumer warps have written the new token's rows (append_bar).
+    bool append_pending = p.k_new != nullptr;
+    int3 cur = fetch(u0 + lane);
     bool abort = false;
     for (long long ub = u0; ub < u1 && !abort; ub += 32) {
       // advance this lane's walker to its unit of the next batch and start that load
-      int2 nxt = make_int2(-1, 0);
+      int3 nxt = make_int3(-1, 0, 0);
       if (ub + 32 + lane < u1) {
         wk.advance(32, sm_prefix, N, H_kv);
         nxt = fetch(ub + 32 + lane);
@@ -308,8 +320,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         const int j = j0 + (lane < issue_lanes ? lane : 0);
         const int pb = __shfl_sync(0xffffffffu, cur.x, j);
         const int g = __shfl_sync(0xffffffffu, cur.y, j);
+        const int last_page = __shfl_sync(0xffffffffu, cur.z, j);
         bool bad = false;
-        if (lane < issue_lanes && j0 + lane < cnt) {
+        if (append_pending &&
+            __any_sync(0xffffffffu, lane < issue_lanes && j0 + lane < cnt && last_page)) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(append_bar, 0);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            bad = true;
+          }
+          append_pending = false;
+        }
+        if (lane < issue_lanes && j0 + lane < cnt && !bad) {
           const long long i = ub - u0 + j;  // unit index within this CTA
           const int stage = (int)(i % p.stages);
           const uint32_t phase = (uint32_t)((i / p.stages) & 1);
@@ -814,6 +837,80 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
   ahead = next_piece(ahead);
+  if (p.k_new != nullptr) {
+    // ---- fused cache append.  The new token of each (s, g) whose last page
+    // lies in this range is written here, while the first pages are in
+    // flight: each such page is read by this CTA alone, and only after
+    // append_bar.  Thread 0 lists the rows in the (idle) merge buffer, every
+    // consumer thread moves 16-byte chunks of them (loads first, then stores),
+    // and each writer fences its stores against the tensor copies that will
+    // read them.
+    int* const list = reinterpret_cast<int*>(sm_o);   // s * H_kv + g
+    const int list_cap = kConsumerWarps * G * kRowStride;
+    int* const sm_cnt = sm_flag + 16;                 // [0] rows listed, [1] more to list
+    int cs = wk.s, cg = wk.g;                          // thread 0's piece cursor
+    constexpr int kChunks = 2 * (D / 8);               // 16-byte chunks of a K row + V row
+    for (;;) {
+      if (ctid == 0) {
+        int n = 0;
+        bool more = false;
+        while (cs < N) {
+          const int np = sm_prefix[cs + 1] - sm_prefix[cs];
+          const long long sb = (long long)sm_prefix[cs] * H_kv + (long long)cg * np;
+          if (sb >= u1) break;
+          if (n == list_cap) {
+            more = true;
+            break;
+          }
+          if (sb + np - 1 < u1) list[n++] = cs * H_kv + cg;  // its last page is here
+          if (++cg == H_kv) {
+            cg = 0;
+            do {
+              ++cs;
+            } while (cs < N && sm_prefix[cs + 1] == sm_prefix[cs]);
+          }
+        }
+        sm_cnt[0] = n;
+        sm_cnt[1] = more ? 1 : 0;
+      }
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);
+      const int n = sm_cnt[0];
+      const bool more = sm_cnt[1] != 0;
+      for (int c0 = ctid; c0 < n * kChunks; c0 += 4 * kConsumerThreads) {
+        uint4 v[4];
+        uint4* dst[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = c0 + k * kConsumerThreads;
+          dst[k] = nullptr;
+          if (c < n * kChunks) {
+            const int row = list[c / kChunks];
+            const int ch = c % kChunks;
+            const int s = row / H_kv, g = row - (row / H_kv) * H_kv;
+            const int kv = ch / (D / 8), off = (ch % (D / 8)) * 8;
+            const int t = sm_len[s] - 1;
+            const int b = __ldg(p.block_tables + (size_t)s * p.maxb + t / BS);
+            if (p.num_blocks > 0 && (b < 0 || (long long)b >= p.num_blocks)) continue;
+            v[k] = __ldg(reinterpret_cast<const uint4*>(
+                (kv ? p.v_new : p.k_new) + ((size_t)s * H_kv + g) * D + off));
+            dst[k] = reinterpret_cast<uint4*>(
+                (kv ? p.v_cache : p.k_cache) + (((size_t)b * H_kv + g) * BS + t % BS) * D + off);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (dst[k] != nullptr) *dst[k] = v[k];
+      }
+      __syncwarp();
+      named_barrier(kConsumerBarrier, kConsumerThreads);  // the list may be refilled
+      if (!more) break;
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    named_barrier(kConsumerBarrier, kConsumerThreads);
+    if (ctid == 0) mbar_arrive(append_bar);
+  }
   cp_async_wait_all();
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);

@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "append.h"
 #include "launch.h"
 #include "paged_attn.h"
 
@@ -249,10 +250,12 @@ int check_pointers(const void* q, const void* k, const void* v, const void* out,
 }
 
 // Runs the whole operation in chunks of plan.chunk sequences on `stream`.
+// With k_new / v_new (else null), each sequence's new token is first written
+// into the caches by the decode kernel itself (fused cache append).
 int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache, void* out,
         const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
         int max_blocks_per_seq, float scale, void* ws, int32_t* status, long long num_blocks,
-        cudaStream_t stream) {
+        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
   CUtensorMap tk, tv;
   int rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk);
   if (rc != PAGED_ATTN_OK) return rc;
@@ -277,6 +280,12 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
     p.counters = reinterpret_cast<int32_t*>(wsb + pl.off_counters);
     p.partials = reinterpret_cast<float*>(wsb + pl.off_partials);
     p.num_blocks = num_blocks;
+    p.k_new = k_new ? static_cast<const __nv_bfloat16*>(k_new) + (size_t)s0 * H_kv * pl.D
+                    : nullptr;
+    p.v_new = v_new ? static_cast<const __nv_bfloat16*>(v_new) + (size_t)s0 * H_kv * pl.D
+                    : nullptr;
+    p.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+    p.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
     cudaError_t e = launch_dim(pl.D, pl.BS, pl.g16, tk, tv, p, pl.grid, pl.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -370,6 +379,55 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
   if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
   return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
              max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
+int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, void* out, const int32_t* block_tables,
+                             const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
+                             int head_dim, int max_blocks_per_seq, int block_size, float scale,
+                             void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PAGED_ATTN_ERR_POINTER;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st, k_new, v_new);
+}
+
+int paged_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int H_kv,
+                    int head_dim, int max_blocks_per_seq, int block_size, void* stream) {
+  // the decode's size rules with a one-head query group
+  int rc = validate_sizes(num_seqs, H_kv, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(block_tables) || !aligned16(seq_lens))
+    return PAGED_ATTN_ERR_POINTER;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  AppendParams a;
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.H_kv = H_kv;
+  a.D = head_dim;
+  a.maxb = max_blocks_per_seq;
+  a.BS = block_size;
+  a.num_blocks = 0;
+  cudaError_t e = launch_append(a, di.sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PAGED_ATTN_OK : cuda_fail(e);
 }
 
 size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,

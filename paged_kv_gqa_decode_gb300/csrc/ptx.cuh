@@ -109,6 +109,13 @@ __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy global-memory writes before later
+// async-proxy (tensor copy) reads of them, by this or (after a barrier) any
+// thread of the CTA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -31,9 +31,9 @@ struct SmemLayout {
   int stages, G, num_seqs;
   // [0, bars): the ring of `stages` K/V pages (at the end of a range it holds the
   // partial states being combined); then the mbarriers full[stages],
-  // empty[stages] and one for the combine's copies
+  // empty[stages], one for the combine's copies and one for the fused append
   PAGEDATTN_HD int bars() const { return stages * kStageBytes; }
-  PAGEDATTN_HD int merge_m() const { return align_up(bars() + (2 * stages + 1) * 8, 128); }
+  PAGEDATTN_HD int merge_m() const { return align_up(bars() + (2 * stages + 2) * 8, 128); }
   PAGEDATTN_HD int merge_l() const { return merge_m() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int flag() const { return final_ml() + 32 * 4; }  // a few ints

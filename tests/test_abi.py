@@ -23,7 +23,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(paged_attn_\w+)\s*\(", text,
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(paged_(?:attn|kv)_\w+)\s*\(", text,
                                  flags=re.M)))
 
 

@@ -35,7 +35,7 @@ void run() {
         const L l{st, G, n};
         CHECK(l.bars() % 1024 == 0, "bars D%d BS%d st%d\n", D, BS, st);
         CHECK(L::kStageBytes % 1024 == 0, "stage size D%d BS%d\n", D, BS);
-        CHECK(l.merge_m() >= l.bars() + (2 * st + 1) * 8, "barrier overlap\n");
+        CHECK(l.merge_m() >= l.bars() + (2 * st + 2) * 8, "barrier overlap\n");
         const int starts[] = {l.merge_m(), l.merge_l(), l.final_ml(), l.flag(), l.merge_o(),
                               l.qtile(), l.prefix(), l.lens()};
         for (int x : starts)
