@@ -259,9 +259,32 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
 
+    # --op: the decode alone, or with each sequence's new token appended to the
+    # cache first (fused into the decode launch, or as a separate launch)
+    op = args.op
+    k_new = v_new = None
+    if op != "decode":
+        gk = torch.Generator(device="cpu").manual_seed(seed + 17)
+        shape = (spec.num_seqs, spec.H_kv, spec.D)
+        k_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
+        v_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
+        rows = sum(1 for L in lens if L > 0) * spec.H_kv
+        nbytes = dict(nbytes)
+        nbytes["append"] = rows * spec.D * 2 * 2 * 2  # K and V rows, read once, written once
+        nbytes["total"] += nbytes["append"]
+
+    def run_op(q, bt, sl, kc, vc, kn, vn):
+        if op == "decode":
+            pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
+        elif op == "append_decode":
+            pa.paged_attn_append_decode(q, kn, vn, kc, vc, bt, sl, w.scale, out=out,
+                                        stream=stream)
+        else:
+            pa.paged_kv_append(kn, vn, kc, vc, bt, sl, stream=stream)
+            pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
+
     def step(i):
-        pa.paged_attn_decode(w.q, ks[i % reps], vs[i % reps], w.block_tables, w.seq_lens,
-                             w.scale, out=out, stream=stream)
+        run_op(w.q, w.block_tables, w.seq_lens, ks[i % reps], vs[i % reps], k_new, v_new)
 
     for i in range(args.warmup):
         step(i)
@@ -312,7 +335,7 @@ def run_ours(args, world, rank, local):
         clocks.stop()
         clock_info = clocks.summary(t0, t1)
     per_step = elapsed / steps
-    launches_per_step = -(-len(lens) // 4096)
+    launches_per_step = -(-len(lens) // 4096) + (1 if op == "append_then_decode" else 0)
 
     # end to end through the public API: pinned host inputs in, result back to host
     host_q = w.q.cpu().pin_memory()
@@ -321,14 +344,20 @@ def run_ours(args, world, rank, local):
     host_out = torch.empty_like(host_q).pin_memory()
     dq, dbt, dsl = torch.empty_like(w.q), torch.empty_like(w.block_tables), \
         torch.empty_like(w.seq_lens)
+    host_kn = k_new.cpu().pin_memory() if k_new is not None else None
+    host_vn = v_new.cpu().pin_memory() if v_new is not None else None
+    dkn = torch.empty_like(k_new) if k_new is not None else None
+    dvn = torch.empty_like(v_new) if v_new is not None else None
     e2e_steps = max(20, min(steps, 2000))
 
     def e2e_step(i):
         dq.copy_(host_q, non_blocking=True)
         dbt.copy_(host_bt, non_blocking=True)
         dsl.copy_(host_sl, non_blocking=True)
-        pa.paged_attn_decode(dq, ks[i % reps], vs[i % reps], dbt, dsl, w.scale, out=out,
-                             stream=stream)
+        if host_kn is not None:
+            dkn.copy_(host_kn, non_blocking=True)
+            dvn.copy_(host_vn, non_blocking=True)
+        run_op(dq, dbt, dsl, ks[i % reps], vs[i % reps], dkn, dvn)
         host_out.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -340,13 +369,15 @@ def run_ours(args, world, rank, local):
         e2e_step(i)
     e2e_time = reduce_max((time.perf_counter() - t) / e2e_steps, world)
     h2d = host_q.numel() * 2 + host_bt.numel() * 4 + host_sl.numel() * 4
+    if host_kn is not None:
+        h2d += (host_kn.numel() + host_vn.numel()) * 2
     d2h = host_out.numel() * 2
 
     result = None
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = nbytes["total"] / kernel_s / 1e9
-        traffic = profile_traffic(args.config)
+        traffic = profile_traffic(args.config) if op == "decode" else None
         cpu = None
         if not args.no_cpu_baseline:
             w_host = workloads.host_copy(w)
@@ -379,7 +410,7 @@ def run_ours(args, world, rank, local):
                 "name": args.config,
                 "num_seqs": spec.num_seqs, "H_q": spec.H_q, "H_kv": spec.H_kv,
                 "head_dim": spec.D, "block_size": spec.block_size,
-                "tokens": int(sum(lens)), "seed": seed,
+                "tokens": int(sum(lens)), "seed": seed, "op": op,
                 "bytes_per_step": nbytes,
                 "l2": f"inputs larger than L2: {reps} KV-cache replicas rotated "
                       f"({reps * kv_bytes / 1e9:.2f} GB vs 129 MB L2)",
@@ -390,7 +421,11 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback 6800 GB/s",
-                "kernel": "paged_decode_kernel (one launch per step, fused combine)",
+                "kernel": {"decode": "paged_decode_kernel (one launch per step, fused combine)",
+                           "append_decode": "paged_decode_kernel with the fused cache append "
+                                            "(one launch per step)",
+                           "append_then_decode": "paged_kv_append_kernel + paged_decode_kernel "
+                                                 "(two launches per step)"}[op],
                 "kernel_us": round(kernel_s * 1e6, 2),
                 "timing": f"CUDA events around {j} of the {steps} timed launches",
             },
@@ -463,6 +498,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="llama8b", choices=sorted(workloads.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="decode",
+                    choices=["decode", "append_decode", "append_then_decode"],
+                    help="decode alone, or with each sequence's new token appended to the "
+                         "cache first (fused into the decode launch, or a separate launch)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

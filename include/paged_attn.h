@@ -182,11 +182,16 @@ PAGED_ATTN_API int paged_kv_append(const void* k_new, const void* v_new, void* k
 
 /*
  * paged_kv_append followed by paged_attn_decode, fused into the decode launch:
- * the CTA that reads the page holding a sequence's new token writes that
- * token's K and V rows first (while its first pages are in flight), so the
+ * the warp that processes the page holding a sequence's new token puts that
+ * token's K and V rows into its copy of the page in shared memory (whatever
+ * the cache held there is not used) and stores them to the cache, so the
  * append costs no extra launch and no extra pass over the cache.  The blocks
  * that receive the new tokens must not also be read by another sequence of
- * the same call (no copy-on-write sharing of a partly filled block).  Same
+ * the same call (no copy-on-write sharing of a partly filled block).  When the
+ * batch has many (sequence, KV head) pairs per SM (four or more per CTA of the
+ * persistent grid), the per-piece patch would sit on the critical path of the
+ * CTA crossing the most short sequences, and the call instead runs the append
+ * as its own launch just ahead of the decode; the result is the same.  Same
  * arguments, workspace and errors as paged_attn_decode, plus k_new / v_new
  * ([num_seqs, H_kv, head_dim] bf16, 16-byte aligned).
  */

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   constexpr int kTG = BS / 16;        // 16-token groups per page
   constexpr int kQRows = 8 * kNH;                 // query rows one tile holds
   constexpr int kQTileBytes = kQRows * D * 2;     // = lay.q_tile_bytes()
+  constexpr int kQSlotBytes = (kQTileBytes + 4 * D + 16 + 127) / 128 * 128;  // = lay.q_slot_bytes()
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -178,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
-  uint64_t* append_bar = comb_bar + 1;         // the fused append's rows are written
   float* sm_m = reinterpret_cast<float*>(smem + lay.merge_m());
   float* sm_l = reinterpret_cast<float*>(smem + lay.merge_l());
   float* sm_final = reinterpret_cast<float*>(smem + lay.final_ml());  // [0,16) M, [16,32) L
@@ -281,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       mbar_init(&empty_bar[i], 1);
     }
     mbar_init(comb_bar, 1);
-    mbar_init(append_bar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -294,23 +293,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     const int issue_lanes = min(kMaxIssueLanes, p.stages);
     Walker wk;
     if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_kv);
-    auto fetch = [&](long long u) -> int3 {
-      // physical block and KV head of this lane's unit (block -1 past the range),
-      // and whether the unit is the last page of its (s, g)
-      if (u >= u1) return make_int3(-1, 0, 0);
+    auto fetch = [&](long long u) -> int2 {
+      // physical block and KV head of this lane's unit (block -1 past the range)
+      if (u >= u1) return make_int2(-1, 0);
       int pb = __ldg(p.block_tables + (size_t)wk.s * p.maxb + wk.p);
       if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
         atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
-      return make_int3(pb, wk.g, wk.p == wk.n - 1 ? 1 : 0);
+      return make_int2(pb, wk.g);
     };
-    // With a fused append, the last page of a piece may only be read once the
-    // consumer warps have written the new token's rows (append_bar).
-    bool append_pending = p.k_new != nullptr;
-    int3 cur = fetch(u0 + lane);
+    int2 cur = fetch(u0 + lane);
     bool abort = false;
     for (long long ub = u0; ub < u1 && !abort; ub += 32) {
       // advance this lane's walker to its unit of the next batch and start that load
-      int3 nxt = make_int3(-1, 0, 0);
+      int2 nxt = make_int2(-1, 0);
       if (ub + 32 + lane < u1) {
         wk.advance(32, sm_prefix, N, H_kv);
         nxt = fetch(ub + 32 + lane);
@@ -320,19 +315,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         const int j = j0 + (lane < issue_lanes ? lane : 0);
         const int pb = __shfl_sync(0xffffffffu, cur.x, j);
         const int g = __shfl_sync(0xffffffffu, cur.y, j);
-        const int last_page = __shfl_sync(0xffffffffu, cur.z, j);
         bool bad = false;
-        if (append_pending &&
-            __any_sync(0xffffffffu, lane < issue_lanes && j0 + lane < cnt && last_page)) {
-          bool ok = true;
-          if (lane == 0) ok = mbar_wait(append_bar, 0);
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
-            bad = true;
-          }
-          append_pending = false;
-        }
-        if (lane < issue_lanes && j0 + lane < cnt && !bad) {
+        if (lane < issue_lanes && j0 + lane < cnt) {
           const long long i = ub - u0 + j;  // unit index within this CTA
           const int stage = (int)(i % p.stages);
           const uint32_t phase = (uint32_t)((i / p.stages) & 1);
@@ -379,9 +363,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   // The query group of a piece lives in one of two shared tiles
   // [16 heads][D] (16-byte chunk c of head h at c ^ (h % 8) within each 128
   // bytes; heads >= G are zero) and is fetched one piece ahead with cp.async.
+  // With the fused cache append the slot also receives the piece's new K and V
+  // rows and the block id of its last page, so the warp that patches that page
+  // finds them in shared memory.
   auto prefetch_q = [&](int buf, int s, int g) {
     const __nv_bfloat16* qg = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
-    uint8_t* tile = sm_q + buf * kQTileBytes;
+    uint8_t* tile = sm_q + buf * kQSlotBytes;
     for (int i = ctid; i < kQRows * (D / 8); i += kConsumerThreads) {
       const int h = i / (D / 8);
       const int c = i - h * (D / 8);
@@ -391,6 +378,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
                   live ? static_cast<const void*>(qg + (size_t)h * D + c * 8)
                        : static_cast<const void*>(p.q),
                   live ? 16 : 0);
+    }
+    if (p.k_new != nullptr) {
+      const size_t row = ((size_t)s * H_kv + g) * D;
+      for (int i = ctid; i < D / 4; i += kConsumerThreads) {  // K then V, 16 bytes each
+        const bool is_v = i >= D / 8;
+        const int c = is_v ? i - D / 8 : i;
+        cp_async_16(tile + kQTileBytes + (is_v ? 2 * D : 0) + c * 16,
+                    (is_v ? p.v_new : p.k_new) + row + c * 8, 16);
+      }
+      if (ctid == kConsumerThreads - 1) {
+        const int last_page = sm_prefix[s + 1] - sm_prefix[s] - 1;
+        cp_async_4(tile + kQTileBytes + 4 * D, p.block_tables + (size_t)s * p.maxb + last_page);
+      }
     }
     cp_async_commit();
   };
@@ -837,80 +837,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
   ahead = next_piece(ahead);
-  if (p.k_new != nullptr) {
-    // ---- fused cache append.  The new token of each (s, g) whose last page
-    // lies in this range is written here, while the first pages are in
-    // flight: each such page is read by this CTA alone, and only after
-    // append_bar.  Thread 0 lists the rows in the (idle) merge buffer, every
-    // consumer thread moves 16-byte chunks of them (loads first, then stores),
-    // and each writer fences its stores against the tensor copies that will
-    // read them.
-    int* const list = reinterpret_cast<int*>(sm_o);   // s * H_kv + g
-    const int list_cap = kConsumerWarps * G * kRowStride;
-    int* const sm_cnt = sm_flag + 16;                 // [0] rows listed, [1] more to list
-    int cs = wk.s, cg = wk.g;                          // thread 0's piece cursor
-    constexpr int kChunks = 2 * (D / 8);               // 16-byte chunks of a K row + V row
-    for (;;) {
-      if (ctid == 0) {
-        int n = 0;
-        bool more = false;
-        while (cs < N) {
-          const int np = sm_prefix[cs + 1] - sm_prefix[cs];
-          const long long sb = (long long)sm_prefix[cs] * H_kv + (long long)cg * np;
-          if (sb >= u1) break;
-          if (n == list_cap) {
-            more = true;
-            break;
-          }
-          if (sb + np - 1 < u1) list[n++] = cs * H_kv + cg;  // its last page is here
-          if (++cg == H_kv) {
-            cg = 0;
-            do {
-              ++cs;
-            } while (cs < N && sm_prefix[cs + 1] == sm_prefix[cs]);
-          }
-        }
-        sm_cnt[0] = n;
-        sm_cnt[1] = more ? 1 : 0;
-      }
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);
-      const int n = sm_cnt[0];
-      const bool more = sm_cnt[1] != 0;
-      for (int c0 = ctid; c0 < n * kChunks; c0 += 4 * kConsumerThreads) {
-        uint4 v[4];
-        uint4* dst[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = c0 + k * kConsumerThreads;
-          dst[k] = nullptr;
-          if (c < n * kChunks) {
-            const int row = list[c / kChunks];
-            const int ch = c % kChunks;
-            const int s = row / H_kv, g = row - (row / H_kv) * H_kv;
-            const int kv = ch / (D / 8), off = (ch % (D / 8)) * 8;
-            const int t = sm_len[s] - 1;
-            const int b = __ldg(p.block_tables + (size_t)s * p.maxb + t / BS);
-            if (p.num_blocks > 0 && (b < 0 || (long long)b >= p.num_blocks)) continue;
-            v[k] = __ldg(reinterpret_cast<const uint4*>(
-                (kv ? p.v_new : p.k_new) + ((size_t)s * H_kv + g) * D + off));
-            dst[k] = reinterpret_cast<uint4*>(
-                (kv ? p.v_cache : p.k_cache) + (((size_t)b * H_kv + g) * BS + t % BS) * D + off);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (dst[k] != nullptr) *dst[k] = v[k];
-      }
-      __syncwarp();
-      named_barrier(kConsumerBarrier, kConsumerThreads);  // the list may be refilled
-      if (!more) break;
-    }
-    fence_proxy_async_global();
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-    if (ctid == 0) mbar_arrive(append_bar);
-  }
   cp_async_wait_all();
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);
@@ -923,6 +849,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     // waits on its slots' phases strictly in order (a parity wait cannot tell
     // phase k from phase k - 2) whatever the ring depth.
     if (stage % kConsumerWarps == warp && !abort) {
+      // Fused cache append: the last page of a piece holds the sequence's new
+      // token.  Its rows (prefetched with the piece's query group) are patched
+      // into the page in shared memory once the page has landed (the tensor
+      // copy brought whatever the cache held) and stored to the cache for later
+      // calls.  This page is read by this CTA alone.
+      const bool patch = p.k_new != nullptr && wk.p == wk.n - 1;
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.
@@ -932,8 +864,33 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         abort = true;
       } else {
         const int valid = min(BS, sm_len[wk.s] - wk.p * BS);
-        const uint8_t* st = smem + stage * kStageBytes;
-        process_page(st, st + kPageBytes, sm_q + qbuf * kQTileBytes, valid);
+        uint8_t* st = smem + stage * kStageBytes;
+        const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
+        if (patch) {
+          const int slot = valid - 1;  // the new token, t = L - 1
+          if (lane < D / 8) {
+            // 16-byte chunk `lane` of the row: half lane / 8, swizzled position within it
+            const int off = (lane >> 3) * kTileBytes + slot * 128 + (((lane & 7) ^ (slot & 7)) << 4);
+            *reinterpret_cast<uint4*>(st + off) = reinterpret_cast<const uint4*>(extra)[lane];
+            *reinterpret_cast<uint4*>(st + kPageBytes + off) =
+                reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
+          }
+          __syncwarp();
+        }
+        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
+        if (patch) {
+          // the patch's generic writes precede the next tensor copy into this slot
+          fence_proxy_async_shared();
+          const int slot = valid - 1;
+          const int new_block = *reinterpret_cast<const int*>(extra + 4 * D);
+          if (lane < D / 8 &&
+              (p.num_blocks <= 0 || (new_block >= 0 && (long long)new_block < p.num_blocks))) {
+            const size_t dst = (((size_t)new_block * H_kv + wk.g) * BS + slot) * D + lane * 8;
+            *reinterpret_cast<uint4*>(p.k_cache + dst) = reinterpret_cast<const uint4*>(extra)[lane];
+            *reinterpret_cast<uint4*>(p.v_cache + dst) =
+                reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
       }

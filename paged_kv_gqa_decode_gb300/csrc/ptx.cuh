@@ -109,13 +109,6 @@ __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
 }
 
-// Orders this thread's earlier generic-proxy global-memory writes before later
-// async-proxy (tensor copy) reads of them, by this or (after a barrier) any
-// thread of the CTA.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_shared() {
@@ -129,6 +122,11 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
                "r"(src_bytes)
+               : "memory");
+}
+// 4-byte asynchronous global -> shared copy.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {

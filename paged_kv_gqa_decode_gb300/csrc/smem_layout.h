@@ -31,19 +31,22 @@ struct SmemLayout {
   int stages, G, num_seqs;
   // [0, bars): the ring of `stages` K/V pages (at the end of a range it holds the
   // partial states being combined); then the mbarriers full[stages],
-  // empty[stages], one for the combine's copies and one for the fused append
+  // empty[stages] and one for the combine's copies
   PAGEDATTN_HD int bars() const { return stages * kStageBytes; }
-  PAGEDATTN_HD int merge_m() const { return align_up(bars() + (2 * stages + 2) * 8, 128); }
+  PAGEDATTN_HD int merge_m() const { return align_up(bars() + (2 * stages + 1) * 8, 128); }
   PAGEDATTN_HD int merge_l() const { return merge_m() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int flag() const { return final_ml() + 32 * 4; }  // a few ints
   PAGEDATTN_HD int merge_o() const { return flag() + 128; }
   // one query tile: the group's rows padded to 8 (G <= 8) or 16 heads
   PAGEDATTN_HD int q_tile_bytes() const { return (G > 8 ? 16 : 8) * D * 2; }
-  PAGEDATTN_HD int qtile() const {  // two query tiles
+  // one query slot: the tile, then (fused cache append) the piece's new K row,
+  // new V row and the block id of its last page
+  PAGEDATTN_HD int q_slot_bytes() const { return align_up(q_tile_bytes() + 4 * D + 16, 128); }
+  PAGEDATTN_HD int qtile() const {  // two query slots
     return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
   }
-  PAGEDATTN_HD int prefix() const { return qtile() + 2 * q_tile_bytes(); }
+  PAGEDATTN_HD int prefix() const { return qtile() + 2 * q_slot_bytes(); }
   PAGEDATTN_HD int lens() const { return prefix() + align_up((num_seqs + 1) * 4, 128); }
   PAGEDATTN_HD int total() const { return lens() + num_seqs * 4; }
 };

@@ -108,10 +108,12 @@ def test_one_token_sequences_decode_to_their_new_v():
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
 
 
-def test_many_short_sequences_fill_the_append_list():
-    # 700 short sequences x 8 KV heads: some CTAs own more new rows than one pass lists
-    lens = list(np.random.default_rng(25).integers(0, 40, size=700))
-    sp = workloads.custom_spec("short", len(lens), 8, 8, 64, 16, lens, max_len=48)
+@pytest.mark.parametrize("num_seqs,H_kv", [(1100, 1), (700, 8)])
+def test_many_short_sequences(num_seqs, H_kv):
+    # 1100 x 1 KV head: fused, nearly every page is the last of its piece;
+    # 700 x 8: enough pieces per CTA that the call runs the append apart
+    lens = list(np.random.default_rng(25).integers(0, 40, size=num_seqs))
+    sp = workloads.custom_spec("short", len(lens), 8, H_kv, 64, 16, lens, max_len=48)
     w = workloads.make(sp, seed=25, device="cuda", poison="nan")
     k_new, v_new = new_rows(w, 9)
     exp = expected(w, k_new, v_new)

@@ -35,7 +35,7 @@ void run() {
         const L l{st, G, n};
         CHECK(l.bars() % 1024 == 0, "bars D%d BS%d st%d\n", D, BS, st);
         CHECK(L::kStageBytes % 1024 == 0, "stage size D%d BS%d\n", D, BS);
-        CHECK(l.merge_m() >= l.bars() + (2 * st + 2) * 8, "barrier overlap\n");
+        CHECK(l.merge_m() >= l.bars() + (2 * st + 1) * 8, "barrier overlap\n");
         const int starts[] = {l.merge_m(), l.merge_l(), l.final_ml(), l.flag(), l.merge_o(),
                               l.qtile(), l.prefix(), l.lens()};
         for (int x : starts)
@@ -45,7 +45,8 @@ void run() {
         CHECK(l.flag() - l.final_ml() >= 32 * 4, "final size\n");
         CHECK(l.merge_o() - l.flag() >= 4 * 4, "flag size\n");
         CHECK(l.qtile() - l.merge_o() >= kConsumerWarps * G * L::kRowStride * 4, "merge_o size\n");
-        CHECK(l.prefix() - l.qtile() >= 2 * (G > 8 ? 16 : 8) * D * 2, "qtile size\n");
+        CHECK(l.prefix() - l.qtile() >= 2 * ((G > 8 ? 16 : 8) * D * 2 + 4 * D + 4), "qtile size\n");
+        CHECK(l.q_slot_bytes() % 128 == 0, "q slot\n");
         CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
         CHECK(l.lens() - l.prefix() >= (n + 1) * 4, "prefix size\n");
