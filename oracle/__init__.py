@@ -10,6 +10,8 @@ imports this package, and this package imports nothing from it.
 * ``pieces``       -- the per-range softmax pieces (M, l, o) of rows.
 * ``append``       -- the cache write of each sequence's new token (the step
                       before the decode).
+* ``decode_fp8``   -- the definition over FP8 caches (e4m3 bytes and a dequant
+                      float per cache row).
 * ``combine`` / ``finish`` -- the merge of two partial softmax states and the
                       final normalisation, as "Paged Attention Kernel
                       Architecture for BI-V100" (section 2, Level 1: the
@@ -83,6 +85,11 @@ def _load():
             lib.oracle_partial_pairs.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F, P, P, I,
                                                  P, P, P]
             lib.oracle_partial_pairs.restype = I
+            lib.oracle_decode_fp8_pairs.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, LL, F,
+                                                     P, I, P, I]
+            lib.oracle_decode_fp8_pairs.restype = I
+            lib.oracle_e4m3_table.argtypes = [P]
+            lib.oracle_e4m3_table.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             _lib = lib
@@ -172,6 +179,76 @@ def decode(x, pairs: Optional[Sequence[Sequence[int]]] = None, num_threads: int 
                                      int(num_threads))
     if rc != 0:
         raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return out
+
+
+class Fp8Inputs:
+    """Host views of one decode problem over FP8 caches: e4m3 bytes in the bf16
+    layout plus one float per (block, KV head, slot) for K and for V."""
+
+    def __init__(self, q, k8, v8, k_scale, v_scale, block_tables, seq_lens, scale: float):
+        self.q = _bits(q)
+        self.k8 = _u8(k8)
+        self.v8 = _u8(v8)
+        self.ks = _f32(k_scale)
+        self.vs = _f32(v_scale)
+        self.bt = _i32(block_tables)
+        self.lens = _i32(seq_lens)
+        if self.q.ndim != 3 or self.k8.ndim != 4 or self.k8.shape != self.v8.shape:
+            raise ValueError("q must be [S,H_q,D] and the caches [NB,H_kv,BS,D]")
+        self.num_seqs, self.H_q, self.D = self.q.shape
+        self.num_blocks, self.H_kv, self.BS, Dk = self.k8.shape
+        if Dk != self.D:
+            raise ValueError("head_dim of q and of the caches differ")
+        if self.ks.shape != self.k8.shape[:3] or self.vs.shape != self.ks.shape:
+            raise ValueError("scales must be [NB, H_kv, BS]")
+        self.maxb = self.bt.shape[1]
+        self.scale = float(np.float32(scale))
+
+    @classmethod
+    def from_workload(cls, w) -> "Fp8Inputs":
+        return cls(w.q, w.k8, w.v8, w.k_scale, w.v_scale, w.block_tables, w.seq_lens, w.scale)
+
+
+def _u8(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.uint8)
+    import torch
+
+    return x.detach().cpu().contiguous().view(torch.uint8).numpy()
+
+
+def _f32(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float32)
+    return np.ascontiguousarray(x.detach().cpu().float().numpy(), dtype=np.float32)
+
+
+def decode_fp8(x, pairs: Optional[Sequence[Sequence[int]]] = None,
+               num_threads: int = 0) -> np.ndarray:
+    """The definition over FP8 caches in float64: every K/V element is its e4m3
+    value times the float of its (block, KV head, slot) row; see the C source."""
+    inp = x if isinstance(x, Fp8Inputs) else Fp8Inputs.from_workload(x)
+    if pairs is None:
+        pr = np.stack(np.meshgrid(np.arange(inp.num_seqs), np.arange(inp.H_q), indexing="ij"),
+                      axis=-1).reshape(-1, 2).astype(np.int32)
+    else:
+        pr = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+    pr = np.ascontiguousarray(pr)
+    out = np.zeros((pr.shape[0], inp.D), dtype=np.float64)
+    rc = _load().oracle_decode_fp8_pairs(
+        _ptr(inp.q), _ptr(inp.k8), _ptr(inp.v8), _ptr(inp.ks), _ptr(inp.vs), _ptr(inp.bt),
+        _ptr(inp.lens), inp.num_seqs, inp.H_q, inp.H_kv, inp.D, inp.maxb, inp.BS,
+        inp.num_blocks, inp.scale, _ptr(pr), pr.shape[0], _ptr(out), int(num_threads))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return out if pairs is not None else out.reshape(inp.num_seqs, inp.H_q, inp.D)
+
+
+def e4m3_table() -> np.ndarray:
+    """The oracle's e4m3 decoding of the 256 byte codes."""
+    out = np.zeros(256, dtype=np.float64)
+    _load().oracle_e4m3_table(_ptr(out))
     return out
 
 

@@ -33,6 +33,15 @@
  *   scale is the float the caller passes, widened to double.  L = 0 gives a
  *   zero row (the pages never define an empty softmax; this is the reading
  *   the library documents).
+ *
+ *   FP8 caches (the nvfp4-megamoe README, "Stage D: FP8 Paged KV Gather" and
+ *   "FP8 KV Quantize/Dequant": e4m3 values with a dequant scale per position)
+ *   hold e4m3 bytes in the same layout plus one float per (block, KV head,
+ *   slot) for K and for V; an element is its e4m3 value times that float:
+ *     K_t[d] = e4m3(k8[bt[s, t / BS], g, t % BS, d]) * k_scale[bt[s, t / BS], g, t % BS]
+ *   and everything else is the definition above.  e4m3 is the OCP 8-bit
+ *   format with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa bits,
+ *   subnormals at exponent 0, no infinities, S.1111.111 = NaN (max 448).
  */
 #include <math.h>
 #include <stdint.h>
@@ -54,6 +63,34 @@ static double widen_bf16(uint16_t bits) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* The e4m3 value of one byte, decoded from its bit fields. */
+static double e4m3_value(uint8_t b) {
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* A paged K/V cache pair: bf16 elements, or e4m3 bytes with a float per row. */
+typedef struct {
+    const uint16_t* k16;
+    const uint16_t* v16;
+    const uint8_t* k8;
+    const uint8_t* v8;
+    const float* k_scale; /* [num_blocks * H_kv * BS] */
+    const float* v_scale;
+} Cache;
+
+/* Element d of cache row `row` = (block * H_kv + g) * BS + slot. */
+static double cache_k(const Cache* c, size_t row, int d, int D) {
+    if (c->k16) return widen_bf16(c->k16[row * D + d]);
+    return e4m3_value(c->k8[row * D + d]) * (double)c->k_scale[row];
+}
+static double cache_v(const Cache* c, size_t row, int d, int D) {
+    if (c->v16) return widen_bf16(c->v16[row * D + d]);
+    return e4m3_value(c->v8[row * D + d]) * (double)c->v_scale[row];
 }
 
 /* Validate the sequence lengths and every block-table entry a sequence uses. */
@@ -79,10 +116,9 @@ static int check_inputs(const int32_t* bt, const int32_t* seq_lens, int num_seqs
  *   M = max_t z_t,  l = sum_t exp(z_t - M),  o[d] = sum_t exp(z_t - M) V_t[d].
  * An empty range gives M = -inf, l = 0, o = 0.  z is scratch of >= t1 - t0 doubles.
  */
-static void row_pieces(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                       const int32_t* bt, int s, int h, int H_q, int H_kv, int D, int max_blocks,
-                       int BS, double scale, int t0, int t1, double* z, double* M_out,
-                       double* l_out, double* o) {
+static void row_pieces(const uint16_t* q, const Cache* c, const int32_t* bt, int s, int h,
+                       int H_q, int H_kv, int D, int max_blocks, int BS, double scale, int t0,
+                       int t1, double* z, double* M_out, double* l_out, double* o) {
     const int g = (int)(((long long)h * H_kv) / H_q);
     const uint16_t* qrow = q + ((size_t)s * H_q + h) * D;
 
@@ -94,9 +130,9 @@ static void row_pieces(const uint16_t* q, const uint16_t* k_cache, const uint16_
     /* z_t = scale * q . K_t, K_t reached through the block table */
     for (int t = t0; t < t1; ++t) {
         const size_t pb = (size_t)bt[(size_t)s * max_blocks + t / BS];
-        const uint16_t* krow = k_cache + ((pb * H_kv + g) * BS + (size_t)(t % BS)) * D;
+        const size_t krow = (pb * H_kv + g) * BS + (size_t)(t % BS);
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += widen_bf16(qrow[d]) * widen_bf16(krow[d]);
+        for (int d = 0; d < D; ++d) dot += widen_bf16(qrow[d]) * cache_k(c, krow, d, D);
         z[t - t0] = scale * dot;
     }
 
@@ -108,21 +144,20 @@ static void row_pieces(const uint16_t* q, const uint16_t* k_cache, const uint16_
         const double w = exp(z[t - t0] - M);
         l += w;
         const size_t pb = (size_t)bt[(size_t)s * max_blocks + t / BS];
-        const uint16_t* vrow = v_cache + ((pb * H_kv + g) * BS + (size_t)(t % BS)) * D;
-        for (int d = 0; d < D; ++d) o[d] += w * widen_bf16(vrow[d]);
+        const size_t vrow = (pb * H_kv + g) * BS + (size_t)(t % BS);
+        for (int d = 0; d < D; ++d) o[d] += w * cache_v(c, vrow, d, D);
     }
     *M_out = M;
     *l_out = l;
 }
 
 /* One (s, h) row of the definition: out = o / l over the whole sequence. */
-static void attend_row(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                       const int32_t* bt, const int32_t* seq_lens, int s, int h, int H_q,
-                       int H_kv, int D, int max_blocks, int BS, double scale, double* z,
-                       double* out_row) {
+static void attend_row(const uint16_t* q, const Cache* c, const int32_t* bt,
+                       const int32_t* seq_lens, int s, int h, int H_q, int H_kv, int D,
+                       int max_blocks, int BS, double scale, double* z, double* out_row) {
     double M, l;
-    row_pieces(q, k_cache, v_cache, bt, s, h, H_q, H_kv, D, max_blocks, BS, scale, 0,
-               seq_lens[s], z, &M, &l, out_row);
+    row_pieces(q, c, bt, s, h, H_q, H_kv, D, max_blocks, BS, scale, 0, seq_lens[s], z, &M, &l,
+               out_row);
     if (l > 0.0)
         for (int d = 0; d < D; ++d) out_row[d] /= l;
 }
@@ -131,11 +166,11 @@ static void attend_row(const uint16_t* q, const uint16_t* k_cache, const uint16_
  * Rows listed in `pairs` ([num_pairs][2] = (s, h)); out is [num_pairs, D].
  * num_threads <= 0 uses the OpenMP default.  Returns 0 or a negative code.
  */
-int oracle_decode_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
-                        int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
-                        long long num_blocks, float scale, const int32_t* pairs, int num_pairs,
-                        double* out, int num_threads) {
+static int decode_pairs(const uint16_t* q, const Cache* c, const int32_t* block_tables,
+                        const int32_t* seq_lens, int num_seqs, int H_q, int H_kv, int D,
+                        int max_blocks_per_seq, int block_size, long long num_blocks,
+                        float scale, const int32_t* pairs, int num_pairs, double* out,
+                        int num_threads) {
     int rc = check_inputs(block_tables, seq_lens, num_seqs, H_q, H_kv, D, max_blocks_per_seq,
                           block_size, num_blocks);
     if (rc != ORACLE_OK) return rc;
@@ -168,13 +203,42 @@ int oracle_decode_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16
                 failed = 1;
                 continue;
             }
-            attend_row(q, k_cache, v_cache, block_tables, seq_lens, pairs[2 * i],
-                       pairs[2 * i + 1], H_q, H_kv, D, max_blocks_per_seq, block_size, sc, z,
-                       out + (size_t)i * D);
+            attend_row(q, c, block_tables, seq_lens, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv,
+                       D, max_blocks_per_seq, block_size, sc, z, out + (size_t)i * D);
         }
         free(z);
     }
     return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+int oracle_decode_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                        int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                        long long num_blocks, float scale, const int32_t* pairs, int num_pairs,
+                        double* out, int num_threads) {
+    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+    return decode_pairs(q, &c, block_tables, seq_lens, num_seqs, H_q, H_kv, D,
+                        max_blocks_per_seq, block_size, num_blocks, scale, pairs, num_pairs, out,
+                        num_threads);
+}
+
+/* The same rows over FP8 caches (e4m3 bytes and per-row dequant floats). */
+int oracle_decode_fp8_pairs(const uint16_t* q, const uint8_t* k8, const uint8_t* v8,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                            int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
+                            long long num_blocks, float scale, const int32_t* pairs,
+                            int num_pairs, double* out, int num_threads) {
+    if (!k8 || !v8 || !k_scale || !v_scale) return ORACLE_ERR_ARGS;
+    const Cache c = {NULL, NULL, k8, v8, k_scale, v_scale};
+    return decode_pairs(q, &c, block_tables, seq_lens, num_seqs, H_q, H_kv, D,
+                        max_blocks_per_seq, block_size, num_blocks, scale, pairs, num_pairs, out,
+                        num_threads);
+}
+
+/* e4m3 values of the 256 byte codes (for checking the decoder). */
+void oracle_e4m3_table(double* out) {
+    for (int b = 0; b < 256; ++b) out[b] = e4m3_value((uint8_t)b);
 }
 
 /* Every row: out is [num_seqs, H_q, D]. */
@@ -230,9 +294,10 @@ int oracle_partial_pairs(const uint16_t* q, const uint16_t* k_cache, const uint1
     }
     double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
     if (!z) return ORACLE_ERR_NOMEM;
+    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
     for (int i = 0; i < num_pairs; ++i)
-        row_pieces(q, k_cache, v_cache, block_tables, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv,
-                   D, max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],
+        row_pieces(q, &c, block_tables, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv, D,
+                   max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],
                    ranges[2 * i + 1], z, M + i, l + i, o + (size_t)i * D);
     free(z);
     return ORACLE_OK;

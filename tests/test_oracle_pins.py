@@ -287,14 +287,15 @@ MUTANTS = [
     ("kv head h % H_kv", "(int)(((long long)h * H_kv) / H_q)", "(h % H_kv)"),
     ("scale dropped", "z[t - t0] = scale * dot;", "z[t - t0] = dot;"),
     ("page index from t % BS", "bt[(size_t)s * max_blocks + t / BS]", "bt[(size_t)s * max_blocks + t % BS]"),
-    ("slot index from t / BS", "+ (size_t)(t % BS)) * D;", "+ (size_t)(t / BS)) * D;"),
+    ("slot index from t / BS", "(pb * H_kv + g) * BS + (size_t)(t % BS);",
+     "(pb * H_kv + g) * BS + (size_t)(t / BS);"),
     ("max not subtracted", "exp(z[t - t0] - M)", "exp(z[t - t0])"),
     ("softmax sign flipped", "exp(z[t - t0] - M)", "exp(M - z[t - t0])"),
     ("last token dropped", "for (int t = t0; t < t1; ++t) {\n        const double w",
      "for (int t = t0; t < t1 - 1; ++t) {\n        const double w"),
     ("no normalisation", "out_row[d] /= l;", "out_row[d] /= 1.0;"),
-    ("K row reversed", "widen_bf16(qrow[d]) * widen_bf16(krow[d])",
-     "widen_bf16(qrow[d]) * widen_bf16(krow[D - 1 - d])"),
+    ("K row reversed", "widen_bf16(qrow[d]) * cache_k(c, krow, d, D)",
+     "widen_bf16(qrow[d]) * cache_k(c, krow, D - 1 - d, D)"),
     ("query head from kv head", "qrow = q + ((size_t)s * H_q + h) * D",
      "qrow = q + ((size_t)s * H_q + g) * D"),
 ]
@@ -486,3 +487,102 @@ def test_append_pins_catch_planted_mistakes(name, old, new):
 
 def test_unmutated_append_passes_the_same_pins():
     assert _append_pins_pass(oracle.append)
+
+
+# ---------------------------------------------------------------- FP8 caches
+
+def test_e4m3_decoding_matches_torch_float8():
+    """Every byte code decodes as torch's float8_e4m3fn does (NaN codes included)."""
+    t = oracle.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(t), np.isnan(ref))
+    assert np.array_equal(t[~np.isnan(t)], ref[~np.isnan(ref)])
+
+
+def _fp8_with_exact_bf16_twin(seed=0, lens=(1, 15, 16, 17, 40), H_q=8, H_kv=2, D=64, BS=16):
+    """An FP8 problem with random finite e4m3 codes and power-of-two row floats,
+    and the bf16 problem holding exactly the same values (e4m3 x 2^k is exact in
+    bf16), built without the oracle's decoder: through torch's float8 type."""
+    spec = workloads.custom_spec("fp8twin", len(lens), H_q, H_kv, D, BS, list(lens))
+    w = workloads.make(spec, seed=seed, poison="none")
+    rng = np.random.default_rng(seed)
+    shape = tuple(w.k_cache.shape)
+    codes = rng.integers(0, 256, size=(2,) + shape, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes (0x38 = 1.0)
+    scales = np.ldexp(1.0, rng.integers(-6, 7, size=(2,) + shape[:3])).astype(np.float32)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double() * \
+        torch.from_numpy(scales).double().unsqueeze(-1)
+    k16, v16 = vals[0].to(torch.bfloat16), vals[1].to(torch.bfloat16)
+    assert torch.equal(k16.double(), vals[0]) and torch.equal(v16.double(), vals[1])
+    bf = oracle.Inputs(w.q, k16, v16, w.block_tables, w.seq_lens, w.scale)
+    f8 = oracle.Fp8Inputs(w.q, codes[0], codes[1], scales[0], scales[1], w.block_tables,
+                          w.seq_lens, w.scale)
+    return f8, bf
+
+
+def test_fp8_decode_equals_bf16_decode_of_the_same_values():
+    for seed in range(3):
+        f8, bf = _fp8_with_exact_bf16_twin(seed)
+        assert np.array_equal(oracle.decode_fp8(f8), oracle.decode(bf))
+
+
+def test_fp8_row_floats_scale_as_stated():
+    f8, _ = _fp8_with_exact_bf16_twin(7)
+    base = oracle.decode_fp8(f8)
+    f8.vs = f8.vs * np.float32(4.0)        # every V row x4: the output x4
+    assert np.allclose(oracle.decode_fp8(f8), 4.0 * base, rtol=1e-12, atol=0)
+    f8.vs = f8.vs / np.float32(4.0)
+    f8.ks = f8.ks * np.float32(2.0)        # every K row x2 == softmax scale x2
+    twice = oracle.decode_fp8(f8)
+    f8.ks = f8.ks / np.float32(2.0)
+    f8.scale = float(np.float32(2.0 * f8.scale))
+    assert np.allclose(twice, oracle.decode_fp8(f8), rtol=1e-12, atol=1e-15)
+
+
+def _fp8_pins_pass() -> bool:
+    try:
+        test_e4m3_decoding_matches_torch_float8()
+        test_fp8_decode_equals_bf16_decode_of_the_same_values()
+        test_fp8_row_floats_scale_as_stated()
+    except (AssertionError, oracle.OracleError, FloatingPointError):
+        return False
+    return True
+
+
+FP8_MUTANTS = [
+    ("exponent bias 8", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("subnormal scale", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    ("sign dropped", "return sign ? -v : v;", "return v;"),
+    ("K row float from V", "* (double)c->k_scale[row];", "* (double)c->v_scale[row];"),
+    ("row float of the next row", "* (double)c->v_scale[row];", "* (double)c->v_scale[row + 1];"),
+    ("mantissa 4 bits", "(double)m / 8.0, e - 7", "(double)m / 16.0, e - 7"),
+]
+
+_FP8_MUTANT_RUNNER = _MUTANT_RUNNER.replace(
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs")',
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs", '
+    '"oracle_decode_fp8_pairs", "oracle_e4m3_table")').replace(
+    "T._pins_pass()", "T._fp8_pins_pass()")
+
+
+@pytest.mark.parametrize("name,old,new", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_pins_catch_planted_mistakes(name, old, new, tmp_path):
+    import subprocess
+    import sys
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, name
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _FP8_MUTANT_RUNNER.format(root=os.path.dirname(here), tests=here, so=str(so))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode < 0 or "PINS_FAIL" in r.stdout, \
+        f"no pin noticed the planted mistake: {name}\n{r.stdout}\n{r.stderr[-2000:]}"
+
+
+def test_unmutated_oracle_passes_the_fp8_pins():
+    assert _fp8_pins_pass()

@@ -47,6 +47,8 @@ __all__ = [
     "make",
     "custom_spec",
     "host_copy",
+    "to_fp8",
+    "Fp8Workload",
 ]
 
 
@@ -277,6 +279,48 @@ def make(spec_or_name, seed: Optional[int] = None, device="cpu", poison: str = "
         block_tables=torch.from_numpy(bt).to(dev),
         seq_lens=torch.from_numpy(lens.astype(np.int32)).to(dev),
         num_blocks=num_blocks, poison_block=poison_block, poison=poison)
+
+
+E4M3_MAX = 448.0  # largest finite e4m3 value
+
+
+@dataclass
+class Fp8Workload:
+    """A workload whose caches are FP8: e4m3 bytes in the bf16 layout and one
+    dequant float per (block, KV head, slot) for K and for V, so that
+    element = e4m3 value x row float.  q, tables and lengths are the base's."""
+
+    base: Workload
+    k8: torch.Tensor       # uint8 [num_blocks, H_kv, BS, D]
+    v8: torch.Tensor
+    k_scale: torch.Tensor  # float32 [num_blocks, H_kv, BS]
+    v_scale: torch.Tensor
+
+    def __getattr__(self, name):  # q, block_tables, seq_lens, scale, spec, lens_list, ...
+        return getattr(self.base, name)
+
+
+def _quantize_rows(x: torch.Tensor):
+    """Per-row (last axis) e4m3 quantization of a bf16 cache, chunked over blocks:
+    the row float is max|x| / 448 (1 for an all-zero row; NaN rows stay NaN)."""
+    q8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    step = max(1, (1 << 24) // max(1, x[0].numel()))
+    for b0 in range(0, x.shape[0], step):
+        xf = x[b0:b0 + step].float()
+        amax = xf.abs().amax(dim=-1)
+        s = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+        s = torch.where(torch.isnan(amax), amax, s)
+        q8[b0:b0 + step] = (xf / s.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+        sc[b0:b0 + step] = s
+    return q8, sc
+
+
+def to_fp8(w: Workload) -> Fp8Workload:
+    """The same problem with FP8 caches (the bf16 caches quantized per row)."""
+    k8, ks = _quantize_rows(w.k_cache)
+    v8, vs = _quantize_rows(w.v_cache)
+    return Fp8Workload(base=w, k8=k8, v8=v8, k_scale=ks, v_scale=vs)
 
 
 def host_copy(w: Workload) -> Workload:
