@@ -252,10 +252,20 @@ def run_ours(args, world, rank, local):
     w = workloads.make(spec, seed=seed, device=dev, poison="zero")
     lens = w.lens_list
     nbytes = algorithmic_bytes(spec, lens)
-    kv_bytes = w.k_cache.numel() * 2 * 2
+    fp8 = args.kv == "fp8"
+    if fp8:
+        # e4m3 caches: one byte per element plus one float per (token, KV head) for K and V
+        f = workloads.to_fp8(w)
+        w.k_cache = w.v_cache = None
+        kv = sum(int(L) for L in lens) * spec.H_kv * (2 * spec.D + 8)
+        nbytes = dict(nbytes, kv=kv, total=kv + nbytes["q_out"] + nbytes["block_table"])
+        base = (f.k8, f.v8, f.k_scale, f.v_scale)
+    else:
+        base = (w.k_cache, w.v_cache, None, None)
+    kv_bytes = sum(t.numel() * t.element_size() for t in base if t is not None)
     reps = max(1, min(8, math.ceil(4 * L2_BYTES / max(1, kv_bytes))))
-    ks = [w.k_cache] + [w.k_cache.clone() for _ in range(reps - 1)]
-    vs = [w.v_cache] + [w.v_cache.clone() for _ in range(reps - 1)]
+    caches = [base] + [tuple(t.clone() if t is not None else None for t in base)
+                       for _ in range(reps - 1)]
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
 
@@ -273,8 +283,12 @@ def run_ours(args, world, rank, local):
         nbytes["append"] = rows * spec.D * 2 * 2 * 2  # K and V rows, read once, written once
         nbytes["total"] += nbytes["append"]
 
-    def run_op(q, bt, sl, kc, vc, kn, vn):
-        if op == "decode":
+    def run_op(q, bt, sl, cache, kn, vn):
+        kc, vc, ksc, vsc = cache
+        if fp8:
+            pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
+                                     stream=stream)
+        elif op == "decode":
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
         elif op == "append_decode":
             pa.paged_attn_append_decode(q, kn, vn, kc, vc, bt, sl, w.scale, out=out,
@@ -284,7 +298,7 @@ def run_ours(args, world, rank, local):
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
 
     def step(i):
-        run_op(w.q, w.block_tables, w.seq_lens, ks[i % reps], vs[i % reps], k_new, v_new)
+        run_op(w.q, w.block_tables, w.seq_lens, caches[i % reps], k_new, v_new)
 
     for i in range(args.warmup):
         step(i)
@@ -357,7 +371,7 @@ def run_ours(args, world, rank, local):
         if host_kn is not None:
             dkn.copy_(host_kn, non_blocking=True)
             dvn.copy_(host_vn, non_blocking=True)
-        run_op(dq, dbt, dsl, ks[i % reps], vs[i % reps], dkn, dvn)
+        run_op(dq, dbt, dsl, caches[i % reps], dkn, dvn)
         host_out.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -377,9 +391,9 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = nbytes["total"] / kernel_s / 1e9
-        traffic = profile_traffic(args.config) if op == "decode" else None
+        traffic = profile_traffic(args.config) if op == "decode" and not fp8 else None
         cpu = None
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and not fp8:  # the baseline leg times the bf16 oracle
             w_host = workloads.host_copy(w)
             threads = len(os.sched_getaffinity(0))
             secs, b, ngroups, total_groups = oracle_baseline(w_host, spec, args.cpu_budget,
@@ -403,14 +417,14 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "e4m3" if fp8 else "bf16",
             "data": "synthetic (seeded; see workloads.py)",
             "config": {
                 "workload": spec.description,
                 "name": args.config,
                 "num_seqs": spec.num_seqs, "H_q": spec.H_q, "H_kv": spec.H_kv,
                 "head_dim": spec.D, "block_size": spec.block_size,
-                "tokens": int(sum(lens)), "seed": seed, "op": op,
+                "tokens": int(sum(lens)), "seed": seed, "op": op, "kv": args.kv,
                 "bytes_per_step": nbytes,
                 "l2": f"inputs larger than L2: {reps} KV-cache replicas rotated "
                       f"({reps * kv_bytes / 1e9:.2f} GB vs 129 MB L2)",
@@ -421,7 +435,8 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback 6800 GB/s",
-                "kernel": {"decode": "paged_decode_kernel (one launch per step, fused combine)",
+                "kernel": "paged_decode_kernel over FP8 caches (one launch per step)" if fp8 else
+                {"decode": "paged_decode_kernel (one launch per step, fused combine)",
                            "append_decode": "paged_decode_kernel with the fused cache append "
                                             "(one launch per step)",
                            "append_then_decode": "paged_kv_append_kernel + paged_decode_kernel "
@@ -498,6 +513,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="llama8b", choices=sorted(workloads.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="cache format: bf16, or e4m3 bytes with a float per cache row")
     ap.add_argument("--op", default="decode",
                     choices=["decode", "append_decode", "append_then_decode"],
                     help="decode alone, or with each sequence's new token appended to the "
@@ -511,6 +528,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.kv == "fp8" and args.op != "decode":
+        ap.error("--kv fp8 runs the decode alone (--op decode)")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)

@@ -157,6 +157,29 @@ PAGED_ATTN_API int paged_attn_decode_static(const void* q, const void* k_cache, 
                              int block_size, float scale, void* stream);
 
 /*
+ * The same operation over FP8 caches: the nvfp4-megamoe README's FP8 KV path
+ * ("Stage D: FP8 Paged KV Gather", "FP8 KV Quantize/Dequant": e4m3 values,
+ * dequantized with a scale per position during the gather).  k_cache / v_cache
+ * hold e4m3 bytes (OCP E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, no infinities) in the bf16 layout above, 1 byte per element, and
+ *   k_scale, v_scale  [num_blocks, H_kv, block_size]  float32  (read)
+ * give each cache row its dequant factor:
+ *   K_t[d] = e4m3(k_cache[b, g, slot, d]) * k_scale[b, g, slot]   (V alike).
+ * head_dim must be 128 or 256 (PAGED_ATTN_ERR_HEAD_DIM otherwise).  The
+ * products run on f16 tensor cores: q is rounded to f16 (exact for bf16 values
+ * of magnitude 2^-14 .. 65504), the probabilities times the V row factors are
+ * rounded to f16; accumulation is fp32.  Workspace, allocation and errors as
+ * paged_attn_decode; rows past a sequence's length may hold anything (NaN
+ * bytes and factors included).
+ */
+PAGED_ATTN_API int paged_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                         const float* k_scale, const float* v_scale, void* out,
+                                         const int32_t* block_tables, const int32_t* seq_lens,
+                                         int num_seqs, int H_q, int H_kv, int head_dim,
+                                         int max_blocks_per_seq, int block_size, float scale,
+                                         void* stream);
+
+/*
  * Cache append ("reshape and cache") of one new token per sequence, the write
  * that precedes the decode: the paged-decode layout above counts the new token
  * in seq_lens ("context length including the new token"), so its K and V must

@@ -23,6 +23,7 @@ __all__ = [
     "paged_attn_decode_static",
     "paged_attn_append_decode",
     "paged_kv_append",
+    "paged_attn_decode_fp8",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "EXPORTED_SYMBOLS",
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "paged_attn_decode_static",
     "paged_kv_append",
     "paged_attn_append_decode",
+    "paged_attn_decode_fp8",
     "paged_attn_status_string",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
@@ -84,6 +86,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_kv_append.restype = I
         lib.paged_attn_append_decode.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.paged_attn_append_decode.restype = I
+        lib.paged_attn_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.paged_attn_decode_fp8.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -234,4 +238,28 @@ def paged_attn_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables, se
     # (q, k_new, v_new, k_cache, v_cache, out, tables, lens, sizes..., scale)
     _check(load().paged_attn_append_decode(a[0], _ptr(k_new), _ptr(v_new), a[1], a[2], a[3],
                                            *a[4:], _stream(stream)))
+    return out
+
+
+def paged_attn_decode_fp8(q, k8, v8, k_scale, v_scale, block_tables, seq_lens, scale: float,
+                          out=None, stream=None):
+    """Decode over FP8 caches (see paged_attn.h): k8 / v8 hold e4m3 bytes (uint8)
+    [num_blocks, H_kv, block_size, head_dim], k_scale / v_scale one float32 per
+    (block, KV head, slot); head_dim 128 or 256."""
+    import torch
+
+    for name, t in (("k8", k8), ("v8", v8), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if k8.dtype != torch.uint8 or v8.dtype != torch.uint8:
+        raise ValueError("k8 / v8 must be uint8 (e4m3 bytes)")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32 or \
+            tuple(k_scale.shape) != tuple(k8.shape[:3]) or k_scale.shape != v_scale.shape:
+        raise ValueError("k_scale / v_scale must be float32 [num_blocks, H_kv, block_size]")
+    if out is None:
+        out = torch.empty_like(q)
+    a = _args(q, k8, v8, out, block_tables, seq_lens, scale)
+    # (q, k8, v8, k_scale, v_scale, out, tables, lens, sizes..., scale)
+    _check(load().paged_attn_decode_fp8(a[0], a[1], a[2], _ptr(k_scale), _ptr(v_scale), a[3],
+                                        *a[4:], _stream(stream)))
     return out

@@ -92,6 +92,9 @@ struct DecodeParams {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* k_cache;      // [num_blocks, H_kv, BS, D]
   __nv_bfloat16* v_cache;
+  // FP8 caches: one dequant float per (block, KV head, slot) for K and for V
+  const float* k_scale;        // [num_blocks, H_kv, BS]
+  const float* v_scale;
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -155,11 +158,16 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
   return c * W / C;
 }
 
-template <int D, int BS, bool G16>
+// FP8: the caches hold e4m3 bytes (head_dim 128 or 256) and one float per cache
+// row; the products run on f16 tensor cores (e4m3 -> f16 is exact, q is turned
+// into f16 once per piece), the K row floats scale the scores and the V row
+// floats are folded into the probabilities.
+template <int D, int BS, bool G16, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  using L = SmemLayout<D, BS>;
+  using L = SmemLayout<D, BS, FP8>;
+  static_assert(!FP8 || D >= 128, "FP8 caches need head_dim 128 or 256");
   constexpr int kTileBytes = L::kTileBytes;
   constexpr int kPageBytes = L::kPageBytes;
   constexpr int kStageBytes = L::kStageBytes;
@@ -170,7 +178,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   constexpr int kTG = BS / 16;        // 16-token groups per page
   constexpr int kQRows = 8 * kNH;                 // query rows one tile holds
   constexpr int kQTileBytes = kQRows * D * 2;     // = lay.q_tile_bytes()
-  constexpr int kQSlotBytes = (kQTileBytes + 4 * D + 16 + 127) / 128 * 128;  // = lay.q_slot_bytes()
+  constexpr int kQ16Stride = L::kQ16Stride;      // FP8: padded f16 query row
+  constexpr int kQSlotBytes =                     // = lay.q_slot_bytes()
+      (kQTileBytes + (FP8 ? kQRows * kQ16Stride : 4 * D + 16) + 127) / 128 * 128;
+  constexpr int kScaleBytes = L::kScaleBytes;     // FP8: a stage's K and V row floats
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -185,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   int* sm_flag = reinterpret_cast<int*>(smem + lay.flag());
   float* sm_o = reinterpret_cast<float*>(smem + lay.merge_o());
   uint8_t* sm_q = smem + lay.qtile();
+  float* sm_scales = reinterpret_cast<float*>(smem + lay.scales());  // FP8: [stages][2][BS]
   int* sm_prefix = reinterpret_cast<int*>(smem + lay.prefix());
   int* sm_len = reinterpret_cast<int*>(smem + lay.lens());
 
@@ -324,10 +336,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
             atomicOr(p.status, kStatusTimeout);
             bad = true;
           } else {
-            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
             uint8_t* st = smem + stage * kStageBytes;
             tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
             tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
+            if constexpr (FP8) {
+              // the page's K and V row floats (a block outside a checked pool reads
+              // block 0's: its rows are zero-filled by the tensor copy anyway)
+              const long long b =
+                  p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks) ? 0 : pb;
+              const size_t row = ((size_t)b * H_kv + g) * BS;
+              float* sc = sm_scales + (size_t)stage * 2 * BS;
+              bulk_load(sc, p.k_scale + row, BS * 4, &full_bar[stage]);
+              bulk_load(sc + BS, p.v_scale + row, BS * 4, &full_bar[stage]);
+            }
           }
         }
         abort = __any_sync(0xffffffffu, bad);
@@ -379,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
                        : static_cast<const void*>(p.q),
                   live ? 16 : 0);
     }
-    if (p.k_new != nullptr) {
+    if (!FP8 && p.k_new != nullptr) {
       const size_t row = ((size_t)s * H_kv + g) * D;
       for (int i = ctid; i < D / 4; i += kConsumerThreads) {  // K then V, 16 bytes each
         const bool is_v = i >= D / 8;
@@ -393,6 +415,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       }
     }
     cp_async_commit();
+  };
+  // FP8: the slot's bf16 query tile (swizzled, as prefetched) -> f16 rows in
+  // natural order, padded (kQ16Stride) so the page loop's 8-byte reads of four
+  // rows x four lanes fall in distinct banks.
+  auto convert_q = [&](int buf) {
+    const uint8_t* tile = sm_q + buf * kQSlotBytes;
+    uint8_t* q16 = sm_q + buf * kQSlotBytes + kQTileBytes;
+    for (int i = ctid; i < kQRows * (D / 2); i += kConsumerThreads) {
+      const int h = i / (D / 2);
+      const int d = 2 * (i - h * (D / 2));
+      const int c = d / 8;
+      const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
+      const uint32_t v =
+          *reinterpret_cast<const uint32_t*>(tile + h * (D * 2) + pc * 16 + (d % 8) * 2);
+      *reinterpret_cast<uint32_t*>(q16 + h * kQ16Stride + d * 2) =
+          pack_f16x2(bf16lo_to_f32(v), bf16hi_to_f32(v));
+    }
   };
   auto reset = [&]() {
 #pragma unroll
@@ -553,6 +592,173 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           mma_bf16_16816(o_acc[dt][nh], a0, a1, a2, a3, pb0[tg][nh], pb1[tg][nh]);
       }
     }
+  };
+
+  // FP8 page.  S^T = K Q^T on f16 tensor cores: one ldmatrix.x4 on the e4m3 K
+  // tile hands each lane, for two 16-column steps (two 16-byte chunks), the
+  // bytes 4q..4q+3 of its token rows r and r + 8; within each chunk the
+  // contraction runs in a fixed permuted order (bytes 4q, 4q+1 -> MMA k 2q,
+  // 2q+1; 4q+2, 4q+3 -> 2q+8, 2q+9), and the query operand (f16, natural
+  // order) is read in the same order: four consecutive f16 of its row.  The
+  // K row floats scale the scores; the V row floats are folded into the
+  // probabilities.  O^T += V^T P^T: ldmatrix.x4.trans on the e4m3 V tile with
+  // byte pairs as 16-bit units hands each lane, for the d pair (2r, 2r+1) and
+  // tokens (2q, 2q+1), four bytes that one byte permute splits per d; so the
+  // accumulator rows r and r + 8 of a 16-column tile are the columns 2r and
+  // 2r + 1.
+  auto process_page_fp8 = [&](const uint8_t* kt, const uint8_t* vt, const uint8_t* q16,
+                              const float* ks, const float* vs, int valid) {
+    const uint32_t kbase = smem_addr(kt);
+    const uint32_t vbase = smem_addr(vt);
+    const int li = lane >> 3;
+    float s_acc[kTG][kNH][4], s_odd[kTG][kNH][4];
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg)
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s_acc[tg][nh][e] = s_odd[tg][nh][e] = 0.f;
+#pragma unroll
+    for (int kk2 = 0; kk2 < kDT / 2; ++kk2) {
+      uint32_t qf[2][kNH][2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh) {
+          const uint2 b = *reinterpret_cast<const uint2*>(
+              q16 + (8 * nh + row) * kQ16Stride + (16 * (2 * kk2 + x) + 4 * quad) * 2);
+          qf[x][nh][0] = b.x;
+          qf[x][nh][1] = b.y;
+        }
+#pragma unroll
+      for (int tg = 0; tg < kTG; ++tg) {
+        const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
+        const int chunk = 2 * kk2 + (li >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(kbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
+                                       (((chunk & 7) ^ (tok & 7)) << 4)),
+                    r0, r1, r2, r3);
+        const uint32_t a0 = e4m3x2_to_f16x2(r0 & 0xffffu), a2 = e4m3x2_to_f16x2(r0 >> 16);
+        const uint32_t a1 = e4m3x2_to_f16x2(r1 & 0xffffu), a3 = e4m3x2_to_f16x2(r1 >> 16);
+        const uint32_t c0 = e4m3x2_to_f16x2(r2 & 0xffffu), c2 = e4m3x2_to_f16x2(r2 >> 16);
+        const uint32_t c1 = e4m3x2_to_f16x2(r3 & 0xffffu), c3 = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh) {
+          mma_f16_16816(s_acc[tg][nh], a0, a1, a2, a3, qf[0][nh][0], qf[0][nh][1]);
+          mma_f16_16816(s_odd[tg][nh], c0, c1, c2, c3, qf[1][nh][0], qf[1][nh][1]);
+        }
+      }
+    }
+    // ---- online softmax per head (log2 domain); masked tokens are selected out
+    float mx[kNH][2];
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) mx[nh][0] = mx[nh][1] = -INFINITY;
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg) {
+      const int t_lo = 16 * tg + row, t_hi = t_lo + 8;
+      const float k_lo = p.scale_log2 * ks[t_lo], k_hi = p.scale_log2 * ks[t_hi];
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = (e >> 1) ? t_hi : t_lo;
+          const float sum = s_acc[tg][nh][e] + s_odd[tg][nh][e];
+          const float x = tok < valid ? sum * ((e >> 1) ? k_hi : k_lo) : -INFINITY;
+          s_acc[tg][nh][e] = x;
+          mx[nh][e & 1] = fmaxf(mx[nh][e & 1], x);
+        }
+    }
+    float alpha[kNH][2];
+    bool changed = false;
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = mx[nh][e];
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const float m_new = fmaxf(m_run[nh][e], v);
+        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_new);
+        changed |= m_new != m_run[nh][e];
+        m_run[nh][e] = m_new;
+      }
+    uint32_t pb0[kTG][kNH], pb1[kTG][kNH];
+    float psum[kNH][2];
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh) psum[nh][0] = psum[nh][1] = 0.f;
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg) {
+      const int t_lo = 16 * tg + row, t_hi = t_lo + 8;
+      const float v_lo = t_lo < valid ? vs[t_lo] : 0.f;  // masked rows may hold NaN floats
+      const float v_hi = t_hi < valid ? vs[t_hi] : 0.f;
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh) {
+        const float e0 = fast_exp2(s_acc[tg][nh][0] - m_run[nh][0]);
+        const float e1 = fast_exp2(s_acc[tg][nh][1] - m_run[nh][1]);
+        const float e2 = fast_exp2(s_acc[tg][nh][2] - m_run[nh][0]);
+        const float e3 = fast_exp2(s_acc[tg][nh][3] - m_run[nh][1]);
+        psum[nh][0] += e0 + e2;
+        psum[nh][1] += e1 + e3;
+        pb0[tg][nh] = movmatrix_trans(pack_f16x2(e0 * v_lo, e1 * v_lo));
+        pb1[tg][nh] = movmatrix_trans(pack_f16x2(e2 * v_hi, e3 * v_hi));
+      }
+    }
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) l_run[nh][e] = l_run[nh][e] * alpha[nh][e] + psum[nh][e];
+    if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt)
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o_acc[dt][nh][e] *= alpha[nh][e & 1];
+    }
+    const bool tail = valid < BS;
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg) {
+      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+      if (tail) {  // rows past the sequence may hold anything: zero them in the fragment
+        const int t0 = 16 * tg + 2 * quad;
+        mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+        mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+      }
+      const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
+#pragma unroll
+      for (int dt2 = 0; dt2 < kDT / 2; ++dt2) {
+        const int chunk = 2 * dt2 + (li >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4_trans(vbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
+                                             (((chunk & 7) ^ (tok & 7)) << 4)),
+                          r0, r1, r2, r3);
+        // r0 / r1: tokens 0-7 / 8-15 of chunk 2 dt2; r2 / r3: of chunk 2 dt2 + 1
+        const uint32_t x0 = __byte_perm(r0, 0, 0x3120), x1 = __byte_perm(r1, 0, 0x3120);
+        const uint32_t x2 = __byte_perm(r2, 0, 0x3120), x3 = __byte_perm(r3, 0, 0x3120);
+        const uint32_t a0 = e4m3x2_to_f16x2(x0 & 0xffffu) & mlo;  // column 2r, tokens 2q, 2q+1
+        const uint32_t a1 = e4m3x2_to_f16x2(x0 >> 16) & mlo;      // column 2r+1
+        const uint32_t a2 = e4m3x2_to_f16x2(x1 & 0xffffu) & mhi;  // tokens 2q+8, 2q+9
+        const uint32_t a3 = e4m3x2_to_f16x2(x1 >> 16) & mhi;
+        const uint32_t c0 = e4m3x2_to_f16x2(x2 & 0xffffu) & mlo;
+        const uint32_t c1 = e4m3x2_to_f16x2(x2 >> 16) & mlo;
+        const uint32_t c2 = e4m3x2_to_f16x2(x3 & 0xffffu) & mhi;
+        const uint32_t c3 = e4m3x2_to_f16x2(x3 >> 16) & mhi;
+#pragma unroll
+        for (int nh = 0; nh < kNH; ++nh) {
+          mma_f16_16816(o_acc[2 * dt2][nh], a0, a1, a2, a3, pb0[tg][nh], pb1[tg][nh]);
+          mma_f16_16816(o_acc[2 * dt2 + 1][nh], c0, c1, c2, c3, pb0[tg][nh], pb1[tg][nh]);
+        }
+      }
+    }
+  };
+
+  // Head-dimension column of accumulator element e of o_acc[dt] held by this lane.
+  auto acc_col = [&](int dt, int e) -> int {
+    if constexpr (FP8)
+      return 16 * dt + 2 * row + (e >> 1);
+    else
+      return 16 * dt + row + ((e >> 1) << 3);
   };
 
   // Partial state slot this CTA writes for a split piece beginning at sb: slot 0
@@ -748,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = 8 * nh + 2 * quad + (e & 1);
-          const int d = 16 * dt + row + ((e >> 1) << 3);
+          const int d = acc_col(dt, e);
           if (h < G) sm_o[(warp * G + h) * kRowStride + d] = o_acc[dt][nh][e] * f[nh][e & 1];
         }
     __syncwarp();
@@ -841,6 +1047,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);
   if (ahead.s < N && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
+  if constexpr (FP8) {
+    convert_q(0);
+    __syncwarp();
+    named_barrier(kConsumerBarrier, kConsumerThreads);
+  }
   reset();
   int stage = 0;
   uint32_t phase = 0;
@@ -854,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // into the page in shared memory once the page has landed (the tensor
       // copy brought whatever the cache held) and stored to the cache for later
       // calls.  This page is read by this CTA alone.
-      const bool patch = p.k_new != nullptr && wk.p == wk.n - 1;
+      const bool patch = !FP8 && p.k_new != nullptr && wk.p == wk.n - 1;
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.
@@ -877,7 +1088,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           }
           __syncwarp();
         }
-        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
+        if constexpr (FP8) {
+          const float* sc = sm_scales + (size_t)stage * 2 * BS;
+          process_page_fp8(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes + kQTileBytes, sc,
+                           sc + BS, valid);
+        } else {
+          process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
+        }
         if (patch) {
           // the patch's generic writes precede the next tensor copy into this slot
           fence_proxy_async_shared();
@@ -923,6 +1140,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       qbuf ^= 1;
       ahead = next_piece(ahead);
       if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
+      if constexpr (FP8) {
+        convert_q(qbuf);
+        __syncwarp();
+        named_barrier(kConsumerBarrier, kConsumerThreads);
+      }
       reset();
       continue;
     }

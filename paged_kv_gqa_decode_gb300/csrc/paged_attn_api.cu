@@ -98,6 +98,7 @@ int device_info(DeviceInfo* out) {
 struct Plan {
   int D, BS, G;
   bool g16;
+  bool fp8;     // FP8 caches
   int chunk;    // sequences per launch
   int stages;   // pipeline depth
   size_t smem;  // dynamic shared memory per CTA
@@ -105,12 +106,12 @@ struct Plan {
   size_t off_counters, off_partials, ws_bytes;
 };
 
-template <int D, int BS>
+template <int D, int BS, bool FP8>
 bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int* stages, size_t* smem) {
-  using L = SmemLayout<D, BS>;
+  using L = SmemLayout<D, BS, FP8>;
   const L none{0, G, chunk};
   const long long fixed = none.total() + 2048;  // + alignment slack and static shared memory
-  const long long per_stage = L::kStageBytes + 16;
+  const long long per_stage = L::kStageBytes + L::kScaleBytes + 16;
   long long st = (max_smem - fixed) / per_stage;
   if (st > kMaxStages) st = kMaxStages;
   if (st > ring_cap / L::kStageBytes) st = ring_cap / L::kStageBytes;
@@ -122,20 +123,32 @@ bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int* stages, 
   return *smem + 256 <= (size_t)max_smem;  // + the kernel's static shared memory
 }
 
-bool plan_smem_any(int D, int BS, int G, int chunk, int max_smem, long long ring_cap,
-                   int* stages, size_t* smem) {
-  if (D == 64)
-    return BS == 16 ? plan_smem<64, 16>(G, chunk, max_smem, ring_cap, stages, smem)
-                    : plan_smem<64, 32>(G, chunk, max_smem, ring_cap, stages, smem);
+template <bool FP8>
+bool plan_smem_d(int D, int BS, int G, int chunk, int max_smem, long long ring_cap, int* stages,
+                 size_t* smem) {
+  if (D == 64) {
+    if constexpr (FP8) return false;  // FP8 caches need head_dim 128 or 256
+    else
+      return BS == 16 ? plan_smem<64, 16, false>(G, chunk, max_smem, ring_cap, stages, smem)
+                      : plan_smem<64, 32, false>(G, chunk, max_smem, ring_cap, stages, smem);
+  }
   if (D == 128)
-    return BS == 16 ? plan_smem<128, 16>(G, chunk, max_smem, ring_cap, stages, smem)
-                    : plan_smem<128, 32>(G, chunk, max_smem, ring_cap, stages, smem);
-  return BS == 16 ? plan_smem<256, 16>(G, chunk, max_smem, ring_cap, stages, smem)
-                  : plan_smem<256, 32>(G, chunk, max_smem, ring_cap, stages, smem);
+    return BS == 16 ? plan_smem<128, 16, FP8>(G, chunk, max_smem, ring_cap, stages, smem)
+                    : plan_smem<128, 32, FP8>(G, chunk, max_smem, ring_cap, stages, smem);
+  return BS == 16 ? plan_smem<256, 16, FP8>(G, chunk, max_smem, ring_cap, stages, smem)
+                  : plan_smem<256, 32, FP8>(G, chunk, max_smem, ring_cap, stages, smem);
 }
 
-int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& di, Plan* pl) {
+bool plan_smem_any(int D, int BS, bool fp8, int G, int chunk, int max_smem, long long ring_cap,
+                   int* stages, size_t* smem) {
+  return fp8 ? plan_smem_d<true>(D, BS, G, chunk, max_smem, ring_cap, stages, smem)
+             : plan_smem_d<false>(D, BS, G, chunk, max_smem, ring_cap, stages, smem);
+}
+
+int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& di, Plan* pl,
+              bool fp8 = false) {
   pl->D = D;
+  pl->fp8 = fp8;
   pl->BS = BS;
   pl->G = H_q / H_kv;
   pl->g16 = pl->G > 8;
@@ -159,7 +172,7 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
       const long long pieces = (long long)chunk * H_kv;
       const long long ring_cap =
           (pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces : kRingBytesPerSm) / occ;
-      if (plan_smem_any(D, BS, pl->G, chunk, budget, ring_cap, &pl->stages, &pl->smem) &&
+      if (plan_smem_any(D, BS, fp8, pl->G, chunk, budget, ring_cap, &pl->stages, &pl->smem) &&
           (pl->stages >= 4 || chunk <= 64)) {
         ok = true;
         pl->grid = di.sms * occ;
@@ -211,11 +224,14 @@ int get_encoder(EncodeTiledFn* fn) {
 // [half][row][128 bytes] with the 128-byte swizzle the kernel's ldmatrix
 // addressing expects.
 int encode_cache_map(const void* base, int D, int BS, int H_kv, long long num_blocks,
-                     CUtensorMap* map) {
+                     CUtensorMap* map, bool fp8 = false) {
   EncodeTiledFn enc = nullptr;
   int rc = get_encoder(&enc);
   if (rc != PAGED_ATTN_OK) return rc;
-  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  const int elem = fp8 ? 1 : 2;          // bytes per element
+  const cuuint64_t inner = 128 / elem;   // elements in a 128-byte half of a row
+  const cuuint64_t halves = (cuuint64_t)D * elem / 128;
+  const cuuint64_t row_bytes = (cuuint64_t)D * elem;
   const cuuint64_t block_bytes = row_bytes * (cuuint64_t)H_kv * BS;
   cuuint64_t nb = (cuuint64_t)num_blocks;
   if (num_blocks <= 0) {
@@ -224,19 +240,24 @@ int encode_cache_map(const void* base, int D, int BS, int H_kv, long long num_bl
     nb = ((cuuint64_t)1 << 40) / block_bytes;
     if (nb > 0x7fffffffULL) nb = 0x7fffffffULL;
   }
-  const cuuint64_t dims[4] = {64, (cuuint64_t)H_kv * BS, (cuuint64_t)D / 64, nb};
+  const cuuint64_t dims[4] = {inner, (cuuint64_t)H_kv * BS, halves, nb};
   const cuuint64_t strides[3] = {row_bytes, 128, block_bytes};
-  const cuuint32_t box[4] = {64, (cuuint32_t)BS, (cuuint32_t)D / 64, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)BS, (cuuint32_t)halves, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   4, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail((int)r);
   return PAGED_ATTN_OK;
 }
 
-cudaError_t launch_dim(int D, int BS, bool g16, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+cudaError_t launch_dim(int D, int BS, bool g16, bool fp8, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const DecodeParams& p, int grid, size_t smem,
+                       cudaStream_t st) {
+  if (fp8)
+    return D == 128 ? launch_decode_fp8_d128(BS, g16, tk, tv, p, grid, smem, st)
+                    : launch_decode_fp8_d256(BS, g16, tk, tv, p, grid, smem, st);
   if (D == 64) return launch_decode_d64(BS, g16, tk, tv, p, grid, smem, st);
   if (D == 128) return launch_decode_d128(BS, g16, tk, tv, p, grid, smem, st);
   return launch_decode_d256(BS, g16, tk, tv, p, grid, smem, st);
@@ -256,11 +277,12 @@ int check_pointers(const void* q, const void* k, const void* v, const void* out,
 int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache, void* out,
         const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
         int max_blocks_per_seq, float scale, void* ws, int32_t* status, long long num_blocks,
-        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
+        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
+        const float* k_scale = nullptr, const float* v_scale = nullptr) {
   CUtensorMap tk, tv;
-  int rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk);
+  int rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, pl.fp8);
   if (rc != PAGED_ATTN_OK) return rc;
-  rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv);
+  rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv, pl.fp8);
   if (rc != PAGED_ATTN_OK) return rc;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   for (int s0 = 0; s0 < num_seqs; s0 += pl.chunk) {
@@ -287,7 +309,9 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
                     : nullptr;
     p.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
     p.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
-    cudaError_t e = launch_dim(pl.D, pl.BS, pl.g16, tk, tv, p, pl.grid, pl.smem, stream);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    cudaError_t e = launch_dim(pl.D, pl.BS, pl.g16, pl.fp8, tk, tv, p, pl.grid, pl.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return PAGED_ATTN_OK;
@@ -380,6 +404,30 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
   if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
   return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
              max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
+int paged_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale, void* out,
+                          const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                          int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                          int block_size, float scale, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (head_dim == 64) return PAGED_ATTN_ERR_HEAD_DIM;  // FP8 pages need 128-byte rows
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  if (!aligned16(k_scale) || !aligned16(v_scale)) return PAGED_ATTN_ERR_POINTER;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl, true)) !=
+      PAGED_ATTN_OK)
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st, nullptr, nullptr, k_scale, v_scale);
 }
 
 int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,

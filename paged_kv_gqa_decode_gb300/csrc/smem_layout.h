@@ -20,29 +20,39 @@ constexpr int kConsumerWarps = 4;
 
 PAGEDATTN_HD constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int D, int BS>
+// FP8: the caches hold e4m3 bytes (head_dim 128 or 256) plus one float per
+// cache row for K and for V.
+template <int D, int BS, bool FP8 = false>
 struct SmemLayout {
-  static constexpr int kHalves = D / 64;              // 128-byte column halves of a row
+  static constexpr int kElem = FP8 ? 1 : 2;           // bytes per cache element
+  static constexpr int kHalves = D * kElem / 128;     // 128-byte column halves of a row
   static constexpr int kTileBytes = BS * 128;         // one half of one page
   static constexpr int kPageBytes = kHalves * kTileBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;  // K page + V page
+  static constexpr int kScaleBytes = FP8 ? 2 * BS * 4 : 0;  // a stage's K and V row floats
   static constexpr int kRowStride = D + 4;            // padded fp32 row in the merge buffer
+  static constexpr int kQ16Stride = 2 * D + 32;       // FP8: padded f16 query row
 
   int stages, G, num_seqs;
   // [0, bars): the ring of `stages` K/V pages (at the end of a range it holds the
   // partial states being combined); then the mbarriers full[stages],
-  // empty[stages] and one for the combine's copies
+  // empty[stages] and one for the combine's copies; FP8: the ring of row floats
   PAGEDATTN_HD int bars() const { return stages * kStageBytes; }
-  PAGEDATTN_HD int merge_m() const { return align_up(bars() + (2 * stages + 1) * 8, 128); }
+  PAGEDATTN_HD int scales() const { return align_up(bars() + (2 * stages + 1) * 8, 128); }
+  PAGEDATTN_HD int merge_m() const { return align_up(scales() + stages * kScaleBytes, 128); }
   PAGEDATTN_HD int merge_l() const { return merge_m() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int final_ml() const { return merge_l() + kConsumerWarps * 16 * 4; }
   PAGEDATTN_HD int flag() const { return final_ml() + 32 * 4; }  // a few ints
   PAGEDATTN_HD int merge_o() const { return flag() + 128; }
   // one query tile: the group's rows padded to 8 (G <= 8) or 16 heads
-  PAGEDATTN_HD int q_tile_bytes() const { return (G > 8 ? 16 : 8) * D * 2; }
-  // one query slot: the tile, then (fused cache append) the piece's new K row,
-  // new V row and the block id of its last page
-  PAGEDATTN_HD int q_slot_bytes() const { return align_up(q_tile_bytes() + 4 * D + 16, 128); }
+  PAGEDATTN_HD int q_rows() const { return G > 8 ? 16 : 8; }
+  PAGEDATTN_HD int q_tile_bytes() const { return q_rows() * D * 2; }
+  // one query slot: the bf16 tile, then (fused cache append) the piece's new K
+  // row, new V row and the block id of its last page, or (FP8) the tile as f16
+  PAGEDATTN_HD int q_extra_bytes() const { return FP8 ? q_rows() * kQ16Stride : 4 * D + 16; }
+  PAGEDATTN_HD int q_slot_bytes() const {
+    return align_up(q_tile_bytes() + q_extra_bytes(), 128);
+  }
   PAGEDATTN_HD int qtile() const {  // two query slots
     return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
   }

@@ -25,9 +25,9 @@ using namespace pagedattn;
 static int bad = 0;
 #define CHECK(c, ...) do { if (!(c)) { if (bad < 20) std::printf(__VA_ARGS__); ++bad; } } while (0)
 
-template <int D, int BS>
+template <int D, int BS, bool FP8 = false>
 void run() {
-  using L = SmemLayout<D, BS>;
+  using L = SmemLayout<D, BS, FP8>;
   const int ns[] = {1, 2, 3, 5, 7, 31, 32, 33, 255, 256, 257, 1000, 4095, 4096};
   for (int st = 4; st <= 16; ++st)
     for (int G = 1; G <= 16; ++G)
@@ -36,8 +36,10 @@ void run() {
         CHECK(l.bars() % 1024 == 0, "bars D%d BS%d st%d\n", D, BS, st);
         CHECK(L::kStageBytes % 1024 == 0, "stage size D%d BS%d\n", D, BS);
         CHECK(l.merge_m() >= l.bars() + (2 * st + 1) * 8, "barrier overlap\n");
-        const int starts[] = {l.merge_m(), l.merge_l(), l.final_ml(), l.flag(), l.merge_o(),
-                              l.qtile(), l.prefix(), l.lens()};
+        CHECK(l.scales() >= l.bars() + (2 * st + 1) * 8, "scales overlap\n");
+        CHECK(l.merge_m() >= l.scales() + st * L::kScaleBytes, "scale ring size\n");
+        const int starts[] = {l.scales(), l.merge_m(), l.merge_l(), l.final_ml(), l.flag(),
+                              l.merge_o(), l.qtile(), l.prefix(), l.lens()};
         for (int x : starts)
           CHECK(x % 128 == 0, "region at %d D%d BS%d st%d G%d n%d\n", x, D, BS, st, G, n);
         CHECK(l.merge_l() - l.merge_m() >= kConsumerWarps * 16 * 4, "merge_m size\n");
@@ -46,6 +48,11 @@ void run() {
         CHECK(l.merge_o() - l.flag() >= 4 * 4, "flag size\n");
         CHECK(l.qtile() - l.merge_o() >= kConsumerWarps * G * L::kRowStride * 4, "merge_o size\n");
         CHECK(l.prefix() - l.qtile() >= 2 * ((G > 8 ? 16 : 8) * D * 2 + 4 * D + 4), "qtile size\n");
+        if (FP8) {
+          CHECK(l.q_extra_bytes() >= (G > 8 ? 16 : 8) * (2 * D + 32), "q16 size\n");
+          CHECK(L::kQ16Stride % 32 == 0, "q16 stride\n");
+          CHECK(L::kPageBytes == BS * D, "fp8 page\n");
+        }
         CHECK(l.q_slot_bytes() % 128 == 0, "q slot\n");
         CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
@@ -56,6 +63,7 @@ void run() {
 
 int main() {
   run<64, 16>(); run<64, 32>(); run<128, 16>(); run<128, 32>(); run<256, 16>(); run<256, 32>();
+  run<128, 16, true>(); run<128, 32, true>(); run<256, 16, true>(); run<256, 32, true>();
   std::printf(bad ? "FAIL %d\n" : "OK\n", bad);
   return bad ? 1 : 0;
 }
