@@ -40,6 +40,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -594,30 +595,39 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
   };
 
-  // FP8 page.  S^T = K Q^T on f16 tensor cores: one ldmatrix.x4 on the e4m3 K
-  // tile hands each lane, for two 16-column steps (two 16-byte chunks), the
-  // bytes 4q..4q+3 of its token rows r and r + 8; within each chunk the
-  // contraction runs in a fixed permuted order (bytes 4q, 4q+1 -> MMA k 2q,
-  // 2q+1; 4q+2, 4q+3 -> 2q+8, 2q+9), and the query operand (f16, natural
-  // order) is read in the same order: four consecutive f16 of its row.  The
-  // K row floats scale the scores; the V row floats are folded into the
+  // FP8 tiles.  The unit of work is a group of NT 16-token tiles (one BS = 16
+  // page, the two halves of a BS = 32 page, or two pages of one piece taken
+  // together), each tile with its own K / V shared-memory rows, row floats and
+  // count of valid tokens.  S^T = K Q^T on f16 tensor cores: one ldmatrix.x4
+  // on the e4m3 K tile hands each lane, for two 16-column steps (two 16-byte
+  // chunks), the bytes 4q..4q+3 of its token rows r and r + 8; within each
+  // chunk the contraction runs in a fixed permuted order (bytes 4q, 4q+1 ->
+  // MMA k 2q, 2q+1; 4q+2, 4q+3 -> 2q+8, 2q+9), and the query operand (f16,
+  // natural order) is read in the same order: four consecutive f16 of its row.
+  // The K row floats scale the scores; the V row floats are folded into the
   // probabilities.  O^T += V^T P^T: ldmatrix.x4.trans on the e4m3 V tile with
   // byte pairs as 16-bit units hands each lane, for the d pair (2r, 2r+1) and
   // tokens (2q, 2q+1), four bytes that one byte permute splits per d; so the
   // accumulator rows r and r + 8 of a 16-column tile are the columns 2r and
-  // 2r + 1.
-  auto process_page_fp8 = [&](const uint8_t* kt, const uint8_t* vt, const uint8_t* q16,
-                              const float* ks, const float* vs, int valid) {
-    const uint32_t kbase = smem_addr(kt);
-    const uint32_t vbase = smem_addr(vt);
+  // 2r + 1.  V rows past the sequence were zeroed in shared memory by the
+  // caller, so the V operand needs no mask.
+  struct Tile8 {
+    uint32_t k, v;        // shared-memory address of the tile's first K / V row
+    const float* ks;      // its 16 K row floats
+    const float* vs;      // its 16 V row floats
+    int valid;            // tokens of the tile inside the sequence (0..16)
+  };
+  auto process_fp8 = [&](auto nt, const Tile8* tl, const uint8_t* q16) {
+    constexpr int NT = decltype(nt)::value;
     const int li = lane >> 3;
-    float s_acc[kTG][kNH][4], s_odd[kTG][kNH][4];
+    float s_acc[NT][kNH][4], s_odd[NT][kNH][4];
 #pragma unroll
-    for (int tg = 0; tg < kTG; ++tg)
+    for (int tg = 0; tg < NT; ++tg)
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s_acc[tg][nh][e] = s_odd[tg][nh][e] = 0.f;
+    const int trow = (lane & 7) + ((li & 1) << 3);  // tile row this lane addresses
 #pragma unroll
     for (int kk2 = 0; kk2 < kDT / 2; ++kk2) {
       uint32_t qf[2][kNH][2];
@@ -630,18 +640,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           qf[x][nh][0] = b.x;
           qf[x][nh][1] = b.y;
         }
+      const int chunk = 2 * kk2 + (li >> 1);
+      const uint32_t coff =
+          (uint32_t)((chunk >> 3) * kTileBytes + trow * 128 + (((chunk & 7) ^ (trow & 7)) << 4));
 #pragma unroll
-      for (int tg = 0; tg < kTG; ++tg) {
-        const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
-        const int chunk = 2 * kk2 + (li >> 1);
+      for (int tg = 0; tg < NT; ++tg) {
         uint32_t r0, r1, r2, r3;
-        ldmatrix_x4(kbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
-                                       (((chunk & 7) ^ (tok & 7)) << 4)),
-                    r0, r1, r2, r3);
-        const uint32_t a0 = e4m3x2_to_f16x2(r0 & 0xffffu), a2 = e4m3x2_to_f16x2(r0 >> 16);
-        const uint32_t a1 = e4m3x2_to_f16x2(r1 & 0xffffu), a3 = e4m3x2_to_f16x2(r1 >> 16);
-        const uint32_t c0 = e4m3x2_to_f16x2(r2 & 0xffffu), c2 = e4m3x2_to_f16x2(r2 >> 16);
-        const uint32_t c1 = e4m3x2_to_f16x2(r3 & 0xffffu), c3 = e4m3x2_to_f16x2(r3 >> 16);
+        ldmatrix_x4(tl[tg].k + coff, r0, r1, r2, r3);
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        e4m3x4_to_f16x2x2(r0, a0, a2);
+        e4m3x4_to_f16x2x2(r1, a1, a3);
+        e4m3x4_to_f16x2x2(r2, c0, c2);
+        e4m3x4_to_f16x2x2(r3, c1, c3);
 #pragma unroll
         for (int nh = 0; nh < kNH; ++nh) {
           mma_f16_16816(s_acc[tg][nh], a0, a1, a2, a3, qf[0][nh][0], qf[0][nh][1]);
@@ -654,14 +664,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh) mx[nh][0] = mx[nh][1] = -INFINITY;
 #pragma unroll
-    for (int tg = 0; tg < kTG; ++tg) {
-      const int t_lo = 16 * tg + row, t_hi = t_lo + 8;
-      const float k_lo = p.scale_log2 * ks[t_lo], k_hi = p.scale_log2 * ks[t_hi];
+    for (int tg = 0; tg < NT; ++tg) {
+      const int valid = tl[tg].valid;
+      const float k_lo = p.scale_log2 * tl[tg].ks[row], k_hi = p.scale_log2 * tl[tg].ks[row + 8];
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int tok = (e >> 1) ? t_hi : t_lo;
+          const int tok = row + ((e >> 1) << 3);
           const float sum = s_acc[tg][nh][e] + s_odd[tg][nh][e];
           const float x = tok < valid ? sum * ((e >> 1) ? k_hi : k_lo) : -INFINITY;
           s_acc[tg][nh][e] = x;
@@ -683,15 +693,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         changed |= m_new != m_run[nh][e];
         m_run[nh][e] = m_new;
       }
-    uint32_t pb0[kTG][kNH], pb1[kTG][kNH];
+    uint32_t pb0[NT][kNH], pb1[NT][kNH];
     float psum[kNH][2];
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh) psum[nh][0] = psum[nh][1] = 0.f;
 #pragma unroll
-    for (int tg = 0; tg < kTG; ++tg) {
-      const int t_lo = 16 * tg + row, t_hi = t_lo + 8;
-      const float v_lo = t_lo < valid ? vs[t_lo] : 0.f;  // masked rows may hold NaN floats
-      const float v_hi = t_hi < valid ? vs[t_hi] : 0.f;
+    for (int tg = 0; tg < NT; ++tg) {
+      const int valid = tl[tg].valid;
+      const float v_lo = row < valid ? tl[tg].vs[row] : 0.f;  // masked rows may hold NaN floats
+      const float v_hi = row + 8 < valid ? tl[tg].vs[row + 8] : 0.f;
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh) {
         const float e0 = fast_exp2(s_acc[tg][nh][0] - m_run[nh][0]);
@@ -716,34 +726,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
           for (int e = 0; e < 4; ++e) o_acc[dt][nh][e] *= alpha[nh][e & 1];
     }
-    const bool tail = valid < BS;
 #pragma unroll
-    for (int tg = 0; tg < kTG; ++tg) {
-      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-      if (tail) {  // rows past the sequence may hold anything: zero them in the fragment
-        const int t0 = 16 * tg + 2 * quad;
-        mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-        mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-      }
-      const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
+    for (int dt2 = 0; dt2 < kDT / 2; ++dt2) {
+      const int chunk = 2 * dt2 + (li >> 1);
+      const uint32_t coff =
+          (uint32_t)((chunk >> 3) * kTileBytes + trow * 128 + (((chunk & 7) ^ (trow & 7)) << 4));
 #pragma unroll
-      for (int dt2 = 0; dt2 < kDT / 2; ++dt2) {
-        const int chunk = 2 * dt2 + (li >> 1);
+      for (int tg = 0; tg < NT; ++tg) {
         uint32_t r0, r1, r2, r3;
-        ldmatrix_x4_trans(vbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
-                                             (((chunk & 7) ^ (tok & 7)) << 4)),
-                          r0, r1, r2, r3);
+        ldmatrix_x4_trans(tl[tg].v + coff, r0, r1, r2, r3);
         // r0 / r1: tokens 0-7 / 8-15 of chunk 2 dt2; r2 / r3: of chunk 2 dt2 + 1
         const uint32_t x0 = __byte_perm(r0, 0, 0x3120), x1 = __byte_perm(r1, 0, 0x3120);
         const uint32_t x2 = __byte_perm(r2, 0, 0x3120), x3 = __byte_perm(r3, 0, 0x3120);
-        const uint32_t a0 = e4m3x2_to_f16x2(x0 & 0xffffu) & mlo;  // column 2r, tokens 2q, 2q+1
-        const uint32_t a1 = e4m3x2_to_f16x2(x0 >> 16) & mlo;      // column 2r+1
-        const uint32_t a2 = e4m3x2_to_f16x2(x1 & 0xffffu) & mhi;  // tokens 2q+8, 2q+9
-        const uint32_t a3 = e4m3x2_to_f16x2(x1 >> 16) & mhi;
-        const uint32_t c0 = e4m3x2_to_f16x2(x2 & 0xffffu) & mlo;
-        const uint32_t c1 = e4m3x2_to_f16x2(x2 >> 16) & mlo;
-        const uint32_t c2 = e4m3x2_to_f16x2(x3 & 0xffffu) & mhi;
-        const uint32_t c3 = e4m3x2_to_f16x2(x3 >> 16) & mhi;
+        // a0 / a1: columns 2r / 2r+1, tokens 2q, 2q+1; a2 / a3: tokens 2q+8, 2q+9
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        e4m3x4_to_f16x2x2(x0, a0, a1);
+        e4m3x4_to_f16x2x2(x1, a2, a3);
+        e4m3x4_to_f16x2x2(x2, c0, c1);
+        e4m3x4_to_f16x2x2(x3, c2, c3);
 #pragma unroll
         for (int nh = 0; nh < kNH; ++nh) {
           mma_f16_16816(o_acc[2 * dt2][nh], a0, a1, a2, a3, pb0[tg][nh], pb1[tg][nh]);
@@ -1055,17 +1055,86 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   reset();
   int stage = 0;
   uint32_t phase = 0;
+  // FP8 with 16-token pages and a ring depth that is a multiple of 4 (so a
+  // warp's next unit is always 4 on, in the slot 4 on): a warp takes its page
+  // and its next one together, as one 32-token group, when both belong to the
+  // same piece; `taken` is that second unit.
+  const bool pairs = FP8 && BS == 16 && p.stages % kConsumerWarps == 0 &&
+                     p.stages >= 3 * kConsumerWarps;
+  long long taken = -1;
   for (long long u = u0; u < u1; ++u) {
     // Ring slot `stage` always belongs to consumer warp stage % 4, so each warp
     // waits on its slots' phases strictly in order (a parity wait cannot tell
     // phase k from phase k - 2) whatever the ring depth.
-    if (stage % kConsumerWarps == warp && !abort) {
+    if constexpr (FP8) {
+      if (stage % kConsumerWarps == warp && !abort && u != taken) {
+        const bool two = pairs && wk.p + kConsumerWarps < wk.n && u + kConsumerWarps < u1;
+        const int stage2 = two ? (stage + kConsumerWarps) % p.stages : stage;
+        const uint32_t phase2 = phase ^ (uint32_t)(stage + kConsumerWarps >= p.stages);
+        const bool ready = __all_sync(
+            0xffffffffu, mbar_wait(&full_bar[stage], phase) &&
+                             (!two || mbar_wait(&full_bar[stage2], phase2)));
+        if (!ready) {
+          if (lane == 0) atomicOr(p.status, kStatusTimeout);
+          abort = true;
+        } else {
+          const int len = sm_len[wk.s];
+          const int valid = min(BS, len - wk.p * BS);
+          const int valid2 = two ? min(BS, len - (wk.p + kConsumerWarps) * BS) : 0;
+          uint8_t* st = smem + stage * kStageBytes;
+          uint8_t* st2 = smem + stage2 * kStageBytes;
+          // Only the piece's last page can end early: zero its V rows past the
+          // sequence (they may hold anything) so the V operand needs no mask.
+          uint8_t* tail_v = (two ? st2 : st) + kPageBytes;
+          const int tail_valid = two ? valid2 : valid;
+          const bool tail = tail_valid < BS;
+          if (tail) {
+            const int chunks = (BS - tail_valid) * L::kHalves * 8;  // 16-byte chunks
+            for (int c = lane; c < chunks; c += 32) {
+              const int r = tail_valid + c / (L::kHalves * 8);
+              const int h = (c / 8) % L::kHalves;
+              *reinterpret_cast<uint4*>(tail_v + h * kTileBytes + r * 128 + (c % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+          }
+          const float* sc = sm_scales + (size_t)stage * 2 * BS;
+          const float* sc2 = sm_scales + (size_t)stage2 * 2 * BS;
+          const uint8_t* q16 = sm_q + qbuf * kQSlotBytes + kQTileBytes;
+          const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
+          if constexpr (BS == 16) {
+            if (two) {
+              const Tile8 t[2] = {{k0, v0, sc, sc + BS, valid},
+                                  {smem_addr(st2), smem_addr(st2 + kPageBytes), sc2, sc2 + BS,
+                                   valid2}};
+              process_fp8(std::integral_constant<int, 2>(), t, q16);
+            } else {
+              const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
+              process_fp8(std::integral_constant<int, 1>(), t, q16);
+            }
+          } else {  // the two 16-token halves of a 32-token page
+            const Tile8 t[2] = {{k0, v0, sc, sc + BS, min(16, valid)},
+                                {k0 + 16 * 128, v0 + 16 * 128, sc + 16, sc + BS + 16,
+                                 max(0, valid - 16)}};
+            process_fp8(std::integral_constant<int, 2>(), t, q16);
+          }
+          // the zeroing's generic writes precede the next tensor copy into the slot
+          if (tail) fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty_bar[stage]);
+            if (two) mbar_arrive(&empty_bar[stage2]);
+          }
+          if (two) taken = u + kConsumerWarps;
+        }
+      }
+    } else if (stage % kConsumerWarps == warp && !abort) {
       // Fused cache append: the last page of a piece holds the sequence's new
       // token.  Its rows (prefetched with the piece's query group) are patched
       // into the page in shared memory once the page has landed (the tensor
       // copy brought whatever the cache held) and stored to the cache for later
       // calls.  This page is read by this CTA alone.
-      const bool patch = !FP8 && p.k_new != nullptr && wk.p == wk.n - 1;
+      const bool patch = p.k_new != nullptr && wk.p == wk.n - 1;
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.
@@ -1088,13 +1157,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           }
           __syncwarp();
         }
-        if constexpr (FP8) {
-          const float* sc = sm_scales + (size_t)stage * 2 * BS;
-          process_page_fp8(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes + kQTileBytes, sc,
-                           sc + BS, valid);
-        } else {
-          process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
-        }
+        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
         if (patch) {
           // the patch's generic writes precede the next tensor copy into this slot
           fence_proxy_async_shared();

@@ -8,7 +8,6 @@
 
 #include <cuda.h>  // CUtensorMap
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 namespace pagedattn {
 
@@ -255,11 +254,15 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 values (low byte first) -> packed f16x2 (exact), low byte in bits 0..15.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four e4m3 values -> two packed f16x2 (exact): bytes 0, 1 -> lo; bytes 2, 3 -> hi.
+// One conversion instruction per half word, no unpacking or repacking around it.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 // Two fp32 values -> packed f16x2 (round to nearest even), `lo` in bits 0..15.
