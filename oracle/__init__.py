@@ -88,6 +88,9 @@ def _load():
             lib.oracle_decode_fp8_pairs.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, LL, F,
                                                      P, I, P, I]
             lib.oracle_decode_fp8_pairs.restype = I
+            lib.oracle_decode_xpacked_pairs.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F,
+                                                         P, I, P, I]
+            lib.oracle_decode_xpacked_pairs.restype = I
             lib.oracle_e4m3_table.argtypes = [P]
             lib.oracle_e4m3_table.restype = None
             lib.oracle_max_threads.argtypes = []
@@ -240,6 +243,51 @@ def decode_fp8(x, pairs: Optional[Sequence[Sequence[int]]] = None,
         _ptr(inp.q), _ptr(inp.k8), _ptr(inp.v8), _ptr(inp.ks), _ptr(inp.vs), _ptr(inp.bt),
         _ptr(inp.lens), inp.num_seqs, inp.H_q, inp.H_kv, inp.D, inp.maxb, inp.BS,
         inp.num_blocks, inp.scale, _ptr(pr), pr.shape[0], _ptr(out), int(num_threads))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return out if pairs is not None else out.reshape(inp.num_seqs, inp.H_q, inp.D)
+
+
+class XpackedInputs:
+    """Host views of one decode problem over x-packed K [NB, H_kv, D/8, BS, 8]
+    and D-major V [NB, H_kv, D, BS] (bf16)."""
+
+    def __init__(self, q, kx, vt, block_tables, seq_lens, scale: float):
+        self.q = _bits(q)
+        self.kx = _bits(kx)
+        self.vt = _bits(vt)
+        self.bt = _i32(block_tables)
+        self.lens = _i32(seq_lens)
+        if self.q.ndim != 3 or self.kx.ndim != 5 or self.vt.ndim != 4:
+            raise ValueError("q must be [S,H_q,D], K [NB,H_kv,D/8,BS,8] and V [NB,H_kv,D,BS]")
+        self.num_seqs, self.H_q, self.D = self.q.shape
+        self.num_blocks, self.H_kv, dx, self.BS, x = self.kx.shape
+        if x != 8 or dx * 8 != self.D or self.vt.shape != (self.num_blocks, self.H_kv, self.D,
+                                                              self.BS):
+            raise ValueError("cache shapes do not match q's head_dim")
+        self.maxb = self.bt.shape[1]
+        self.scale = float(np.float32(scale))
+
+    @classmethod
+    def from_workload(cls, w) -> "XpackedInputs":
+        return cls(w.q, w.kx, w.vt, w.block_tables, w.seq_lens, w.scale)
+
+
+def decode_xpacked(x, pairs: Optional[Sequence[Sequence[int]]] = None,
+                   num_threads: int = 0) -> np.ndarray:
+    """The definition in float64 over x-packed K and D-major V; see the C source."""
+    inp = x if isinstance(x, XpackedInputs) else XpackedInputs.from_workload(x)
+    if pairs is None:
+        pr = np.stack(np.meshgrid(np.arange(inp.num_seqs), np.arange(inp.H_q), indexing="ij"),
+                      axis=-1).reshape(-1, 2).astype(np.int32)
+    else:
+        pr = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+    pr = np.ascontiguousarray(pr)
+    out = np.zeros((pr.shape[0], inp.D), dtype=np.float64)
+    rc = _load().oracle_decode_xpacked_pairs(
+        _ptr(inp.q), _ptr(inp.kx), _ptr(inp.vt), _ptr(inp.bt), _ptr(inp.lens), inp.num_seqs,
+        inp.H_q, inp.H_kv, inp.D, inp.maxb, inp.BS, inp.num_blocks, inp.scale, _ptr(pr),
+        pr.shape[0], _ptr(out), int(num_threads))
     if rc != 0:
         raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
     return out if pairs is not None else out.reshape(inp.num_seqs, inp.H_q, inp.D)

@@ -42,6 +42,14 @@
  *   and everything else is the definition above.  e4m3 is the OCP 8-bit
  *   format with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa bits,
  *   subnormals at exponent 0, no infinities, S.1111.111 = NaN (max 448).
+ *
+ *   The x-packed caches ("Paged Attention Kernel Architecture for BI-V100",
+ *   section 3, Paged K/V Gather) hold the same bf16 values in another order:
+ *     key cache    [num_blocks, H_kv, D / x, block_size, x],  x = 16 / 2 = 8
+ *     value cache  [num_blocks, H_kv, D, block_size]
+ *   so K_t[d] = kx[bt[s, t / BS], g, d / 8, t % BS, d % 8] and
+ *      V_t[d] = vt[bt[s, t / BS], g, d, t % BS];
+ *   everything else is the definition above.
  */
 #include <math.h>
 #include <stdint.h>
@@ -81,15 +89,27 @@ typedef struct {
     const uint8_t* v8;
     const float* k_scale; /* [num_blocks * H_kv * BS] */
     const float* v_scale;
+    const uint16_t* kx;   /* x-packed bf16 K [num_blocks, H_kv, D / 8, BS, 8] */
+    const uint16_t* vt;   /* D-major bf16 V [num_blocks, H_kv, D, BS] */
+    int BS;               /* block size (x-packed layout only) */
 } Cache;
 
 /* Element d of cache row `row` = (block * H_kv + g) * BS + slot. */
 static double cache_k(const Cache* c, size_t row, int d, int D) {
     if (c->k16) return widen_bf16(c->k16[row * D + d]);
+    if (c->kx) {
+        const size_t head = row / (size_t)c->BS, slot = row % (size_t)c->BS;
+        return widen_bf16(c->kx[((head * (size_t)(D / 8) + (size_t)(d / 8)) * c->BS + slot) * 8 +
+                                (size_t)(d % 8)]);
+    }
     return e4m3_value(c->k8[row * D + d]) * (double)c->k_scale[row];
 }
 static double cache_v(const Cache* c, size_t row, int d, int D) {
     if (c->v16) return widen_bf16(c->v16[row * D + d]);
+    if (c->vt) {
+        const size_t head = row / (size_t)c->BS, slot = row % (size_t)c->BS;
+        return widen_bf16(c->vt[(head * (size_t)D + (size_t)d) * c->BS + slot]);
+    }
     return e4m3_value(c->v8[row * D + d]) * (double)c->v_scale[row];
 }
 
@@ -216,7 +236,7 @@ int oracle_decode_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16
                         int H_q, int H_kv, int D, int max_blocks_per_seq, int block_size,
                         long long num_blocks, float scale, const int32_t* pairs, int num_pairs,
                         double* out, int num_threads) {
-    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL, NULL, NULL, 0};
     return decode_pairs(q, &c, block_tables, seq_lens, num_seqs, H_q, H_kv, D,
                         max_blocks_per_seq, block_size, num_blocks, scale, pairs, num_pairs, out,
                         num_threads);
@@ -230,7 +250,21 @@ int oracle_decode_fp8_pairs(const uint16_t* q, const uint8_t* k8, const uint8_t*
                             long long num_blocks, float scale, const int32_t* pairs,
                             int num_pairs, double* out, int num_threads) {
     if (!k8 || !v8 || !k_scale || !v_scale) return ORACLE_ERR_ARGS;
-    const Cache c = {NULL, NULL, k8, v8, k_scale, v_scale};
+    const Cache c = {NULL, NULL, k8, v8, k_scale, v_scale, NULL, NULL, 0};
+    return decode_pairs(q, &c, block_tables, seq_lens, num_seqs, H_q, H_kv, D,
+                        max_blocks_per_seq, block_size, num_blocks, scale, pairs, num_pairs, out,
+                        num_threads);
+}
+
+/* The same rows over x-packed K and D-major V (bf16; head_dim a multiple of 8). */
+int oracle_decode_xpacked_pairs(const uint16_t* q, const uint16_t* kx, const uint16_t* vt,
+                                const int32_t* block_tables, const int32_t* seq_lens,
+                                int num_seqs, int H_q, int H_kv, int D, int max_blocks_per_seq,
+                                int block_size, long long num_blocks, float scale,
+                                const int32_t* pairs, int num_pairs, double* out,
+                                int num_threads) {
+    if (!kx || !vt || D % 8 != 0) return ORACLE_ERR_ARGS;
+    const Cache c = {NULL, NULL, NULL, NULL, NULL, NULL, kx, vt, block_size};
     return decode_pairs(q, &c, block_tables, seq_lens, num_seqs, H_q, H_kv, D,
                         max_blocks_per_seq, block_size, num_blocks, scale, pairs, num_pairs, out,
                         num_threads);
@@ -294,7 +328,7 @@ int oracle_partial_pairs(const uint16_t* q, const uint16_t* k_cache, const uint1
     }
     double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
     if (!z) return ORACLE_ERR_NOMEM;
-    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL, NULL, NULL, 0};
     for (int i = 0; i < num_pairs; ++i)
         row_pieces(q, &c, block_tables, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv, D,
                    max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],

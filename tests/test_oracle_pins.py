@@ -586,3 +586,95 @@ def test_fp8_pins_catch_planted_mistakes(name, old, new, tmp_path):
 
 def test_unmutated_oracle_passes_the_fp8_pins():
     assert _fp8_pins_pass()
+
+
+# ---------------------------------------------------------------- x-packed layout
+# "Paged Attention Kernel Architecture for BI-V100", section 3 (Paged K/V
+# Gather): key cache [num_blocks, kv_heads, head_dim / x, block_size, x] with
+# x = 16 / sizeof(element) (8 for bf16), value cache [num_blocks, kv_heads,
+# head_dim, block_size].
+
+def _xpacked_problem(seed=0, lens=(1, 15, 16, 17, 40, 33), H_q=8, H_kv=2, D=64, BS=16):
+    spec = workloads.custom_spec("xp", len(lens), H_q, H_kv, D, BS, list(lens))
+    w = workloads.make(spec, seed=seed, poison="nan")
+    return w, workloads.to_xpacked(w)
+
+
+def test_xpacked_repack_follows_the_stated_layout():
+    """Element by element, written from the layout's definition (not from the
+    repack): kx[b, g, d // 8, t, d % 8] = K[b, g, t, d] and vt[b, g, d, t] = V[b, g, t, d]."""
+    w, x = _xpacked_problem(1, BS=32, D=128)
+    k = w.k_cache.view(torch.int16)
+    v = w.v_cache.view(torch.int16)
+    kx = x.kx.view(torch.int16)
+    vt = x.vt.view(torch.int16)
+    assert tuple(kx.shape) == (k.shape[0], k.shape[1], k.shape[3] // 8, k.shape[2], 8)
+    assert tuple(vt.shape) == (v.shape[0], v.shape[1], v.shape[3], v.shape[2])
+    rng = np.random.default_rng(0)
+    for _ in range(2000):
+        b, g = int(rng.integers(k.shape[0])), int(rng.integers(k.shape[1]))
+        t, d = int(rng.integers(k.shape[2])), int(rng.integers(k.shape[3]))
+        assert kx[b, g, d // 8, t, d % 8] == k[b, g, t, d]
+        assert vt[b, g, d, t] == v[b, g, t, d]
+
+
+def test_xpacked_decode_equals_decode_of_the_same_values():
+    """Same values in another order: the oracle's output is bit-identical."""
+    for seed, BS, D in ((0, 16, 64), (1, 32, 128), (2, 16, 256)):
+        w, x = _xpacked_problem(seed, BS=BS, D=D)
+        assert np.array_equal(oracle.decode_xpacked(x), oracle.decode(w))
+
+
+def test_xpacked_reads_only_the_sequences_rows():
+    """NaN in every unread slot and block (the poison of the problem) never shows."""
+    w, x = _xpacked_problem(3)
+    assert np.isfinite(oracle.decode_xpacked(x)).all()
+
+
+def _xpacked_pins_pass() -> bool:
+    try:
+        test_xpacked_decode_equals_decode_of_the_same_values()
+        test_xpacked_reads_only_the_sequences_rows()
+    except (AssertionError, oracle.OracleError, FloatingPointError):
+        return False
+    return True
+
+
+XPACKED_MUTANTS = [
+    ("slot and d/8 swapped",
+     "((head * (size_t)(D / 8) + (size_t)(d / 8)) * c->BS + slot) * 8",
+     "((head * (size_t)c->BS + slot) * (size_t)(D / 8) + (size_t)(d / 8)) * 8"),
+    ("x = 16", "* c->BS + slot) * 8 +\n                                (size_t)(d % 8)",
+     "* c->BS + slot) * 8 +\n                                (size_t)(d % 16)"),
+    ("V token-major", "c->vt[(head * (size_t)D + (size_t)d) * c->BS + slot]",
+     "c->vt[(head * (size_t)c->BS + slot) * D + (size_t)d]"),
+    ("V of the K row", "return widen_bf16(c->vt[", "return widen_bf16(c->kx["),
+]
+
+_XPACKED_MUTANT_RUNNER = _MUTANT_RUNNER.replace(
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs")',
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs", '
+    '"oracle_decode_xpacked_pairs")').replace("T._pins_pass()", "T._xpacked_pins_pass()")
+
+
+@pytest.mark.parametrize("name,old,new", XPACKED_MUTANTS, ids=[m[0] for m in XPACKED_MUTANTS])
+def test_xpacked_pins_catch_planted_mistakes(name, old, new, tmp_path):
+    import subprocess
+    import sys
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, name
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _XPACKED_MUTANT_RUNNER.format(root=os.path.dirname(here), tests=here, so=str(so))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode < 0 or "PINS_FAIL" in r.stdout, \
+        f"no pin noticed the planted mistake: {name}\n{r.stdout}\n{r.stderr[-2000:]}"
+
+
+def test_unmutated_oracle_passes_the_xpacked_pins():
+    assert _xpacked_pins_pass()

@@ -323,6 +323,27 @@ def to_fp8(w: Workload) -> Fp8Workload:
     return Fp8Workload(base=w, k8=k8, v8=v8, k_scale=ks, v_scale=vs)
 
 
+@dataclass
+class XpackedWorkload:
+    """A workload whose bf16 caches are in the x-packed K / D-major V layout:
+    kx[b, g, d // 8, t, d % 8] = k_cache[b, g, t, d], vt[b, g, d, t] = v_cache[b, g, t, d]."""
+
+    base: Workload
+    kx: torch.Tensor  # bf16 [num_blocks, H_kv, D / 8, BS, 8]
+    vt: torch.Tensor  # bf16 [num_blocks, H_kv, D, BS]
+
+    def __getattr__(self, name):
+        return getattr(self.base, name)
+
+
+def to_xpacked(w: Workload) -> XpackedWorkload:
+    """The same problem with its caches repacked (same values, other order)."""
+    nb, hk, bs, d = w.k_cache.shape
+    kx = w.k_cache.view(nb, hk, bs, d // 8, 8).permute(0, 1, 3, 2, 4).contiguous()
+    vt = w.v_cache.permute(0, 1, 3, 2).contiguous()
+    return XpackedWorkload(base=w, kx=kx, vt=vt)
+
+
 def host_copy(w: Workload) -> Workload:
     """The same workload with every tensor copied to host memory."""
     return Workload(spec=w.spec, seed=w.seed, q=w.q.cpu(), k_cache=w.k_cache.cpu(),
