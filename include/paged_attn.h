@@ -180,6 +180,27 @@ PAGED_ATTN_API int paged_attn_decode_fp8(const void* q, const void* k_cache, con
                                          void* stream);
 
 /*
+ * The same operation over bf16 caches in the x-packed layout ("Paged Attention
+ * Kernel Architecture for BI-V100", section 3, Paged K/V Gather: the key cache
+ * split into 16-byte packs of x = 8 elements, the value cache head_dim-major):
+ *
+ *   k_cache  [num_blocks, H_kv, head_dim / 8, block_size, 8]  bf16  (read)
+ *   v_cache  [num_blocks, H_kv, head_dim, block_size]         bf16  (read)
+ *
+ * so K_t[d] = k_cache[b, g, d / 8, t % block_size, d % 8] and
+ * V_t[d] = v_cache[b, g, d, t % block_size] with b = block_tables[s, t / block_size].
+ * Everything else (q, out, tables, lengths, sizes, scale, workspace, errors,
+ * rows past a sequence's length) is as paged_attn_decode; the arithmetic is
+ * the same, so the output equals paged_attn_decode's over the same values.
+ */
+PAGED_ATTN_API int paged_attn_decode_xpacked(const void* q, const void* k_cache,
+                                             const void* v_cache, void* out,
+                                             const int32_t* block_tables,
+                                             const int32_t* seq_lens, int num_seqs, int H_q,
+                                             int H_kv, int head_dim, int max_blocks_per_seq,
+                                             int block_size, float scale, void* stream);
+
+/*
  * Cache append ("reshape and cache") of one new token per sequence, the write
  * that precedes the decode: the paged-decode layout above counts the new token
  * in seq_lens ("context length including the new token"), so its K and V must

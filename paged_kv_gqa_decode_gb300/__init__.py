@@ -24,6 +24,7 @@ __all__ = [
     "paged_attn_append_decode",
     "paged_kv_append",
     "paged_attn_decode_fp8",
+    "paged_attn_decode_xpacked",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "EXPORTED_SYMBOLS",
@@ -42,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "paged_kv_append",
     "paged_attn_append_decode",
     "paged_attn_decode_fp8",
+    "paged_attn_decode_xpacked",
     "paged_attn_status_string",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
@@ -88,6 +90,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_append_decode.restype = I
         lib.paged_attn_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.paged_attn_decode_fp8.restype = I
+        lib.paged_attn_decode_xpacked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.paged_attn_decode_xpacked.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -201,6 +205,33 @@ def paged_attn_decode_static(q, k_cache, v_cache, block_tables, seq_lens, scale:
         out = torch.empty_like(q)
     _check(load().paged_attn_decode_static(*_args(q, k_cache, v_cache, out, block_tables,
                                                   seq_lens, scale), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_xpacked(q, kx, vt, block_tables, seq_lens, scale: float, out=None,
+                              stream=None):
+    """Decode over x-packed bf16 caches (see paged_attn.h): kx [num_blocks, H_kv,
+    head_dim / 8, block_size, 8], vt [num_blocks, H_kv, head_dim, block_size]."""
+    import torch
+
+    for name, t in (("q", q), ("kx", kx), ("vt", vt), ("block_tables", block_tables),
+                    ("seq_lens", seq_lens)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    num_seqs, H_q, D = (int(x) for x in q.shape)
+    if kx.dim() != 5 or vt.dim() != 4:
+        raise ValueError("kx must be [NB, H_kv, D/8, BS, 8] and vt [NB, H_kv, D, BS]")
+    nb, H_kv, dx, BS, x = (int(v) for v in kx.shape)
+    if x != 8 or dx * 8 != D or tuple(vt.shape) != (nb, H_kv, D, BS):
+        raise ValueError("kx / vt shapes do not match q's head_dim")
+    if out is None:
+        out = torch.empty_like(q)
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(load().paged_attn_decode_xpacked(_ptr(q), _ptr(kx), _ptr(vt), _ptr(out),
+                                            _ptr(block_tables), _ptr(seq_lens), num_seqs, H_q,
+                                            H_kv, D, maxb, BS, float(scale), _stream(stream)))
     return out
 
 

@@ -7,7 +7,7 @@ namespace pagedattn {
 cudaError_t launch_decode_fp8_d128(int block_size, bool g16, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const DecodeParams& p, int grid,
                                    size_t smem, cudaStream_t stream) {
-  return launch_for_dim<128, true>(block_size, g16, tk, tv, p, grid, smem, stream);
+  return launch_for_dim<128, kKvFp8>(block_size, g16, tk, tv, p, grid, smem, stream);
 }
 
 }  // namespace pagedattn

@@ -62,6 +62,11 @@ constexpr int kMinPagesPerCta = 8;
 constexpr int kMaxStages = 16;  // ring depth cap (slot s belongs to consumer warp s % 4)
 constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
 constexpr int kConsumerBarrier = 1;
+// KV cache formats: bf16 [num_blocks, H_kv, BS, D]; FP8 e4m3 in that layout with
+// per-row floats; bf16 x-packed K / D-major V.
+constexpr int kKvBf16 = 0;
+constexpr int kKvFp8 = 1;
+constexpr int kKvXpacked = 2;
 // Block tables up to this size are prefetched into L2 at kernel entry.
 constexpr size_t kBlockTablePrefetchBytes = size_t(4) << 20;
 
@@ -163,10 +168,18 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
 // row; the products run on f16 tensor cores (e4m3 -> f16 is exact, q is turned
 // into f16 once per piece), the K row floats scale the scores and the V row
 // floats are folded into the probabilities.
-template <int D, int BS, bool G16, bool FP8 = false>
+//
+// XP (x-packed): bf16 caches with K as [num_blocks, H_kv, D / 8, BS, 8] and V as
+// [num_blocks, H_kv, D, BS] ("Paged Attention Kernel Architecture for BI-V100",
+// section 3).  A K page lands in shared memory as [D / 8][BS][16 bytes] and a V
+// page as [D][BS] (V^T, 32- or 64-byte rows), so both MMA operands come from
+// plain ldmatrix with other addresses; everything else is the bf16 path.
+template <int D, int BS, bool G16, int KV = kKvBf16>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr bool FP8 = KV == kKvFp8;
+  constexpr bool XP = KV == kKvXpacked;
   using L = SmemLayout<D, BS, FP8>;
   static_assert(!FP8 || D >= 128, "FP8 caches need head_dim 128 or 256");
   constexpr int kTileBytes = L::kTileBytes;
@@ -339,13 +352,26 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           } else {
             mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
             uint8_t* st = smem + stage * kStageBytes;
-            tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
-            tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
+            if constexpr (XP) {
+              // a page of one KV head is contiguous in both x-packed caches: K
+              // (and V of 16-token pages) come as one bulk copy each; V of 32-token
+              // pages through the tensor map, for the 64-byte swizzle (unswizzled
+              // 64-byte rows would cost 4-way bank conflicts in the V reads)
+              const size_t off = ((size_t)(pb < 0 ? 0 : pb) * H_kv + g) * (size_t)(D * BS);
+              bulk_load(st, p.k_cache + off, kPageBytes, &full_bar[stage]);
+              if constexpr (BS == 16)
+                bulk_load(st + kPageBytes, p.v_cache + off, kPageBytes, &full_bar[stage]);
+              else
+                tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, 0, g, pb, policy);
+            } else {
+              tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
+              tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
+            }
             if constexpr (FP8) {
               // the page's K and V row floats (a block outside a checked pool reads
               // block 0's: its rows are zero-filled by the tensor copy anyway)
               const long long b =
-                  p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks) ? 0 : pb;
+                  pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
               const size_t row = ((size_t)b * H_kv + g) * BS;
               float* sc = sm_scales + (size_t)stage * 2 * BS;
               bulk_load(sc, p.k_scale + row, BS * 4, &full_bar[stage]);
@@ -489,7 +515,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         for (int tg = 0; tg < kTG; ++tg) {
           const int tok = 16 * tg + (lane & 7) + ((li & 1) << 3);
           uint32_t a0, a1, a2, a3;
-          ldmatrix_x4(kbase + coff + (uint32_t)(tok * 128), a0, a1, a2, a3);
+          if constexpr (XP)  // [D / 8][BS][8]: 16-byte rows, consecutive tokens adjacent
+            ldmatrix_x4(kbase + (uint32_t)((chunk * BS + tok) * 16), a0, a1, a2, a3);
+          else
+            ldmatrix_x4(kbase + coff + (uint32_t)(tok * 128), a0, a1, a2, a3);
 #pragma unroll
           for (int nh = 0; nh < kNH; ++nh)
             mma_bf16_16816(x ? s_odd[tg][nh] : s_acc[tg][nh], a0, a1, a2, a3, qf[x][nh][0],
@@ -579,11 +608,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       const int tok = 16 * tg + (lane & 7) + ((li >> 1) << 3);
 #pragma unroll
       for (int dt = 0; dt < kDT; ++dt) {
-        const int chunk = 2 * dt + (li & 1);
-        const uint32_t addr = vbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
-                                                 (((chunk & 7) ^ (lane & 7)) << 4));
         uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        if constexpr (XP) {
+          // V^T rows d (BS * 2 bytes each), 16-byte chunk j = 8 tokens; 32-token
+          // pages carry the 64-byte TMA swizzle (chunk j stored at j ^ bits 7-8 of
+          // the row's address), 16-token pages are a plain copy (2-way conflicts)
+          const int d = 16 * dt + (lane & 7) + ((li & 1) << 3);
+          const int j = 2 * tg + (li >> 1);
+          const int sw = BS == 16 ? 0 : (d >> 1) & 3;
+          ldmatrix_x4(vbase + (uint32_t)(d * BS * 2 + ((j ^ sw) << 4)), a0, a1, a2, a3);
+        } else {
+          const int chunk = 2 * dt + (li & 1);
+          const uint32_t addr = vbase + (uint32_t)((chunk >> 3) * kTileBytes + tok * 128 +
+                                                   (((chunk & 7) ^ (lane & 7)) << 4));
+          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        }
         a0 &= mlo;
         a1 &= mlo;
         a2 &= mhi;
@@ -1134,7 +1173,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // into the page in shared memory once the page has landed (the tensor
       // copy brought whatever the cache held) and stored to the cache for later
       // calls.  This page is read by this CTA alone.
-      const bool patch = p.k_new != nullptr && wk.p == wk.n - 1;
+      const bool patch = !XP && p.k_new != nullptr && wk.p == wk.n - 1;
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.

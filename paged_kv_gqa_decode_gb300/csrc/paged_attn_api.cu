@@ -99,6 +99,7 @@ struct Plan {
   int D, BS, G;
   bool g16;
   bool fp8;     // FP8 caches
+  bool xp;      // x-packed K / D-major V caches (bf16)
   int chunk;    // sequences per launch
   int stages;   // pipeline depth
   size_t smem;  // dynamic shared memory per CTA
@@ -149,6 +150,7 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
               bool fp8 = false) {
   pl->D = D;
   pl->fp8 = fp8;
+  pl->xp = false;
   pl->BS = BS;
   pl->G = H_q / H_kv;
   pl->g16 = pl->G > 8;
@@ -252,9 +254,44 @@ int encode_cache_map(const void* base, int D, int BS, int H_kv, long long num_bl
   return PAGED_ATTN_OK;
 }
 
-cudaError_t launch_dim(int D, int BS, bool g16, bool fp8, const CUtensorMap& tk,
+// x-packed caches.  A page of one KV head is contiguous in both (K [num_blocks,
+// H_kv, D / 8, BS, 8], V [num_blocks, H_kv, D, BS]) and the kernel bulk-copies
+// it, except V pages of 32 tokens, read through the 4-D view (BS, D, H_kv,
+// block) of V: the box {BS, D, 1, 1} lands as [D][BS] with the 64-byte swizzle.
+// The K map of the launch is unused and set to the same view.
+int encode_xpacked_maps(const void* v, int D, int BS, int H_kv, long long num_blocks,
+                        CUtensorMap* tk, CUtensorMap* tv) {
+  EncodeTiledFn enc = nullptr;
+  int rc = get_encoder(&enc);
+  if (rc != PAGED_ATTN_OK) return rc;
+  const cuuint64_t head_bytes = (cuuint64_t)D * BS * 2;
+  const cuuint64_t block_bytes = head_bytes * (cuuint64_t)H_kv;
+  cuuint64_t nb = (cuuint64_t)num_blocks;
+  if (num_blocks <= 0) {
+    nb = ((cuuint64_t)1 << 40) / block_bytes;
+    if (nb > 0x7fffffffULL) nb = 0x7fffffffULL;
+  }
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const cuuint64_t vdims[4] = {(cuuint64_t)BS, (cuuint64_t)D, (cuuint64_t)H_kv, nb};
+  const cuuint64_t vstrides[3] = {(cuuint64_t)BS * 2, head_bytes, block_bytes};
+  const cuuint32_t vbox[4] = {(cuuint32_t)BS, (cuuint32_t)D, 1, 1};
+  CUresult r = enc(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v), vdims,
+                   vstrides, vbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   BS == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail((int)r);
+  *tk = *tv;
+  return PAGED_ATTN_OK;
+}
+
+cudaError_t launch_dim(int D, int BS, bool g16, bool fp8, bool xp, const CUtensorMap& tk,
                        const CUtensorMap& tv, const DecodeParams& p, int grid, size_t smem,
                        cudaStream_t st) {
+  if (xp) {
+    if (D == 64) return launch_decode_xp_d64(BS, g16, tk, tv, p, grid, smem, st);
+    if (D == 128) return launch_decode_xp_d128(BS, g16, tk, tv, p, grid, smem, st);
+    return launch_decode_xp_d256(BS, g16, tk, tv, p, grid, smem, st);
+  }
   if (fp8)
     return D == 128 ? launch_decode_fp8_d128(BS, g16, tk, tv, p, grid, smem, st)
                     : launch_decode_fp8_d256(BS, g16, tk, tv, p, grid, smem, st);
@@ -280,10 +317,16 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
         cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
         const float* k_scale = nullptr, const float* v_scale = nullptr) {
   CUtensorMap tk, tv;
-  int rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, pl.fp8);
-  if (rc != PAGED_ATTN_OK) return rc;
-  rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv, pl.fp8);
-  if (rc != PAGED_ATTN_OK) return rc;
+  int rc;
+  if (pl.xp) {
+    rc = encode_xpacked_maps(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, &tv);
+    if (rc != PAGED_ATTN_OK) return rc;
+  } else {
+    rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, pl.fp8);
+    if (rc != PAGED_ATTN_OK) return rc;
+    rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv, pl.fp8);
+    if (rc != PAGED_ATTN_OK) return rc;
+  }
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   for (int s0 = 0; s0 < num_seqs; s0 += pl.chunk) {
     const int n = num_seqs - s0 < pl.chunk ? num_seqs - s0 : pl.chunk;
@@ -311,7 +354,8 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
     p.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    cudaError_t e = launch_dim(pl.D, pl.BS, pl.g16, pl.fp8, tk, tv, p, pl.grid, pl.smem, stream);
+    cudaError_t e =
+        launch_dim(pl.D, pl.BS, pl.g16, pl.fp8, pl.xp, tk, tv, p, pl.grid, pl.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return PAGED_ATTN_OK;
@@ -399,6 +443,26 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
   Plan pl;
   if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
     return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
+int paged_attn_decode_xpacked(const void* q, const void* k_cache, const void* v_cache, void* out,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                              int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                              int block_size, float scale, void* stream) {
+  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                         head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+    return rc;
+  pl.xp = true;  // same shared-memory plan as the bf16 layout
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
