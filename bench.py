@@ -260,6 +260,11 @@ def run_ours(args, world, rank, local):
         kv = sum(int(L) for L in lens) * spec.H_kv * (2 * spec.D + 8)
         nbytes = dict(nbytes, kv=kv, total=kv + nbytes["q_out"] + nbytes["block_table"])
         base = (f.k8, f.v8, f.k_scale, f.v_scale)
+    elif args.kv == "xpacked":
+        # the same bf16 values in the x-packed K / D-major V layout
+        x = workloads.to_xpacked(w)
+        w.k_cache = w.v_cache = None
+        base = (x.kx, x.vt, None, None)
     else:
         base = (w.k_cache, w.v_cache, None, None)
     kv_bytes = sum(t.numel() * t.element_size() for t in base if t is not None)
@@ -288,6 +293,8 @@ def run_ours(args, world, rank, local):
         if fp8:
             pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
                                      stream=stream)
+        elif args.kv == "xpacked":
+            pa.paged_attn_decode_xpacked(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
         elif op == "decode":
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
         elif op == "append_decode":
@@ -391,9 +398,9 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = nbytes["total"] / kernel_s / 1e9
-        traffic = profile_traffic(args.config) if op == "decode" and not fp8 else None
+        traffic = profile_traffic(args.config) if op == "decode" and args.kv == "bf16" else None
         cpu = None
-        if not args.no_cpu_baseline and not fp8:  # the baseline leg times the bf16 oracle
+        if not args.no_cpu_baseline and args.kv == "bf16":  # the baseline leg times the bf16 oracle
             w_host = workloads.host_copy(w)
             threads = len(os.sched_getaffinity(0))
             secs, b, ngroups, total_groups = oracle_baseline(w_host, spec, args.cpu_budget,
@@ -436,6 +443,8 @@ def run_ours(args, world, rank, local):
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback 6800 GB/s",
                 "kernel": "paged_decode_kernel over FP8 caches (one launch per step)" if fp8 else
+                "paged_decode_kernel over x-packed caches (one launch per step)"
+                if args.kv == "xpacked" else
                 {"decode": "paged_decode_kernel (one launch per step, fused combine)",
                            "append_decode": "paged_decode_kernel with the fused cache append "
                                             "(one launch per step)",
@@ -513,8 +522,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="llama8b", choices=sorted(workloads.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
-                    help="cache format: bf16, or e4m3 bytes with a float per cache row")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8", "xpacked"],
+                    help="cache format: bf16, e4m3 bytes with a float per cache row, or bf16 "
+                         "in the x-packed K / D-major V layout")
     ap.add_argument("--op", default="decode",
                     choices=["decode", "append_decode", "append_then_decode"],
                     help="decode alone, or with each sequence's new token appended to the "
@@ -528,8 +538,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.kv == "fp8" and args.op != "decode":
-        ap.error("--kv fp8 runs the decode alone (--op decode)")
+    if args.kv != "bf16" and args.op != "decode":
+        ap.error(f"--kv {args.kv} runs the decode alone (--op decode)")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
