@@ -91,6 +91,8 @@ def _load():
             lib.oracle_decode_xpacked_pairs.argtypes = [P, P, P, P, P, I, I, I, I, I, I, LL, F,
                                                          P, I, P, I]
             lib.oracle_decode_xpacked_pairs.restype = I
+            lib.oracle_decode_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, LL, F, I, P, I]
+            lib.oracle_decode_multi.restype = I
             lib.oracle_e4m3_table.argtypes = [P]
             lib.oracle_e4m3_table.restype = None
             lib.oracle_max_threads.argtypes = []
@@ -291,6 +293,44 @@ def decode_xpacked(x, pairs: Optional[Sequence[Sequence[int]]] = None,
     if rc != 0:
         raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
     return out if pairs is not None else out.reshape(inp.num_seqs, inp.H_q, inp.D)
+
+
+def decode_multi(x: Inputs, qo_indptr, causal: bool = True, num_threads: int = 0) -> np.ndarray:
+    """Multi-token decode in float64 (see the C source): ``x.q`` holds the
+    [total_q, H_q, D] query rows, sequence s owning rows qo_indptr[s] ..
+    qo_indptr[s+1] - 1 (its last tokens); returns [total_q, H_q, D]."""
+    qo = _i32(qo_indptr)
+    if qo.shape != (len(x.lens) + 1,) or int(qo[-1]) != x.q.shape[0]:
+        raise ValueError("qo_indptr must be [num_seqs + 1] ending at q's row count")
+    out = np.zeros(x.q.shape, dtype=np.float64)
+    rc = _load().oracle_decode_multi(
+        _ptr(x.q), _ptr(x.k), _ptr(x.v), _ptr(qo), _ptr(x.bt), _ptr(x.lens), len(x.lens),
+        x.H_q, x.H_kv, x.D, x.maxb, x.BS, x.num_blocks, x.scale, int(bool(causal)), _ptr(out),
+        int(num_threads))
+    if rc != 0:
+        raise OracleError(f"oracle rejected the input: {ERRORS.get(rc, rc)}")
+    return out
+
+
+class MultiInputs(Inputs):
+    """Inputs whose q holds any number of query rows ([total_q, H_q, D]); the
+    sequence count comes from seq_lens."""
+
+    def __init__(self, q, k_cache, v_cache, block_tables, seq_lens, scale: float):
+        self.q = _bits(q)
+        self.k = _bits(k_cache)
+        self.v = _bits(v_cache)
+        self.bt = _i32(block_tables)
+        self.lens = _i32(seq_lens)
+        if self.q.ndim != 3 or self.k.ndim != 4 or self.k.shape != self.v.shape:
+            raise ValueError("q must be [total_q,H_q,D] and the caches [NB,H_kv,BS,D]")
+        _, self.H_q, self.D = self.q.shape
+        self.num_seqs = len(self.lens)
+        self.num_blocks, self.H_kv, self.BS, Dk = self.k.shape
+        if Dk != self.D or self.bt.shape[0] != self.num_seqs:
+            raise ValueError("shapes disagree")
+        self.maxb = self.bt.shape[1]
+        self.scale = float(np.float32(scale))
 
 
 def e4m3_table() -> np.ndarray:

@@ -50,6 +50,16 @@
  *   so K_t[d] = kx[bt[s, t / BS], g, d / 8, t % BS, d % 8] and
  *      V_t[d] = vt[bt[s, t / BS], g, d, t % BS];
  *   everything else is the definition above.
+ *
+ *   Multi-token decode (AstrAI's CUDA Kernels page: the prefill path over a
+ *   ragged batch, "Q Scheduling and KV Addressing", with qo_indptr, and the
+ *   wrappers' is_causal; "Python Wrappers"): sequence s owns the query rows
+ *   qo_indptr[s] .. qo_indptr[s+1] - 1 of q ([total_q, H_q, D]), its last
+ *   q_len = qo_indptr[s+1] - qo_indptr[s] tokens, all of them already in the
+ *   cache (L = seq_lens[s] counts them).  With the causal mask, query i sees the
+ *   tokens t <= L - q_len + i (its own position and everything before); without
+ *   it, all L tokens.  Each query row is the definition above over the tokens
+ *   it sees; a row that sees none is zero.
  */
 #include <math.h>
 #include <stdint.h>
@@ -136,11 +146,11 @@ static int check_inputs(const int32_t* bt, const int32_t* seq_lens, int num_seqs
  *   M = max_t z_t,  l = sum_t exp(z_t - M),  o[d] = sum_t exp(z_t - M) V_t[d].
  * An empty range gives M = -inf, l = 0, o = 0.  z is scratch of >= t1 - t0 doubles.
  */
-static void row_pieces(const uint16_t* q, const Cache* c, const int32_t* bt, int s, int h,
-                       int H_q, int H_kv, int D, int max_blocks, int BS, double scale, int t0,
-                       int t1, double* z, double* M_out, double* l_out, double* o) {
-    const int g = (int)(((long long)h * H_kv) / H_q);
-    const uint16_t* qrow = q + ((size_t)s * H_q + h) * D;
+static int kv_head(int h, int H_q, int H_kv) { return (int)(((long long)h * H_kv) / H_q); }
+
+static void row_pieces(const uint16_t* qrow, const Cache* c, const int32_t* bt, int s, int g,
+                       int H_kv, int D, int max_blocks, int BS, double scale, int t0, int t1,
+                       double* z, double* M_out, double* l_out, double* o) {
 
     for (int d = 0; d < D; ++d) o[d] = 0.0;
     *l_out = 0.0;
@@ -176,7 +186,9 @@ static void attend_row(const uint16_t* q, const Cache* c, const int32_t* bt,
                        const int32_t* seq_lens, int s, int h, int H_q, int H_kv, int D,
                        int max_blocks, int BS, double scale, double* z, double* out_row) {
     double M, l;
-    row_pieces(q, c, bt, s, h, H_q, H_kv, D, max_blocks, BS, scale, 0, seq_lens[s], z, &M, &l,
+    const int g = kv_head(h, H_q, H_kv);
+    const uint16_t* qrow = q + ((size_t)s * H_q + h) * D;
+    row_pieces(qrow, c, bt, s, g, H_kv, D, max_blocks, BS, scale, 0, seq_lens[s], z, &M, &l,
                out_row);
     if (l > 0.0)
         for (int d = 0; d < D; ++d) out_row[d] /= l;
@@ -329,10 +341,73 @@ int oracle_partial_pairs(const uint16_t* q, const uint16_t* k_cache, const uint1
     double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
     if (!z) return ORACLE_ERR_NOMEM;
     const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL, NULL, NULL, 0};
-    for (int i = 0; i < num_pairs; ++i)
-        row_pieces(q, &c, block_tables, pairs[2 * i], pairs[2 * i + 1], H_q, H_kv, D,
-                   max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],
+    for (int i = 0; i < num_pairs; ++i) {
+        const int s = pairs[2 * i], h = pairs[2 * i + 1];
+        row_pieces(q + ((size_t)s * H_q + h) * D, &c, block_tables, s, kv_head(h, H_q, H_kv), H_kv,
+                   D, max_blocks_per_seq, block_size, (double)scale, ranges[2 * i],
                    ranges[2 * i + 1], z, M + i, l + i, o + (size_t)i * D);
+    }
     free(z);
     return ORACLE_OK;
+}
+
+/*
+ * Multi-token decode: q and out are [total_q, H_q, D] with total_q =
+ * qo_indptr[num_seqs]; qo_indptr [num_seqs + 1] is non-decreasing from 0 and
+ * q_len <= L for every sequence.  causal != 0 applies the causal mask.
+ */
+int oracle_decode_multi(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* qo_indptr, const int32_t* block_tables,
+                        const int32_t* seq_lens, int num_seqs, int H_q, int H_kv, int D,
+                        int max_blocks_per_seq, int block_size, long long num_blocks,
+                        float scale, int causal, double* out, int num_threads) {
+    int rc = check_inputs(block_tables, seq_lens, num_seqs, H_q, H_kv, D, max_blocks_per_seq,
+                          block_size, num_blocks);
+    if (rc != ORACLE_OK) return rc;
+    if (!qo_indptr || qo_indptr[0] != 0) return ORACLE_ERR_ARGS;
+    int Lmax = 1;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int ql = qo_indptr[s + 1] - qo_indptr[s];
+        if (ql < 0 || ql > seq_lens[s]) return ORACLE_ERR_ARGS;
+        if (seq_lens[s] > Lmax) Lmax = seq_lens[s];
+    }
+    const Cache c = {k_cache, v_cache, NULL, NULL, NULL, NULL, NULL, NULL, 0};
+    const double sc = (double)scale;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(num_threads)
+#endif
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)Lmax);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int s = 0; s < num_seqs; ++s) {
+            if (!z) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                failed = 1;
+                continue;
+            }
+            const int L = seq_lens[s];
+            const int ql = qo_indptr[s + 1] - qo_indptr[s];
+            for (int i = 0; i < ql; ++i) {
+                const int seen = causal ? L - ql + i + 1 : L;  /* tokens t < seen */
+                const size_t r = (size_t)qo_indptr[s] + (size_t)i;
+                for (int h = 0; h < H_q; ++h) {
+                    double M, l;
+                    double* orow = out + (r * H_q + h) * D;
+                    row_pieces(q + (r * H_q + h) * D, &c, block_tables, s, kv_head(h, H_q, H_kv),
+                               H_kv, D, max_blocks_per_seq, block_size, sc, 0, seen, z, &M, &l,
+                               orow);
+                    if (l > 0.0)
+                        for (int d = 0; d < D; ++d) orow[d] /= l;
+                }
+            }
+        }
+        free(z);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }

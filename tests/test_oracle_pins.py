@@ -678,3 +678,128 @@ def test_xpacked_pins_catch_planted_mistakes(name, old, new, tmp_path):
 
 def test_unmutated_oracle_passes_the_xpacked_pins():
     assert _xpacked_pins_pass()
+
+
+# ---------------------------------------------------------------- multi-token decode
+# AstrAI CUDA Kernels page, "Q Scheduling and KV Addressing" (ragged qo_indptr)
+# and "Python Wrappers" (is_causal): each sequence's last q_len tokens query the
+# cache; with the causal mask query i sees the tokens t <= L - q_len + i.
+
+def _multi_problem(seed, lens, qlens, H_q, H_kv, D, BS):
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    K = [_bf16(torch.randn(L, H_kv, D, generator=g)) for L in lens]
+    V = [_bf16(torch.randn(L, H_kv, D, generator=g)) for L in lens]
+    kc, vc, bt, sl = _page(K, V, BS, rng)
+    qo = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q = _bf16(torch.randn(int(qo[-1]), H_q, D, generator=g))
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    return q, K, V, oracle.MultiInputs(q, kc, vc, bt, sl, scale), qo, scale
+
+
+MULTI_CASES = [
+    # seed, lens, qlens, H_q, H_kv, D, BS
+    (1, [37, 100, 5], [1, 4, 5], 4, 2, 64, 16),
+    (2, [16, 17, 33, 64], [2, 0, 7, 3], 8, 2, 32, 16),
+    (3, [129, 8], [16, 8], 6, 1, 64, 32),
+]
+
+
+@pytest.mark.parametrize("seed,lens,qlens,H_q,H_kv,D,BS", MULTI_CASES)
+def test_multi_matches_torch_sdpa_with_a_causal_mask(seed, lens, qlens, H_q, H_kv, D, BS):
+    """torch float64 attention over the unpaged K/V with the mask written from
+    the definition: query i of a sequence sees t <= L - q_len + i."""
+    q, K, V, x, qo, scale = _multi_problem(seed, lens, qlens, H_q, H_kv, D, BS)
+    got = oracle.decode_multi(x, qo, causal=True)
+    for s, (L, ql) in enumerate(zip(lens, qlens)):
+        if ql == 0:
+            continue
+        G = H_q // H_kv
+        k = K[s].double().transpose(0, 1).repeat_interleave(G, dim=0)[None]  # [1, H_q, L, D]
+        v = V[s].double().transpose(0, 1).repeat_interleave(G, dim=0)[None]
+        qq = q[qo[s]:qo[s + 1]].double().transpose(0, 1)[None]              # [1, H_q, ql, D]
+        mask = torch.tensor([[t <= L - ql + i for t in range(L)] for i in range(ql)])
+        ref = F.scaled_dot_product_attention(qq, k, v, attn_mask=mask, scale=scale)
+        np.testing.assert_allclose(got[qo[s]:qo[s + 1]], ref[0].transpose(0, 1).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def test_multi_rows_equal_single_token_decodes_of_their_prefixes():
+    """Row (s, i) is the single-token decode of sequence s cut at L - q_len + i + 1;
+    without the mask, of the whole sequence."""
+    q, K, V, x, qo, scale = _multi_problem(4, [40, 70], [3, 6], 8, 2, 64, 16)
+    rows_s = np.repeat(np.arange(2), np.diff(qo))
+    rows_i = np.arange(qo[-1]) - qo[rows_s]
+    lens = x.lens[rows_s]
+    for causal in (True, False):
+        cut = lens - (np.diff(qo)[rows_s] - rows_i - 1) if causal else lens
+        single = oracle.Inputs(q, x.k, x.v, x.bt[rows_s], cut.astype(np.int32), scale)
+        assert np.array_equal(oracle.decode_multi(x, qo, causal=causal), oracle.decode(single))
+
+
+def test_multi_with_one_query_per_sequence_is_the_decode():
+    w = workloads.make("tiny", poison="nan")
+    inp = oracle.Inputs.from_workload(w)
+    qo = np.arange(inp.num_seqs + 1, dtype=np.int32)
+    x = oracle.MultiInputs(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+    assert np.array_equal(oracle.decode_multi(x, qo), oracle.decode(inp))
+
+
+def test_multi_rejects_bad_offsets():
+    q, K, V, x, qo, scale = _multi_problem(5, [10, 20], [2, 3], 4, 2, 32, 16)
+    bad = qo.copy()
+    bad[1] = 11  # q_len 11 > L = 10
+    bad[2] = 14
+    with pytest.raises((oracle.OracleError, ValueError)):
+        oracle.decode_multi(oracle.MultiInputs(torch.zeros(14, 4, 32, dtype=torch.bfloat16),
+                                               x.k, x.v, x.bt, x.lens, scale), bad)
+
+
+def _multi_pins_pass() -> bool:
+    try:
+        for case in MULTI_CASES:
+            test_multi_matches_torch_sdpa_with_a_causal_mask(*case)
+        test_multi_rows_equal_single_token_decodes_of_their_prefixes()
+    except (AssertionError, oracle.OracleError, FloatingPointError, ValueError):
+        return False
+    return True
+
+
+MULTI_MUTANTS = [
+    ("query sees one token too many", "const int seen = causal ? L - ql + i + 1 : L;",
+     "const int seen = causal ? L - ql + i + 2 : L;"),
+    ("query sees its own token not", "const int seen = causal ? L - ql + i + 1 : L;",
+     "const int seen = causal ? L - ql + i : L;"),
+    ("queries aligned to the start", "const int seen = causal ? L - ql + i + 1 : L;",
+     "const int seen = causal ? i + 1 : L;"),
+    ("query row of the first token", "const size_t r = (size_t)qo_indptr[s] + (size_t)i;",
+     "const size_t r = (size_t)qo_indptr[s];"),
+]
+
+_MULTI_MUTANT_RUNNER = _MUTANT_RUNNER.replace(
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs")',
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs", "oracle_decode_multi")'
+).replace("T._pins_pass()", "T._multi_pins_pass()")
+
+
+@pytest.mark.parametrize("name,old,new", MULTI_MUTANTS, ids=[m[0] for m in MULTI_MUTANTS])
+def test_multi_pins_catch_planted_mistakes(name, old, new, tmp_path):
+    import subprocess
+    import sys
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, name
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _MULTI_MUTANT_RUNNER.format(root=os.path.dirname(here), tests=here, so=str(so))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode < 0 or "PINS_FAIL" in r.stdout, \
+        f"no pin noticed the planted mistake: {name}\n{r.stdout}\n{r.stderr[-2000:]}"
+
+
+def test_unmutated_oracle_passes_the_multi_pins():
+    assert _multi_pins_pass()
