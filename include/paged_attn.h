@@ -180,6 +180,42 @@ PAGED_ATTN_API int paged_attn_decode_fp8(const void* q, const void* k_cache, con
                                          void* stream);
 
 /*
+ * Multi-token decode: several new tokens per sequence query the cache at once
+ * (speculative decoding, chunked prefill), the ragged query batch of AstrAI's
+ * CUDA Kernels page ("Q Scheduling and KV Addressing": rows located through
+ * qo_indptr; "Python Wrappers": is_causal).  Sequence s owns the query rows
+ * qo_indptr[s] .. qo_indptr[s+1] - 1, its last q_len = qo_indptr[s+1] -
+ * qo_indptr[s] tokens, which are already in the cache (seq_lens[s] counts
+ * them).  Query i of sequence s attends the tokens t <= seq_lens[s] - q_len + i
+ * (causal: its own position and everything before):
+ *
+ *   out[qo[s] + i, h, :] = softmax_t(scale * q[qo[s] + i, h, :] . K_t) . V_t,
+ *                          t in [0, seq_lens[s] - q_len + i]
+ *
+ *   q, out      [total_q, H_q, head_dim]  bf16 (read / written)
+ *   qo_indptr   [num_seqs + 1]  int32, device, 16-byte aligned: qo_indptr[0] = 0,
+ *               non-decreasing, qo_indptr[num_seqs] = total_q
+ *   max_q_len   the largest q_len (host value); max_q_len * (H_q / H_kv) <= 256
+ *
+ * Caches, tables, lengths, head_dim, block_size and scale as paged_attn_decode
+ * (bf16 caches in the standard layout).  The q_len * G query rows of one KV
+ * head are processed together, in pieces of 16 rows when they are more than 8:
+ * every piece streams the KV head's pages once.  Rows whose query sees no token
+ * (q_len > seq_len) and the rows of empty sequences are zero.  Query rows a
+ * sequence does not own are not written.  Returns PAGED_ATTN_ERR_SIZES for
+ * total_q < 0, max_q_len < 1 or max_q_len * G > 256; errors otherwise as
+ * paged_attn_decode.  Uses the library-owned workspace.
+ */
+PAGED_ATTN_API int paged_attn_decode_multi(const void* q, const void* k_cache,
+                                           const void* v_cache, void* out,
+                                           const int32_t* qo_indptr,
+                                           const int32_t* block_tables,
+                                           const int32_t* seq_lens, int num_seqs, int total_q,
+                                           int max_q_len, int H_q, int H_kv, int head_dim,
+                                           int max_blocks_per_seq, int block_size, float scale,
+                                           void* stream);
+
+/*
  * The same operation over bf16 caches in the x-packed layout ("Paged Attention
  * Kernel Architecture for BI-V100", section 3, Paged K/V Gather: the key cache
  * split into 16-byte packs of x = 8 elements, the value cache head_dim-major):

@@ -25,6 +25,7 @@ __all__ = [
     "paged_kv_append",
     "paged_attn_decode_fp8",
     "paged_attn_decode_xpacked",
+    "paged_attn_decode_multi",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "EXPORTED_SYMBOLS",
@@ -44,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "paged_attn_append_decode",
     "paged_attn_decode_fp8",
     "paged_attn_decode_xpacked",
+    "paged_attn_decode_multi",
     "paged_attn_status_string",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
@@ -92,6 +94,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_decode_fp8.restype = I
         lib.paged_attn_decode_xpacked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.paged_attn_decode_xpacked.restype = I
+        lib.paged_attn_decode_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
+                                                P]
+        lib.paged_attn_decode_multi.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -232,6 +237,34 @@ def paged_attn_decode_xpacked(q, kx, vt, block_tables, seq_lens, scale: float, o
     _check(load().paged_attn_decode_xpacked(_ptr(q), _ptr(kx), _ptr(vt), _ptr(out),
                                             _ptr(block_tables), _ptr(seq_lens), num_seqs, H_q,
                                             H_kv, D, maxb, BS, float(scale), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_multi(q, k_cache, v_cache, qo_indptr, block_tables, seq_lens,
+                            scale: float, max_q_len: int, out=None, stream=None):
+    """Multi-token decode (see paged_attn.h): q [total_q, H_q, D], sequence s owning
+    rows qo_indptr[s] .. qo_indptr[s+1] - 1 (its last tokens, causal)."""
+    import torch
+
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("qo_indptr", qo_indptr), ("block_tables", block_tables),
+                    ("seq_lens", seq_lens)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    total_q, H_q, D = (int(x) for x in q.shape)
+    _, H_kv, BS, Dk = (int(x) for x in k_cache.shape)
+    if Dk != D:
+        raise ValueError("q and the caches disagree on head_dim")
+    num_seqs = int(seq_lens.shape[0])
+    if tuple(qo_indptr.shape) != (num_seqs + 1,) or qo_indptr.dtype != torch.int32:
+        raise ValueError("qo_indptr must be int32 [num_seqs + 1]")
+    if out is None:
+        out = torch.empty_like(q)
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(load().paged_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                          _ptr(qo_indptr), _ptr(block_tables), _ptr(seq_lens),
+                                          num_seqs, total_q, int(max_q_len), H_q, H_kv, D, maxb,
+                                          BS, float(scale), _stream(stream)))
     return out
 
 

@@ -101,6 +101,15 @@ struct DecodeParams {
   // FP8 caches: one dequant float per (block, KV head, slot) for K and for V
   const float* k_scale;        // [num_blocks, H_kv, BS]
   const float* v_scale;
+  // Multi-token decode (null qo_indptr: one query token per sequence).  Sequence
+  // s owns rows qo_indptr[s] .. qo_indptr[s+1] - 1 of q and out ([rows, H_q, D]):
+  // its last q_len tokens, query i seeing the tokens t <= seq_len - q_len + i.
+  // The q_len * G query rows of one KV head (token-major: row r is query r / G,
+  // head r % G of the group) are split into `chunks` pieces of `rows` rows.
+  const int32_t* qo_indptr;
+  int rows;
+  int chunks;
+  int total_q;  // rows of q and out (offsets outside [0, total_q) are never touched)
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -200,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const L lay{p.stages, p.G, p.num_seqs};
+  const bool multi = p.qo_indptr != nullptr;
+  const L lay{p.stages, multi ? p.rows : p.G, p.num_seqs, multi ? p.num_seqs + 1 : 0};
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
@@ -213,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   float* sm_scales = reinterpret_cast<float*>(smem + lay.scales());  // FP8: [stages][2][BS]
   int* sm_prefix = reinterpret_cast<int*>(smem + lay.prefix());
   int* sm_len = reinterpret_cast<int*>(smem + lay.lens());
+  int* sm_qo = reinterpret_cast<int*>(smem + lay.qo());  // multi: qo_indptr[0..N]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -220,6 +231,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   const int N = p.num_seqs;
   const int H_kv = p.H_kv;
   const int G = p.G;
+  const int R = multi ? p.rows : G;      // query rows of one piece
+  const int QC = multi ? p.chunks : 1;   // pieces per (sequence, KV head)
+  const int H_v = H_kv * QC;             // pieces per sequence, walked like KV heads
   const int cap = p.maxb * BS;
 
   // ---- 0. Programmatic dependent launch: let the next kernel in the stream be
@@ -278,17 +292,31 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       run += (sm_len[s] + BS - 1) / BS;
     }
     if (tid == kThreads - 1) sm_prefix[N] = base + incl;
+    if (multi) {
+      for (int s = tid; s <= N; s += kThreads) sm_qo[s] = __ldg(p.qo_indptr + s);
+    }
     __syncthreads();
+    if (multi && blockIdx.x == 0) {
+      // rows a sequence cannot hold (q_len < 0, or more than the pieces carry) are
+      // reported; they are never read or written
+      for (int s = tid; s < N; s += kThreads) {
+        const int ql = sm_qo[s + 1] - sm_qo[s];
+        if (ql < 0 || (long long)ql * G > (long long)R * QC) atomicOr(p.status, kStatusBadLength);
+      }
+    }
   }
 
   // ---- 2. empty sequences get zero rows (spread over CTAs)
   for (int s = blockIdx.x; s < N; s += gridDim.x) {
     if (sm_len[s] != 0) continue;
-    uint32_t* o32 = reinterpret_cast<uint32_t*>(p.out + (size_t)s * p.H_q * D);
-    for (int i = tid; i < p.H_q * D / 2; i += kThreads) o32[i] = 0u;
+    const int r0 = multi ? min(max(sm_qo[s], 0), p.total_q) : s;
+    const int nr = multi ? max(0, min(min(sm_qo[s + 1] - sm_qo[s], R * QC / G), p.total_q - r0))
+                         : 1;
+    uint32_t* o32 = reinterpret_cast<uint32_t*>(p.out + (size_t)r0 * p.H_q * D);
+    for (int i = tid; i < nr * p.H_q * D / 2; i += kThreads) o32[i] = 0u;
   }
 
-  const long long W = (long long)sm_prefix[N] * H_kv;
+  const long long W = (long long)sm_prefix[N] * H_v;
   if (W == 0) return;
   if (p.stages < kConsumerWarps) {  // the host plan never launches fewer
     if (tid == 0) atomicOr(p.status, kStatusConfig);
@@ -318,14 +346,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     // stages, so the lanes of one wave always wait on distinct slots.
     const int issue_lanes = min(kMaxIssueLanes, p.stages);
     Walker wk;
-    if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_kv);
+    if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_v);
     auto fetch = [&](long long u) -> int2 {
       // physical block and KV head of this lane's unit (block -1 past the range)
       if (u >= u1) return make_int2(-1, 0);
       int pb = __ldg(p.block_tables + (size_t)wk.s * p.maxb + wk.p);
       if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
         atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
-      return make_int2(pb, wk.g);
+      return make_int2(pb, wk.g / QC);  // the piece's KV head
     };
     int2 cur = fetch(u0 + lane);
     bool abort = false;
@@ -333,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
       if (ub + 32 + lane < u1) {
-        wk.advance(32, sm_prefix, N, H_kv);
+        wk.advance(32, sm_prefix, N, H_v);
         nxt = fetch(ub + 32 + lane);
       }
       const int cnt = (int)min(32LL, u1 - ub);
@@ -415,18 +443,37 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   // With the fused cache append the slot also receives the piece's new K and V
   // rows and the block id of its last page, so the warp that patches that page
   // finds them in shared memory.
+  // Row of q / out ([rows, H_q, D] viewed as rows of D) that row r of piece
+  // (s, gv) stands for, or -1 for a padding row (never stored).  gv is the
+  // piece's index among its sequence's H_kv * QC pieces.
+  auto qrow = [&](int s, int gv, int r) -> long long {
+    if (!multi) return r < G ? (long long)s * p.H_q + (long long)gv * G + r : -1;
+    const int g = gv / QC;
+    const int rr = (gv - g * QC) * R + r;  // row within the KV head's q_len * G rows
+    const int i = rr / G;
+    const long long t = (long long)sm_qo[s] + i;  // the query's row of q / out
+    if (r >= R || i >= sm_qo[s + 1] - sm_qo[s] || t < 0 || t >= p.total_q) return -1;
+    return t * p.H_q + (long long)g * G + (rr - i * G);
+  };
+  // Last token row r of piece (s, gv) attends (causal in multi-token decode).
+  auto row_limit = [&](int s, int gv, int r) -> int {
+    if (!multi) return 0x7fffffff;
+    const int g = gv / QC;
+    const int i = ((gv - g * QC) * R + r) / G;
+    const int ql = sm_qo[s + 1] - sm_qo[s];
+    return i < ql ? sm_len[s] - ql + i : 0x7fffffff;  // padding rows: anything
+  };
   auto prefetch_q = [&](int buf, int s, int g) {
-    const __nv_bfloat16* qg = p.q + ((size_t)s * p.H_q + (size_t)g * G) * D;
     uint8_t* tile = sm_q + buf * kQSlotBytes;
     for (int i = ctid; i < kQRows * (D / 8); i += kConsumerThreads) {
       const int h = i / (D / 8);
       const int c = i - h * (D / 8);
       const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
-      const bool live = h < G;
+      const long long qr = qrow(s, g, h);
       cp_async_16(tile + h * (D * 2) + pc * 16,
-                  live ? static_cast<const void*>(qg + (size_t)h * D + c * 8)
-                       : static_cast<const void*>(p.q),
-                  live ? 16 : 0);
+                  qr >= 0 ? static_cast<const void*>(p.q + qr * D + c * 8)
+                          : static_cast<const void*>(p.q),
+                  qr >= 0 ? 16 : 0);
     }
     if (!FP8 && p.k_new != nullptr) {
       const size_t row = ((size_t)s * H_kv + g) * D;
@@ -460,6 +507,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           pack_f16x2(bf16lo_to_f32(v), bf16hi_to_f32(v));
     }
   };
+  int lim[kNH][2];  // last token each of this lane's query columns may see
+  auto set_limits = [&](int s, int gv) {
+#pragma unroll
+    for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) lim[nh][e] = row_limit(s, gv, 8 * nh + 2 * quad + e);
+  };
   auto reset = [&]() {
 #pragma unroll
     for (int dt = 0; dt < kDT; ++dt)
@@ -477,8 +531,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   };
 
   // One page: S^T = K Q^T, online softmax, O^T += V^T P^T.
+  // `tb`: the page's first token; `lim`: the last token each of the lane's
+  // query columns may see (causal multi-token decode; the maximum int otherwise).
   auto process_page = [&](const uint8_t* kt, const uint8_t* vt, const uint8_t* qtile,
-                          int valid) {
+                          int valid, int tb, const int (&lim)[kNH][2]) {
     const uint32_t kbase = smem_addr(kt);
     const uint32_t vbase = smem_addr(vt);
     const uint32_t qbase = smem_addr(qtile);
@@ -544,10 +600,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 16 * tg + row + ((e >> 1) << 3);
-          const float x = tok < valid ? s_acc[tg][nh][e] * p.scale_log2 : -INFINITY;
+          const float x = tok < valid && tb + tok <= lim[nh][e & 1]
+                              ? s_acc[tg][nh][e] * p.scale_log2
+                              : -INFINITY;
           s_acc[tg][nh][e] = x;
           mx[nh][e & 1] = fmaxf(mx[nh][e & 1], x);
         }
+    float m_sub[kNH][2];
     float alpha[kNH][2];
     bool changed = false;
 #pragma unroll
@@ -559,7 +618,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
         const float m_new = fmaxf(m_run[nh][e], v);
-        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_new);
+        // a column that has seen no token yet (all masked) keeps -inf; subtract 0
+        // then, so its weights are exp2(-inf) = 0 instead of NaN
+        m_sub[nh][e] = m_new == -INFINITY ? 0.f : m_new;
+        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_sub[nh][e]);
         changed |= m_new != m_run[nh][e];
         m_run[nh][e] = m_new;
       }
@@ -571,10 +633,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     for (int tg = 0; tg < kTG; ++tg)
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh) {
-        const float e0 = fast_exp2(s_acc[tg][nh][0] - m_run[nh][0]);
-        const float e1 = fast_exp2(s_acc[tg][nh][1] - m_run[nh][1]);
-        const float e2 = fast_exp2(s_acc[tg][nh][2] - m_run[nh][0]);
-        const float e3 = fast_exp2(s_acc[tg][nh][3] - m_run[nh][1]);
+        const float e0 = fast_exp2(s_acc[tg][nh][0] - m_sub[nh][0]);
+        const float e1 = fast_exp2(s_acc[tg][nh][1] - m_sub[nh][1]);
+        const float e2 = fast_exp2(s_acc[tg][nh][2] - m_sub[nh][0]);
+        const float e3 = fast_exp2(s_acc[tg][nh][3] - m_sub[nh][1]);
         const uint32_t lo = pack_bf16x2(e0, e1);  // tokens row,   heads 2q, 2q+1
         const uint32_t hi = pack_bf16x2(e2, e3);  // tokens row+8, heads 2q, 2q+1
         psum[nh][0] += bf16lo_to_f32(lo) + bf16lo_to_f32(hi);
@@ -830,19 +892,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
                   float (&l_acc)[kSlots]) {
 #pragma unroll
     for (int k = 0; k < kSlots; ++k) {
-      const int v = ctid + k * kConsumerThreads;  // float4 index within [G][D/4]
-      if (v >= G * (D / 4)) continue;
+      const int v = ctid + k * kConsumerThreads;  // float4 index within [R][D/4]
+      if (v >= R * (D / 4)) continue;
       const int r = v / (D / 4), d4 = v - r * (D / 4);
       float m_new = m_acc[k];
 #pragma unroll 4
-      for (int j = 0; j < nc; ++j) m_new = fmaxf(m_new, parts[(j * G + r) * kPartialRow]);
+      for (int j = 0; j < nc; ++j) m_new = fmaxf(m_new, parts[(j * R + r) * kPartialRow]);
       if (m_new == -INFINITY) continue;
       const float sc = m_acc[k] == -INFINITY ? 0.f : fast_exp2(m_acc[k] - m_new);
       float4 a = make_float4(acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc);
       float l = l_acc[k] * sc;
 #pragma unroll 4
       for (int j = 0; j < nc; ++j) {
-        const float* prow = parts + (j * G + r) * kPartialRow;
+        const float* prow = parts + (j * R + r) * kPartialRow;
         const float2 ml = *reinterpret_cast<const float2*>(prow);
         const float4 o4 = *reinterpret_cast<const float4*>(prow + 4 + 4 * d4);
         const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - m_new);
@@ -861,14 +923,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
     for (int k = 0; k < kSlots; ++k) {
       const int v = ctid + k * kConsumerThreads;
-      if (v >= G * (D / 4)) continue;
+      if (v >= R * (D / 4)) continue;
       const int r = v / (D / 4), d4 = v - r * (D / 4);
-      const float inv = 1.f / l_acc[k];
+      const long long qr = qrow(x.s, x.g, r);
+      if (qr < 0) continue;
+      const float inv = l_acc[k] > 0.f ? 1.f / l_acc[k] : 0.f;  // a row that saw no token: 0
       uint2 packed;
       packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
       packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
-      *reinterpret_cast<uint2*>(p.out + ((size_t)x.s * p.H_q + (size_t)x.g * G + r) * D +
-                                4 * d4) = packed;
+      *reinterpret_cast<uint2*>(p.out + qr * D + 4 * d4) = packed;
     }
   };
   uint32_t comb_phase = 0;
@@ -876,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   // part number local_t (this CTA's) is not read back from the workspace: its
   // merged state already sits in the ring at that place of the first round.
   auto combine = [&](const Split& x0, const Split& x1, int njobs, int local_t) {
-    const int part_bytes = G * kPartialRow * 4;
+    const int part_bytes = R * kPartialRow * 4;
     const int per_round = (p.stages * kStageBytes) / part_bytes;  // >= 3 for ring >= 4 stages
     if (per_round < 1) {
       if (ctid == 0) atomicOr(p.status, kStatusConfig);
@@ -906,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           const Split& x = t < n0 ? x0 : x1;
           const int c = x.c_first + (t < n0 ? t : t - n0);
           const int slot = c == x.c_first ? x.slot_first : 2 * c;
-          bulk_load(smem + (t - t0) * part_bytes, p.partials + (size_t)slot * G * kPartialRow,
+          bulk_load(smem + (t - t0) * part_bytes, p.partials + (size_t)slot * R * kPartialRow,
                     (uint32_t)part_bytes, comb_bar);
         }
       }
@@ -994,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         for (int e = 0; e < 4; ++e) {
           const int h = 8 * nh + 2 * quad + (e & 1);
           const int d = acc_col(dt, e);
-          if (h < G) sm_o[(warp * G + h) * kRowStride + d] = o_acc[dt][nh][e] * f[nh][e & 1];
+          if (h < R) sm_o[(warp * R + h) * kRowStride + d] = o_acc[dt][nh][e] * f[nh][e & 1];
         }
     __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
@@ -1004,25 +1067,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   // bf16 rows of (s, g) (whole piece), or a partial row set [M, L, -, -, o]
   // at `dst` (a workspace slot, or part 0 of the ring).
   auto emit = [&](int s, int g, float* dst) {
-    for (int i = ctid; i < G * (D / 4); i += kConsumerThreads) {
+    for (int i = ctid; i < R * (D / 4); i += kConsumerThreads) {
       const int r = i / (D / 4);
       const int d = 4 * (i - r * (D / 4));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * G + r) * kRowStride + d);
+        const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * R + r) * kRowStride + d);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
         acc.w += v.w;
       }
       if (dst == nullptr) {
-        const float inv = 1.f / sm_final[16 + r];
+        const long long qr = qrow(s, g, r);
+        if (qr < 0) continue;
+        const float lsum = sm_final[16 + r];
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // a row that saw no token: 0
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(p.out + ((size_t)s * p.H_q + (size_t)g * G + r) * D + d) =
-            packed;
+        *reinterpret_cast<uint2*>(p.out + qr * D + d) = packed;
       } else {
         float* prow = dst + r * kPartialRow;
         *reinterpret_cast<float4*>(prow + 4 + d) = acc;
@@ -1049,30 +1114,30 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   };
   auto next_piece = [&](Piece pc) -> Piece {
     const int n = sm_prefix[pc.s + 1] - sm_prefix[pc.s];
-    if (++pc.g == H_kv) {
+    if (++pc.g == H_v) {
       pc.g = 0;
       do {
         ++pc.s;
       } while (pc.s < N && sm_prefix[pc.s + 1] == sm_prefix[pc.s]);
     }
-    pc.sb = pc.s < N ? (long long)sm_prefix[pc.s] * H_kv +
+    pc.sb = pc.s < N ? (long long)sm_prefix[pc.s] * H_v +
                            (long long)pc.g * (sm_prefix[pc.s + 1] - sm_prefix[pc.s])
                      : pc.sb + n;
     return pc;
   };
 
   Walker wk;
-  wk.start(u0, sm_prefix, N, H_kv);
+  wk.start(u0, sm_prefix, N, H_v);
   // The range's first and last pieces (the only ones that can be split) and
   // their split descriptors, worked out now by thread 0 (off the critical path
   // at the end) and kept in shared memory, not in registers, through the loop.
   Split* const sm_split = reinterpret_cast<Split*>(sm_flag + 4);  // [0] first, [1] last
   int* const sm_split_flags = sm_flag + 4 + 2 * (int)(sizeof(Split) / sizeof(int));
   if (ctid == 0) {
-    const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
+    const long long first_sb = (long long)sm_prefix[wk.s] * H_v + (long long)wk.g * wk.n;
     Walker wl;
-    wl.start(u1 - 1, sm_prefix, N, H_kv);
-    const long long last_sb = (long long)sm_prefix[wl.s] * H_kv + (long long)wl.g * wl.n;
+    wl.start(u1 - 1, sm_prefix, N, H_v);
+    const long long last_sb = (long long)sm_prefix[wl.s] * H_v + (long long)wl.g * wl.n;
     sm_split[0] = make_split(wk.s, wk.g, first_sb, first_sb + wk.n);
     sm_split[1] = make_split(wl.s, wl.g, last_sb, last_sb + wl.n);
     sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
@@ -1092,6 +1157,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     named_barrier(kConsumerBarrier, kConsumerThreads);
   }
   reset();
+  set_limits(wk.s, wk.g);
   int stage = 0;
   uint32_t phase = 0;
   // FP8 with 16-token pages and a ring depth that is a multiple of 4 (so a
@@ -1173,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // into the page in shared memory once the page has landed (the tensor
       // copy brought whatever the cache held) and stored to the cache for later
       // calls.  This page is read by this CTA alone.
-      const bool patch = !XP && p.k_new != nullptr && wk.p == wk.n - 1;
+      const bool patch = !XP && !multi && p.k_new != nullptr && wk.p == wk.n - 1;
       // Lanes poll the barrier independently; the vote both reconverges the warp
       // before the warp-collective ldmatrix / movmatrix / mma and makes the
       // outcome uniform.
@@ -1196,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
           }
           __syncwarp();
         }
-        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid);
+        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid, wk.p * BS, lim);
         if (patch) {
           // the patch's generic writes precede the next tensor copy into this slot
           fence_proxy_async_shared();
@@ -1220,9 +1286,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     }
     const int s = wk.s, g = wk.g, n = wk.n;
     const bool last = u + 1 == u1;
-    wk.next(sm_prefix, N, H_kv);
+    wk.next(sm_prefix, N, H_v);
     if (!last && wk.g == g && wk.s == s) continue;
-    const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
+    const long long sb = (long long)sm_prefix[s] * H_v + (long long)g * n;
     if (!last) {
       // A split piece that is not the range's last is its first: store its
       // partial, then arrive and publish at once with a release add (the
@@ -1230,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       // is only read at the end of the range.
       const bool split = sb < u0;
       merge_warps(nullptr, nullptr);
-      emit(s, g, split ? p.partials + (size_t)my_slot(sb) * G * kPartialRow : nullptr);
+      emit(s, g, split ? p.partials + (size_t)my_slot(sb) * R * kPartialRow : nullptr);
       // The next piece's query group was prefetched into the other tile: make
       // every thread's copies visible, then prefetch the piece after it into
       // the tile just freed.
@@ -1248,6 +1314,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         named_barrier(kConsumerBarrier, kConsumerThreads);
       }
       reset();
+      set_limits(wk.s, wk.g);
       continue;
     }
     // ---- the range's last piece.  When it is split, thread 0 arrives as soon
@@ -1273,10 +1340,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     // this CTA's part of the last piece: its place among the split's parts, and
     // whether the combine can take it from the ring instead of the workspace
     const int local_t = (int)blockIdx.x - xl.c_first;
-    const int part_bytes = G * kPartialRow * 4;
+    const int part_bytes = R * kPartialRow * 4;
     const bool local = cl && local_t < (p.stages * kStageBytes) / part_bytes;
     if (last_split && !local) {
-      emit(s, g, p.partials + (size_t)my_slot(sb) * G * kPartialRow);
+      emit(s, g, p.partials + (size_t)my_slot(sb) * R * kPartialRow);
       __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
       if (ctid == 0) {

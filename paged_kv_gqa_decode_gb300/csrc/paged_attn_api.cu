@@ -20,7 +20,8 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr size_t kWsAlign = 256;
-constexpr int kAppendApartPieces = 4;  // (s, g) pieces per CTA from which the append runs apart
+constexpr int kAppendApartPieces = 4;
+constexpr int kMaxMultiRows = 256;  // multi-token decode: max q_len * G (16 pieces of 16 rows)  // (s, g) pieces per CTA from which the append runs apart
 constexpr long long kRingBytesPerSm = 128 << 10;            // K/V rings of one SM, few pieces per CTA
 constexpr long long kRingBytesPerSmManyPieces = 160 << 10;  // ... two or more pieces per CTA
 
@@ -100,6 +101,8 @@ struct Plan {
   bool g16;
   bool fp8;     // FP8 caches
   bool xp;      // x-packed K / D-major V caches (bf16)
+  int rows;     // query rows of one piece: G, or a multi-token chunk (8 or 16)
+  int qchunks;  // multi-token decode: pieces per (sequence, KV head); 0: single token
   int chunk;    // sequences per launch
   int stages;   // pipeline depth
   size_t smem;  // dynamic shared memory per CTA
@@ -107,10 +110,13 @@ struct Plan {
   size_t off_counters, off_partials, ws_bytes;
 };
 
+// G: query rows of one piece; qo: multi-token decode (room for chunk + 1 row offsets).
 template <int D, int BS, bool FP8>
-bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int* stages, size_t* smem) {
+bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, bool qo, int* stages,
+               size_t* smem) {
   using L = SmemLayout<D, BS, FP8>;
-  const L none{0, G, chunk};
+  const int qo_entries = qo ? chunk + 1 : 0;
+  const L none{0, G, chunk, qo_entries};
   const long long fixed = none.total() + 2048;  // + alignment slack and static shared memory
   const long long per_stage = L::kStageBytes + L::kScaleBytes + 16;
   long long st = (max_smem - fixed) / per_stage;
@@ -118,42 +124,46 @@ bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int* stages, 
   if (st > ring_cap / L::kStageBytes) st = ring_cap / L::kStageBytes;
   // At least one slot per consumer warp (slot s belongs to warp s % 4).
   if (st < kConsumerWarps) return false;
-  const L lay{(int)st, G, chunk};
+  const L lay{(int)st, G, chunk, qo_entries};
   *stages = (int)st;
   *smem = (size_t)lay.total() + 1024;
   return *smem + 256 <= (size_t)max_smem;  // + the kernel's static shared memory
 }
 
 template <bool FP8>
-bool plan_smem_d(int D, int BS, int G, int chunk, int max_smem, long long ring_cap, int* stages,
-                 size_t* smem) {
+bool plan_smem_d(int D, int BS, int G, int chunk, int max_smem, long long ring_cap, bool qo,
+                 int* stages, size_t* smem) {
   if (D == 64) {
     if constexpr (FP8) return false;  // FP8 caches need head_dim 128 or 256
     else
-      return BS == 16 ? plan_smem<64, 16, false>(G, chunk, max_smem, ring_cap, stages, smem)
-                      : plan_smem<64, 32, false>(G, chunk, max_smem, ring_cap, stages, smem);
+      return BS == 16 ? plan_smem<64, 16, false>(G, chunk, max_smem, ring_cap, qo, stages, smem)
+                      : plan_smem<64, 32, false>(G, chunk, max_smem, ring_cap, qo, stages, smem);
   }
   if (D == 128)
-    return BS == 16 ? plan_smem<128, 16, FP8>(G, chunk, max_smem, ring_cap, stages, smem)
-                    : plan_smem<128, 32, FP8>(G, chunk, max_smem, ring_cap, stages, smem);
-  return BS == 16 ? plan_smem<256, 16, FP8>(G, chunk, max_smem, ring_cap, stages, smem)
-                  : plan_smem<256, 32, FP8>(G, chunk, max_smem, ring_cap, stages, smem);
+    return BS == 16 ? plan_smem<128, 16, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem)
+                    : plan_smem<128, 32, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem);
+  return BS == 16 ? plan_smem<256, 16, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem)
+                  : plan_smem<256, 32, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem);
 }
 
 bool plan_smem_any(int D, int BS, bool fp8, int G, int chunk, int max_smem, long long ring_cap,
-                   int* stages, size_t* smem) {
-  return fp8 ? plan_smem_d<true>(D, BS, G, chunk, max_smem, ring_cap, stages, smem)
-             : plan_smem_d<false>(D, BS, G, chunk, max_smem, ring_cap, stages, smem);
+                   bool qo, int* stages, size_t* smem) {
+  return fp8 ? plan_smem_d<true>(D, BS, G, chunk, max_smem, ring_cap, qo, stages, smem)
+             : plan_smem_d<false>(D, BS, G, chunk, max_smem, ring_cap, qo, stages, smem);
 }
 
+// rows > 0: multi-token decode with `rows` query rows per piece and `qchunks`
+// pieces per (sequence, KV head).
 int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& di, Plan* pl,
-              bool fp8 = false) {
+              bool fp8 = false, int rows = 0, int qchunks = 0) {
   pl->D = D;
   pl->fp8 = fp8;
   pl->xp = false;
   pl->BS = BS;
   pl->G = H_q / H_kv;
-  pl->g16 = pl->G > 8;
+  pl->rows = rows > 0 ? rows : pl->G;
+  pl->qchunks = rows > 0 ? qchunks : 0;
+  pl->g16 = pl->rows > 8;
   const int chunk0 =
       num_seqs < kMaxSeqsPerLaunch ? (num_seqs > 0 ? num_seqs : 1) : kMaxSeqsPerLaunch;
   // Two CTAs per SM (two independent pipelines) when their shared memory fits,
@@ -171,10 +181,11 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
       // CTAs per SM: 8 stages 51.4 us, 10 52.2, 12 53.3); CTAs that cross many
       // (s, g) pieces gain from a deeper ring that absorbs the stall at each
       // piece end (ragged 256-sequence batch: 8 stages 617 us, 10 608).
-      const long long pieces = (long long)chunk * H_kv;
+      const long long pieces = (long long)chunk * H_kv * (pl->qchunks > 0 ? pl->qchunks : 1);
       const long long ring_cap =
           (pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces : kRingBytesPerSm) / occ;
-      if (plan_smem_any(D, BS, fp8, pl->G, chunk, budget, ring_cap, &pl->stages, &pl->smem) &&
+      if (plan_smem_any(D, BS, fp8, pl->rows, chunk, budget, ring_cap, pl->qchunks > 0,
+                        &pl->stages, &pl->smem) &&
           (pl->stages >= 4 || chunk <= 64)) {
         ok = true;
         pl->grid = di.sms * occ;
@@ -186,13 +197,15 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
   }
   if (!ok) return PAGED_ATTN_ERR_SIZES;
   pl->chunk = chunk;
-  // [0, 256): status word; then one combine counter per CTA; then the partial
-  // states.  The counter region depends on the device only, so a workspace
-  // reused by calls of any size always finds it zero.
+  // [0, 256): status word; then one combine counter per CTA of the largest grid
+  // any launch on this device uses (two CTAs per SM); then the partial states.
+  // The counter region depends on the device only (not on this launch's grid,
+  // which is one CTA per SM for some shapes), so a workspace reused by calls of
+  // any size always finds it zero: partials never land on it.
   pl->off_counters = kWsAlign;
-  pl->off_partials = pl->off_counters + round_up((size_t)pl->grid * 4, kWsAlign);
+  pl->off_partials = pl->off_counters + round_up((size_t)di.sms * 2 * 4, kWsAlign);
   pl->ws_bytes = pl->off_partials +
-                 round_up((size_t)pl->grid * 2 * pl->G * (size_t)(D + 4) * 4, kWsAlign);
+                 round_up((size_t)pl->grid * 2 * pl->rows * (size_t)(D + 4) * 4, kWsAlign);
   return PAGED_ATTN_OK;
 }
 
@@ -315,7 +328,8 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
         int max_blocks_per_seq, float scale, void* ws, int32_t* status, long long num_blocks,
         cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
-        const float* k_scale = nullptr, const float* v_scale = nullptr) {
+        const float* k_scale = nullptr, const float* v_scale = nullptr,
+        const int32_t* qo_indptr = nullptr, int total_q = 0) {
   CUtensorMap tk, tv;
   int rc;
   if (pl.xp) {
@@ -331,8 +345,14 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
   for (int s0 = 0; s0 < num_seqs; s0 += pl.chunk) {
     const int n = num_seqs - s0 < pl.chunk ? num_seqs - s0 : pl.chunk;
     DecodeParams p;
-    p.q = static_cast<const __nv_bfloat16*>(q) + (size_t)s0 * H_q * pl.D;
-    p.out = static_cast<__nv_bfloat16*>(out) + (size_t)s0 * H_q * pl.D;
+    // multi-token decode: q and out rows are found through qo_indptr (absolute)
+    const size_t row0 = qo_indptr ? 0 : (size_t)s0;
+    p.q = static_cast<const __nv_bfloat16*>(q) + row0 * H_q * pl.D;
+    p.out = static_cast<__nv_bfloat16*>(out) + row0 * H_q * pl.D;
+    p.qo_indptr = qo_indptr ? qo_indptr + s0 : nullptr;
+    p.rows = pl.rows;
+    p.chunks = pl.qchunks > 0 ? pl.qchunks : 1;
+    p.total_q = total_q;
     p.block_tables = bt + (size_t)s0 * max_blocks_per_seq;
     p.seq_lens = seq_lens + s0;
     p.num_seqs = n;
@@ -448,6 +468,39 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
   if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
   return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
              max_blocks_per_seq, scale, ws, nullptr, 0, st);
+}
+
+int paged_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache, void* out,
+                            const int32_t* qo_indptr, const int32_t* block_tables,
+                            const int32_t* seq_lens, int num_seqs, int total_q, int max_q_len,
+                            int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                            int block_size, float scale, void* stream) {
+  int rc = validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return PAGED_ATTN_ERR_SCALE;
+  const int G = H_q / H_kv;
+  if (total_q < 0 || max_q_len < 1 || (long long)max_q_len * G > kMaxMultiRows ||
+      (long long)total_q * H_q * head_dim >= (1LL << 40))
+    return PAGED_ATTN_ERR_SIZES;
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  rc = check_pointers(q, k_cache, v_cache, out, block_tables, seq_lens);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (!aligned16(qo_indptr)) return PAGED_ATTN_ERR_POINTER;
+  DeviceInfo di;
+  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  // one n8 MMA tile of rows when a KV head's q_len * G rows fit, else pieces of 16
+  const int rows = max_q_len * G <= 8 ? 8 : 16;
+  const int qchunks = (max_q_len * G + rows - 1) / rows;
+  Plan pl;
+  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl, false, rows,
+                      qchunks)) != PAGED_ATTN_OK)
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+             max_blocks_per_seq, scale, ws, nullptr, 0, st, nullptr, nullptr, nullptr, nullptr,
+             qo_indptr, total_q);
 }
 
 int paged_attn_decode_xpacked(const void* q, const void* k_cache, const void* v_cache, void* out,

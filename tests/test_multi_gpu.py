@@ -1,0 +1,124 @@
+"""GPU parity of multi-token decode (a ragged batch of new tokens per sequence,
+causal over the cache) against the oracle's float64 definition, on LLaMA- and
+Qwen-shaped caches, a sweep of head dims, block sizes, group sizes and query
+lengths (pieces of 8 and 16 rows, several pieces per KV head), and bit for bit
+against the single-token decode when every sequence has one query."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import paged_kv_gqa_decode_gb300 as pa
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_decode_gb300 import build
+
+    build.build()
+    pa.load()
+
+
+def queries(w, qlens, seed):
+    """Seeded bf16 query rows [sum(qlens), H_q, D] and qo_indptr (int32, device)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    qo = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
+    q = torch.randn(int(qo[-1]), w.spec.H_q, w.spec.D, generator=g).to(torch.bfloat16)
+    return q.cuda(), qo.cuda()
+
+
+def run_multi(w, q, qo, max_q_len):
+    out = pa.paged_attn_decode_multi(q, w.k_cache, w.v_cache, qo, w.block_tables, w.seq_lens,
+                                     w.scale, max_q_len)
+    torch.cuda.synchronize()
+    return out
+
+
+def reference(w, q, qo):
+    x = oracle.MultiInputs(q.cpu(), w.k_cache.cpu(), w.v_cache.cpu(), w.block_tables.cpu(),
+                           w.seq_lens.cpu(), w.scale)
+    return oracle.decode_multi(x, qo.cpu())
+
+
+def assert_parity(out, ref, what=""):
+    got = out.float().cpu().double().numpy().reshape(ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, \
+        f"{what}: max {err.max():.3e} mean {err.mean():.3e}"
+
+
+@pytest.mark.parametrize("name,qlen", [("llama8b", 4), ("llama8b", 2), ("qwen100k", 3),
+                                       ("gqa8", 2), ("tiny", 5)])
+def test_published_workloads_multi(name, qlen):
+    w = workloads.make(name, device="cuda", poison="nan")
+    qlens = [min(qlen, L) for L in w.lens_list]
+    q, qo = queries(w, qlens, 7)
+    assert_parity(run_multi(w, q, qo, qlen), reference(w, q, qo), f"{name} q_len {qlen}")
+
+
+def test_one_query_per_sequence_equals_the_decode():
+    w = workloads.make("ragged256", device="cuda", poison="nan")
+    qlens = [1 if L > 0 else 0 for L in w.lens_list]
+    q, qo = queries(w, qlens, 8)
+    out = run_multi(w, q, qo, 1)
+    # the decode of the same query rows (one per sequence with a token)
+    full = torch.zeros_like(w.q)
+    idx = torch.tensor([s for s, L in enumerate(w.lens_list) if L > 0], device="cuda")
+    full[idx] = q
+    dec = pa.paged_attn_decode(full, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), dec[idx].view(torch.int16))
+
+
+LENS = [1, 15, 16, 17, 31, 33, 100, 257, 1000, 0, 64]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("H_q,H_kv,qmax", [(4, 4, 3), (8, 2, 2), (8, 2, 6), (16, 2, 5),
+                                           (16, 1, 1), (6, 1, 7)])
+def test_multi_shapes_and_query_lengths(D, BS, H_q, H_kv, qmax):
+    sp = workloads.custom_spec("msweep", len(LENS), H_q, H_kv, D, BS, LENS, max_len=1024)
+    w = workloads.make(sp, seed=D + BS + H_q + qmax, device="cuda", poison="nan")
+    rng = np.random.default_rng(D * BS + qmax)
+    qlens = [int(min(L, rng.integers(0, qmax + 1))) for L in LENS]
+    qlens[0] = min(LENS[0], qmax)
+    q, qo = queries(w, qlens, D + qmax)
+    assert_parity(run_multi(w, q, qo, qmax), reference(w, q, qo),
+                  f"D{D} BS{BS} G{H_q // H_kv} qmax{qmax}")
+
+
+def test_multi_long_sequence_split_over_all_ctas():
+    sp = workloads.custom_spec("one", 2, 8, 1, 128, 16, [60000, 3000])
+    w = workloads.make(sp, seed=3, device="cuda")
+    q, qo = queries(w, [4, 4], 9)
+    assert_parity(run_multi(w, q, qo, 4), reference(w, q, qo))
+
+
+def test_multi_repeat_calls_are_bitwise_identical():
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    q, qo = queries(w, [3] * w.spec.num_seqs, 10)
+    a = run_multi(w, q, qo, 3).clone()
+    b = run_multi(w, q, qo, 3)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_multi_rejects_bad_arguments():
+    w = workloads.make("tiny", device="cuda")
+    q, qo = queries(w, [2, 2], 11)
+    lib = pa.load()
+    args = [q.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(), q.data_ptr(),
+            qo.data_ptr(), w.block_tables.data_ptr(), w.seq_lens.data_ptr(), 2, 4]
+    tail = [w.spec.H_q, w.spec.H_kv, w.spec.D, int(w.block_tables.shape[1]),
+            w.spec.block_size, 0.125, 0]
+    assert lib.paged_attn_decode_multi(*args, 0, *tail) == -5          # max_q_len < 1
+    assert lib.paged_attn_decode_multi(*args, 200, *tail) == -5        # q_len * G > 256
+    assert lib.paged_attn_decode_multi(*(args[:4] + [0] + args[5:]), 2, *tail) == -1

@@ -261,3 +261,18 @@ def test_one_workspace_serves_calls_of_different_sizes():
                 refs[n] = reference(w)
             assert_parity(out, refs[n], f"{n} round {rnd}")
     del ws_list
+
+
+def test_workspace_reuse_across_grids_of_one_and_two_ctas_per_sm():
+    """head_dim 256 with G = 16 runs one CTA per SM, the others two: partial states
+    written by the smaller grid must never land where the larger grid's combine
+    counters live (a stale counter corrupts the next call's merge)."""
+    wide = workloads.custom_spec("g16d256", 4, 32, 2, 256, 16, [20000, 15000, 9000, 30000])
+    specs = [wide, "llama8b", wide, "gqa8"]
+    ws_list = [workloads.make(sp, device="cuda", poison="nan") for sp in specs]
+    refs = [reference(w) for w in ws_list]
+    for rnd in range(2):
+        for i, w in enumerate(ws_list):
+            out = run_gpu(w)
+            assert_parity(out, refs[i], f"call {i} round {rnd}")
+    del ws_list

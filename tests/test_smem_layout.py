@@ -19,6 +19,7 @@ CSRC = os.path.join(ROOT, "paged_kv_gqa_decode_gb300", "csrc")
 
 PROGRAM = r"""
 #include <cstdio>
+#include <initializer_list>
 #include "smem_layout.h"
 using namespace pagedattn;
 
@@ -31,8 +32,9 @@ void run() {
   const int ns[] = {1, 2, 3, 5, 7, 31, 32, 33, 255, 256, 257, 1000, 4095, 4096};
   for (int st = 4; st <= 16; ++st)
     for (int G = 1; G <= 16; ++G)
-      for (int n : ns) {
-        const L l{st, G, n};
+      for (int n : ns)
+      for (int qo : {0, n + 1}) {
+        const L l{st, G, n, qo};
         CHECK(l.bars() % 1024 == 0, "bars D%d BS%d st%d\n", D, BS, st);
         CHECK(L::kStageBytes % 1024 == 0, "stage size D%d BS%d\n", D, BS);
         CHECK(l.merge_m() >= l.bars() + (2 * st + 1) * 8, "barrier overlap\n");
@@ -57,7 +59,9 @@ void run() {
         CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
         CHECK(l.lens() - l.prefix() >= (n + 1) * 4, "prefix size\n");
-        CHECK(l.total() - l.lens() >= n * 4, "lens size\n");
+        CHECK(l.qo() - l.lens() >= n * 4, "lens size\n");
+        CHECK(l.qo() % 16 == 0, "qo alignment\n");
+        CHECK(l.total() - l.qo() >= qo * 4, "qo size\n");
       }
 }
 
