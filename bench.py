@@ -288,9 +288,27 @@ def run_ours(args, world, rank, local):
         nbytes["append"] = rows * spec.D * 2 * 2 * 2  # K and V rows, read once, written once
         nbytes["total"] += nbytes["append"]
 
+    # --qlen > 1: multi-token decode, the last qlen tokens of every sequence query
+    # the cache (causal); q and out grow to qlen rows per sequence
+    qlen = args.qlen
+    q_in = w.q
+    qo = None
+    if qlen > 1:
+        gq = torch.Generator(device="cpu").manual_seed(seed + 29)
+        q_in = torch.randn(spec.num_seqs * qlen, spec.H_q, spec.D, generator=gq).to(
+            torch.bfloat16).to(dev)
+        qo = torch.arange(0, spec.num_seqs * qlen + 1, qlen, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q_in)
+        nbytes = dict(nbytes)
+        nbytes["q_out"] = spec.num_seqs * qlen * spec.H_q * spec.D * 2 * 2
+        nbytes["total"] = nbytes["kv"] + nbytes["q_out"] + nbytes["block_table"]
+
     def run_op(q, bt, sl, cache, kn, vn):
         kc, vc, ksc, vsc = cache
-        if fp8:
+        if qo is not None:
+            pa.paged_attn_decode_multi(q, kc, vc, qo, bt, sl, w.scale, qlen, out=out,
+                                       stream=stream)
+        elif fp8:
             pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
                                      stream=stream)
         elif args.kv == "xpacked":
@@ -305,7 +323,7 @@ def run_ours(args, world, rank, local):
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=stream)
 
     def step(i):
-        run_op(w.q, w.block_tables, w.seq_lens, caches[i % reps], k_new, v_new)
+        run_op(q_in, w.block_tables, w.seq_lens, caches[i % reps], k_new, v_new)
 
     for i in range(args.warmup):
         step(i)
@@ -359,11 +377,11 @@ def run_ours(args, world, rank, local):
     launches_per_step = -(-len(lens) // 4096) + (1 if op == "append_then_decode" else 0)
 
     # end to end through the public API: pinned host inputs in, result back to host
-    host_q = w.q.cpu().pin_memory()
+    host_q = q_in.cpu().pin_memory()
     host_bt = w.block_tables.cpu().pin_memory()
     host_sl = w.seq_lens.cpu().pin_memory()
     host_out = torch.empty_like(host_q).pin_memory()
-    dq, dbt, dsl = torch.empty_like(w.q), torch.empty_like(w.block_tables), \
+    dq, dbt, dsl = torch.empty_like(q_in), torch.empty_like(w.block_tables), \
         torch.empty_like(w.seq_lens)
     host_kn = k_new.cpu().pin_memory() if k_new is not None else None
     host_vn = v_new.cpu().pin_memory() if v_new is not None else None
@@ -398,9 +416,10 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         peak, peak_src = measured_peaks()
         achieved = nbytes["total"] / kernel_s / 1e9
-        traffic = profile_traffic(args.config) if op == "decode" and args.kv == "bf16" else None
+        plain = op == "decode" and args.kv == "bf16" and qlen == 1
+        traffic = profile_traffic(args.config) if plain else None
         cpu = None
-        if not args.no_cpu_baseline and args.kv == "bf16":  # the baseline leg times the bf16 oracle
+        if not args.no_cpu_baseline and args.kv == "bf16" and qlen == 1:  # the baseline leg times the bf16 oracle
             w_host = workloads.host_copy(w)
             threads = len(os.sched_getaffinity(0))
             secs, b, ngroups, total_groups = oracle_baseline(w_host, spec, args.cpu_budget,
@@ -431,7 +450,7 @@ def run_ours(args, world, rank, local):
                 "name": args.config,
                 "num_seqs": spec.num_seqs, "H_q": spec.H_q, "H_kv": spec.H_kv,
                 "head_dim": spec.D, "block_size": spec.block_size,
-                "tokens": int(sum(lens)), "seed": seed, "op": op, "kv": args.kv,
+                "tokens": int(sum(lens)), "seed": seed, "op": op, "kv": args.kv, "q_len": qlen,
                 "bytes_per_step": nbytes,
                 "l2": f"inputs larger than L2: {reps} KV-cache replicas rotated "
                       f"({reps * kv_bytes / 1e9:.2f} GB vs 129 MB L2)",
@@ -442,7 +461,9 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback 6800 GB/s",
-                "kernel": "paged_decode_kernel over FP8 caches (one launch per step)" if fp8 else
+                "kernel": f"paged_decode_kernel, multi-token ({qlen} causal queries per "
+                          "sequence; one launch per step)" if qlen > 1 else
+                "paged_decode_kernel over FP8 caches (one launch per step)" if fp8 else
                 "paged_decode_kernel over x-packed caches (one launch per step)"
                 if args.kv == "xpacked" else
                 {"decode": "paged_decode_kernel (one launch per step, fused combine)",
@@ -529,6 +550,8 @@ def main():
                     choices=["decode", "append_decode", "append_then_decode"],
                     help="decode alone, or with each sequence's new token appended to the "
                          "cache first (fused into the decode launch, or a separate launch)")
+    ap.add_argument("--qlen", type=int, default=1,
+                    help="query tokens per sequence: > 1 runs the multi-token (causal) decode")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -540,6 +563,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.kv != "bf16" and args.op != "decode":
         ap.error(f"--kv {args.kv} runs the decode alone (--op decode)")
+    if args.qlen > 1 and (args.kv != "bf16" or args.op != "decode"):
+        ap.error("--qlen > 1 runs the bf16 decode alone")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)

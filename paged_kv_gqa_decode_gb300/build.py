@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["paged_attn_api.cu", "append.cu", "decode_d64.cu", "decode_d128.cu",
            "decode_d256.cu", "decode_fp8_d128.cu", "decode_fp8_d256.cu", "decode_xp_d64.cu",
-           "decode_xp_d128.cu", "decode_xp_d256.cu"]
+           "decode_xp_d128.cu", "decode_xp_d256.cu", "decode_multi_d64.cu",
+           "decode_multi_d128.cu", "decode_multi_d256.cu"]
 
 
 def nvcc() -> str:

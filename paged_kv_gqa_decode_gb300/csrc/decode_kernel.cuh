@@ -183,7 +183,10 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
 // section 3).  A K page lands in shared memory as [D / 8][BS][16 bytes] and a V
 // page as [D][BS] (V^T, 32- or 64-byte rows), so both MMA operands come from
 // plain ldmatrix with other addresses; everything else is the bf16 path.
-template <int D, int BS, bool G16, int KV = kKvBf16>
+//
+// MULTI: multi-token decode (DecodeParams::qo_indptr); compiled separately so
+// the single-token decode carries none of its row mapping or causal masking.
+template <int D, int BS, bool G16, int KV = kKvBf16, bool MULTI = false>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const bool multi = p.qo_indptr != nullptr;
+  constexpr bool multi = MULTI;
   const L lay{p.stages, multi ? p.rows : p.G, p.num_seqs, multi ? p.num_seqs + 1 : 0};
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tok = 16 * tg + row + ((e >> 1) << 3);
-          const float x = tok < valid && tb + tok <= lim[nh][e & 1]
+          const float x = tok < valid && (!MULTI || tb + tok <= lim[nh][e & 1])
                               ? s_acc[tg][nh][e] * p.scale_log2
                               : -INFINITY;
           s_acc[tg][nh][e] = x;
@@ -620,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
         const float m_new = fmaxf(m_run[nh][e], v);
         // a column that has seen no token yet (all masked) keeps -inf; subtract 0
         // then, so its weights are exp2(-inf) = 0 instead of NaN
-        m_sub[nh][e] = m_new == -INFINITY ? 0.f : m_new;
+        m_sub[nh][e] = MULTI && m_new == -INFINITY ? 0.f : m_new;
         alpha[nh][e] = fast_exp2(m_run[nh][e] - m_sub[nh][e]);
         changed |= m_new != m_run[nh][e];
         m_run[nh][e] = m_new;

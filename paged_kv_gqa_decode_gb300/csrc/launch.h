@@ -32,6 +32,16 @@ cudaError_t launch_decode_xp_d128(int block_size, bool g16, const CUtensorMap& t
 cudaError_t launch_decode_xp_d256(int block_size, bool g16, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const DecodeParams& p, int grid,
                                   size_t smem, cudaStream_t stream);
+// Multi-token decode over bf16 caches.
+cudaError_t launch_decode_multi_d64(int block_size, bool g16, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const DecodeParams& p, int grid,
+                                    size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_multi_d128(int block_size, bool g16, const CUtensorMap& tk,
+                                     const CUtensorMap& tv, const DecodeParams& p, int grid,
+                                     size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_multi_d256(int block_size, bool g16, const CUtensorMap& tk,
+                                     const CUtensorMap& tv, const DecodeParams& p, int grid,
+                                     size_t smem, cudaStream_t stream);
 // The same over FP8 caches (head_dim 128 or 256).
 cudaError_t launch_decode_fp8_d128(int block_size, bool g16, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const DecodeParams& p, int grid,
@@ -43,11 +53,11 @@ cudaError_t launch_decode_fp8_d256(int block_size, bool g16, const CUtensorMap& 
 // Launches one instantiation, first raising its dynamic shared-memory limit on
 // the current device when this launch needs more than was set before (the
 // record is per instantiation and per device).
-template <int D, int BS, bool G16, int KV>
+template <int D, int BS, bool G16, int KV, bool MULTI = false>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, size_t smem, cudaStream_t stream) {
   static int limit_set[64] = {0};
-  auto kernel = paged_decode_kernel<D, BS, G16, KV>;
+  auto kernel = paged_decode_kernel<D, BS, G16, KV, MULTI>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -72,14 +82,14 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
   return cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
 }
 
-template <int D, int KV = kKvBf16>
+template <int D, int KV = kKvBf16, bool MULTI = false>
 cudaError_t launch_for_dim(int block_size, bool g16, const CUtensorMap& tk, const CUtensorMap& tv,
                            const DecodeParams& p, int grid, size_t smem, cudaStream_t stream) {
   if (block_size == 16)
-    return g16 ? launch_one<D, 16, true, KV>(tk, tv, p, grid, smem, stream)
-               : launch_one<D, 16, false, KV>(tk, tv, p, grid, smem, stream);
-  return g16 ? launch_one<D, 32, true, KV>(tk, tv, p, grid, smem, stream)
-             : launch_one<D, 32, false, KV>(tk, tv, p, grid, smem, stream);
+    return g16 ? launch_one<D, 16, true, KV, MULTI>(tk, tv, p, grid, smem, stream)
+               : launch_one<D, 16, false, KV, MULTI>(tk, tv, p, grid, smem, stream);
+  return g16 ? launch_one<D, 32, true, KV, MULTI>(tk, tv, p, grid, smem, stream)
+             : launch_one<D, 32, false, KV, MULTI>(tk, tv, p, grid, smem, stream);
 }
 
 }  // namespace pagedattn

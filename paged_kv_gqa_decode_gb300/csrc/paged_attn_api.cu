@@ -300,6 +300,11 @@ int encode_xpacked_maps(const void* v, int D, int BS, int H_kv, long long num_bl
 cudaError_t launch_dim(int D, int BS, bool g16, bool fp8, bool xp, const CUtensorMap& tk,
                        const CUtensorMap& tv, const DecodeParams& p, int grid, size_t smem,
                        cudaStream_t st) {
+  if (p.qo_indptr != nullptr) {
+    if (D == 64) return launch_decode_multi_d64(BS, g16, tk, tv, p, grid, smem, st);
+    if (D == 128) return launch_decode_multi_d128(BS, g16, tk, tv, p, grid, smem, st);
+    return launch_decode_multi_d256(BS, g16, tk, tv, p, grid, smem, st);
+  }
   if (xp) {
     if (D == 64) return launch_decode_xp_d64(BS, g16, tk, tv, p, grid, smem, st);
     if (D == 128) return launch_decode_xp_d128(BS, g16, tk, tv, p, grid, smem, st);
