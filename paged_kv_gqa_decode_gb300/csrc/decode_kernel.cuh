@@ -1161,136 +1161,159 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   }
   reset();
   set_limits(wk.s, wk.g);
-  int stage = 0;
-  uint32_t phase = 0;
-  // FP8 with 16-token pages and a ring depth that is a multiple of 4 (so a
-  // warp's next unit is always 4 on, in the slot 4 on): a warp takes its page
-  // and its next one together, as one 32-token group, when both belong to the
-  // same piece; `taken` is that second unit.
-  const bool pairs = FP8 && BS == 16 && p.stages % kConsumerWarps == 0 &&
-                     p.stages >= 3 * kConsumerWarps;
-  long long taken = -1;
-  for (long long u = u0; u < u1; ++u) {
-    // Ring slot `stage` always belongs to consumer warp stage % 4, so each warp
-    // waits on its slots' phases strictly in order (a parity wait cannot tell
-    // phase k from phase k - 2) whatever the ring depth.
-    if constexpr (FP8) {
-      if (stage % kConsumerWarps == warp && !abort && u != taken) {
-        const bool two = pairs && wk.p + kConsumerWarps < wk.n && u + kConsumerWarps < u1;
-        const int stage2 = two ? (stage + kConsumerWarps) % p.stages : stage;
-        const uint32_t phase2 = phase ^ (uint32_t)(stage + kConsumerWarps >= p.stages);
-        const bool ready = __all_sync(
-            0xffffffffu, mbar_wait(&full_bar[stage], phase) &&
-                             (!two || mbar_wait(&full_bar[stage2], phase2)));
-        if (!ready) {
-          if (lane == 0) atomicOr(p.status, kStatusTimeout);
-          abort = true;
-        } else {
-          const int len = sm_len[wk.s];
-          const int valid = min(BS, len - wk.p * BS);
-          const int valid2 = two ? min(BS, len - (wk.p + kConsumerWarps) * BS) : 0;
-          uint8_t* st = smem + stage * kStageBytes;
-          uint8_t* st2 = smem + stage2 * kStageBytes;
-          // Only the piece's last page can end early: zero its V rows past the
-          // sequence (they may hold anything) so the V operand needs no mask.
-          uint8_t* tail_v = (two ? st2 : st) + kPageBytes;
-          const int tail_valid = two ? valid2 : valid;
-          const bool tail = tail_valid < BS;
-          if (tail) {
-            const int chunks = (BS - tail_valid) * L::kHalves * 8;  // 16-byte chunks
-            for (int c = lane; c < chunks; c += 32) {
-              const int r = tail_valid + c / (L::kHalves * 8);
-              const int h = (c / 8) % L::kHalves;
-              *reinterpret_cast<uint4*>(tail_v + h * kTileBytes + r * 128 + (c % 8) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
+  // Ring ownership: unit i of the range (i = u - u0) sits in slot i % stages,
+  // and slot r belongs to consumer warp r % 4, so each warp waits on its
+  // slots' phases strictly in order (a parity wait cannot tell phase k from
+  // k - 2) whatever the ring depth.  A warp steps from one of its units
+  // straight to its next: slot + 4 in the same round of the ring, else slot
+  // `warp` of the next round.
+  const int n_stages = p.stages;
+  long long own_i = warp;  // this warp's next unit (index within the range)
+  int own_slot = warp;
+  uint32_t own_phase = 0;
+  auto own_step = [&](long long& i, int& slot, uint32_t& ph) {
+    if (slot + kConsumerWarps < n_stages) {
+      i += kConsumerWarps;
+      slot += kConsumerWarps;
+    } else {
+      i += n_stages - slot + warp;
+      slot = warp;
+      ph ^= 1u;
+    }
+  };
+  // FP8 with 16-token pages and a ring of at least 12 slots: a warp takes its
+  // page and its next one together, as one 32-token group, when both belong
+  // to the same piece.
+  const bool pairs = FP8 && BS == 16 && n_stages >= 3 * kConsumerWarps;
+  const long long n_units = u1 - u0;
+  long long ia = 0;  // the current piece's first unit (index within the range)
+  for (;;) {
+    const int s = wk.s, g = wk.g, n = wk.n, p0 = wk.p;
+    const long long ib = min(n_units, ia + (n - p0));  // one past its last unit here
+    while (own_i < ib) {
+      const int pg = p0 + (int)(own_i - ia);  // page of the sequence
+      if constexpr (FP8) {
+        long long i2 = own_i;
+        int slot2 = own_slot;
+        uint32_t ph2 = own_phase;
+        own_step(i2, slot2, ph2);
+        const bool two = pairs && i2 < ib;
+        const int pg2 = p0 + (int)(i2 - ia);
+        if (!abort) {
+          const bool ready = __all_sync(
+              0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase) &&
+                               (!two || mbar_wait(&full_bar[slot2], ph2)));
+          if (!ready) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            abort = true;
+          } else {
+            const int len = sm_len[s];
+            const int valid = min(BS, len - pg * BS);
+            const int valid2 = two ? min(BS, len - pg2 * BS) : 0;
+            uint8_t* st = smem + own_slot * kStageBytes;
+            uint8_t* st2 = smem + (two ? slot2 : own_slot) * kStageBytes;
+            // Only the piece's last page can end early: zero its V rows past
+            // the sequence (they may hold anything) so the V operand needs no mask.
+            uint8_t* tail_v = (two ? st2 : st) + kPageBytes;
+            const int tail_valid = two ? valid2 : valid;
+            const bool tail = tail_valid < BS;
+            if (tail) {
+              const int chunks = (BS - tail_valid) * L::kHalves * 8;  // 16-byte chunks
+              for (int c = lane; c < chunks; c += 32) {
+                const int r = tail_valid + c / (L::kHalves * 8);
+                const int h = (c / 8) % L::kHalves;
+                *reinterpret_cast<uint4*>(tail_v + h * kTileBytes + r * 128 + (c % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              __syncwarp();
+            }
+            const float* sc = sm_scales + (size_t)own_slot * 2 * BS;
+            const float* sc2 = sm_scales + (size_t)(two ? slot2 : own_slot) * 2 * BS;
+            const uint8_t* q16 = sm_q + qbuf * kQSlotBytes + kQTileBytes;
+            const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
+            if constexpr (BS == 16) {
+              if (two) {
+                const Tile8 t[2] = {{k0, v0, sc, sc + BS, valid},
+                                    {smem_addr(st2), smem_addr(st2 + kPageBytes), sc2,
+                                     sc2 + BS, valid2}};
+                process_fp8(std::integral_constant<int, 2>(), t, q16);
+              } else {
+                const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
+                process_fp8(std::integral_constant<int, 1>(), t, q16);
+              }
+            } else {  // the two 16-token halves of a 32-token page
+              const Tile8 t[2] = {{k0, v0, sc, sc + BS, min(16, valid)},
+                                  {k0 + 16 * 128, v0 + 16 * 128, sc + 16, sc + BS + 16,
+                                   max(0, valid - 16)}};
+              process_fp8(std::integral_constant<int, 2>(), t, q16);
+            }
+            // the zeroing's generic writes precede the next tensor copy into the slot
+            if (tail) fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&empty_bar[own_slot]);
+              if (two) mbar_arrive(&empty_bar[slot2]);
+            }
+          }
+        }
+        own_step(own_i, own_slot, own_phase);
+        if (two) own_step(own_i, own_slot, own_phase);
+      } else {
+        if (!abort) {
+          // Fused cache append: the last page of a piece holds the sequence's
+          // new token.  Its rows (prefetched with the piece's query group) are
+          // patched into the page in shared memory once the page has landed
+          // (the tensor copy brought whatever the cache held) and stored to the
+          // cache for later calls.  This page is read by this CTA alone.
+          const bool patch = !XP && !multi && p.k_new != nullptr && pg == n - 1;
+          // Lanes poll the barrier independently; the vote both reconverges
+          // the warp before the warp-collective ldmatrix / movmatrix / mma and
+          // makes the outcome uniform.
+          const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase));
+          if (!ready) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            abort = true;
+          } else {
+            const int valid = min(BS, sm_len[s] - pg * BS);
+            uint8_t* st = smem + own_slot * kStageBytes;
+            const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
+            if (patch) {
+              const int slot = valid - 1;  // the new token, t = L - 1
+              if (lane < D / 8) {
+                // 16-byte chunk `lane` of the row: half lane / 8, swizzled position within it
+                const int off =
+                    (lane >> 3) * kTileBytes + slot * 128 + (((lane & 7) ^ (slot & 7)) << 4);
+                *reinterpret_cast<uint4*>(st + off) = reinterpret_cast<const uint4*>(extra)[lane];
+                *reinterpret_cast<uint4*>(st + kPageBytes + off) =
+                    reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
+              }
+              __syncwarp();
+            }
+            process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid, pg * BS, lim);
+            if (patch) {
+              // the patch's generic writes precede the next tensor copy into this slot
+              fence_proxy_async_shared();
+              const int slot = valid - 1;
+              const int new_block = *reinterpret_cast<const int*>(extra + 4 * D);
+              if (lane < D / 8 &&
+                  (p.num_blocks <= 0 || (new_block >= 0 && (long long)new_block < p.num_blocks))) {
+                const size_t dst = (((size_t)new_block * H_kv + g) * BS + slot) * D + lane * 8;
+                *reinterpret_cast<uint4*>(p.k_cache + dst) =
+                    reinterpret_cast<const uint4*>(extra)[lane];
+                *reinterpret_cast<uint4*>(p.v_cache + dst) =
+                    reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
+              }
             }
             __syncwarp();
-          }
-          const float* sc = sm_scales + (size_t)stage * 2 * BS;
-          const float* sc2 = sm_scales + (size_t)stage2 * 2 * BS;
-          const uint8_t* q16 = sm_q + qbuf * kQSlotBytes + kQTileBytes;
-          const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
-          if constexpr (BS == 16) {
-            if (two) {
-              const Tile8 t[2] = {{k0, v0, sc, sc + BS, valid},
-                                  {smem_addr(st2), smem_addr(st2 + kPageBytes), sc2, sc2 + BS,
-                                   valid2}};
-              process_fp8(std::integral_constant<int, 2>(), t, q16);
-            } else {
-              const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
-              process_fp8(std::integral_constant<int, 1>(), t, q16);
-            }
-          } else {  // the two 16-token halves of a 32-token page
-            const Tile8 t[2] = {{k0, v0, sc, sc + BS, min(16, valid)},
-                                {k0 + 16 * 128, v0 + 16 * 128, sc + 16, sc + BS + 16,
-                                 max(0, valid - 16)}};
-            process_fp8(std::integral_constant<int, 2>(), t, q16);
-          }
-          // the zeroing's generic writes precede the next tensor copy into the slot
-          if (tail) fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&empty_bar[stage]);
-            if (two) mbar_arrive(&empty_bar[stage2]);
-          }
-          if (two) taken = u + kConsumerWarps;
-        }
-      }
-    } else if (stage % kConsumerWarps == warp && !abort) {
-      // Fused cache append: the last page of a piece holds the sequence's new
-      // token.  Its rows (prefetched with the piece's query group) are patched
-      // into the page in shared memory once the page has landed (the tensor
-      // copy brought whatever the cache held) and stored to the cache for later
-      // calls.  This page is read by this CTA alone.
-      const bool patch = !XP && !multi && p.k_new != nullptr && wk.p == wk.n - 1;
-      // Lanes poll the barrier independently; the vote both reconverges the warp
-      // before the warp-collective ldmatrix / movmatrix / mma and makes the
-      // outcome uniform.
-      const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase));
-      if (!ready) {
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
-        abort = true;
-      } else {
-        const int valid = min(BS, sm_len[wk.s] - wk.p * BS);
-        uint8_t* st = smem + stage * kStageBytes;
-        const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
-        if (patch) {
-          const int slot = valid - 1;  // the new token, t = L - 1
-          if (lane < D / 8) {
-            // 16-byte chunk `lane` of the row: half lane / 8, swizzled position within it
-            const int off = (lane >> 3) * kTileBytes + slot * 128 + (((lane & 7) ^ (slot & 7)) << 4);
-            *reinterpret_cast<uint4*>(st + off) = reinterpret_cast<const uint4*>(extra)[lane];
-            *reinterpret_cast<uint4*>(st + kPageBytes + off) =
-                reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
-          }
-          __syncwarp();
-        }
-        process_page(st, st + kPageBytes, sm_q + qbuf * kQSlotBytes, valid, wk.p * BS, lim);
-        if (patch) {
-          // the patch's generic writes precede the next tensor copy into this slot
-          fence_proxy_async_shared();
-          const int slot = valid - 1;
-          const int new_block = *reinterpret_cast<const int*>(extra + 4 * D);
-          if (lane < D / 8 &&
-              (p.num_blocks <= 0 || (new_block >= 0 && (long long)new_block < p.num_blocks))) {
-            const size_t dst = (((size_t)new_block * H_kv + wk.g) * BS + slot) * D + lane * 8;
-            *reinterpret_cast<uint4*>(p.k_cache + dst) = reinterpret_cast<const uint4*>(extra)[lane];
-            *reinterpret_cast<uint4*>(p.v_cache + dst) =
-                reinterpret_cast<const uint4*>(extra + 2 * D)[lane];
+            if (lane == 0) mbar_arrive(&empty_bar[own_slot]);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        own_step(own_i, own_slot, own_phase);
       }
     }
-    if (++stage == p.stages) {
-      stage = 0;
-      phase ^= 1u;
-    }
-    const int s = wk.s, g = wk.g, n = wk.n;
-    const bool last = u + 1 == u1;
-    wk.next(sm_prefix, N, H_v);
-    if (!last && wk.g == g && wk.s == s) continue;
+    const bool last = ib == n_units;
+    if (!last) wk.advance((int)(ib - ia), sm_prefix, N, H_v);  // to the next piece
+    ia = ib;
     const long long sb = (long long)sm_prefix[s] * H_v + (long long)g * n;
     if (!last) {
       // A split piece that is not the range's last is its first: store its
@@ -1376,6 +1399,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       if (cf) *word_f = 0;
       if (cl) *word_l = 0;
     }
+    break;
   }
   cp_async_wait_all();
 }
