@@ -700,9 +700,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
   };
 
   // FP8 tiles.  The unit of work is a group of NT 16-token tiles (one BS = 16
-  // page, the two halves of a BS = 32 page, or two pages of one piece taken
-  // together), each tile with its own K / V shared-memory rows, row floats and
-  // count of valid tokens.  S^T = K Q^T on f16 tensor cores: one ldmatrix.x4
+  // page, or the two halves of a BS = 32 page), each tile with its own K / V
+  // shared-memory rows, row floats and count of valid tokens.  S^T = K Q^T on f16 tensor cores: one ldmatrix.x4
   // on the e4m3 K tile hands each lane, for two 16-column steps (two 16-byte
   // chunks), the bytes 4q..4q+3 of its token rows r and r + 8; within each
   // chunk the contraction runs in a fixed permuted order (bytes 4q, 4q+1 ->
@@ -1181,10 +1180,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
       ph ^= 1u;
     }
   };
-  // FP8 with 16-token pages and a ring of at least 12 slots: a warp takes its
-  // page and its next one together, as one 32-token group, when both belong
-  // to the same piece.
-  const bool pairs = FP8 && BS == 16 && n_stages >= 3 * kConsumerWarps;
   const long long n_units = u1 - u0;
   long long ia = 0;  // the current piece's first unit (index within the range)
   for (;;) {
@@ -1193,54 +1188,33 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
     while (own_i < ib) {
       const int pg = p0 + (int)(own_i - ia);  // page of the sequence
       if constexpr (FP8) {
-        long long i2 = own_i;
-        int slot2 = own_slot;
-        uint32_t ph2 = own_phase;
-        own_step(i2, slot2, ph2);
-        const bool two = pairs && i2 < ib;
-        const int pg2 = p0 + (int)(i2 - ia);
         if (!abort) {
-          const bool ready = __all_sync(
-              0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase) &&
-                               (!two || mbar_wait(&full_bar[slot2], ph2)));
+          const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase));
           if (!ready) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             abort = true;
           } else {
-            const int len = sm_len[s];
-            const int valid = min(BS, len - pg * BS);
-            const int valid2 = two ? min(BS, len - pg2 * BS) : 0;
+            const int valid = min(BS, sm_len[s] - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
-            uint8_t* st2 = smem + (two ? slot2 : own_slot) * kStageBytes;
             // Only the piece's last page can end early: zero its V rows past
             // the sequence (they may hold anything) so the V operand needs no mask.
-            uint8_t* tail_v = (two ? st2 : st) + kPageBytes;
-            const int tail_valid = two ? valid2 : valid;
-            const bool tail = tail_valid < BS;
+            const bool tail = valid < BS;
             if (tail) {
-              const int chunks = (BS - tail_valid) * L::kHalves * 8;  // 16-byte chunks
+              const int chunks = (BS - valid) * L::kHalves * 8;  // 16-byte chunks
               for (int c = lane; c < chunks; c += 32) {
-                const int r = tail_valid + c / (L::kHalves * 8);
+                const int r = valid + c / (L::kHalves * 8);
                 const int h = (c / 8) % L::kHalves;
-                *reinterpret_cast<uint4*>(tail_v + h * kTileBytes + r * 128 + (c % 8) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(st + kPageBytes + h * kTileBytes + r * 128 +
+                                          (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
               }
               __syncwarp();
             }
             const float* sc = sm_scales + (size_t)own_slot * 2 * BS;
-            const float* sc2 = sm_scales + (size_t)(two ? slot2 : own_slot) * 2 * BS;
             const uint8_t* q16 = sm_q + qbuf * kQSlotBytes + kQTileBytes;
             const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
             if constexpr (BS == 16) {
-              if (two) {
-                const Tile8 t[2] = {{k0, v0, sc, sc + BS, valid},
-                                    {smem_addr(st2), smem_addr(st2 + kPageBytes), sc2,
-                                     sc2 + BS, valid2}};
-                process_fp8(std::integral_constant<int, 2>(), t, q16);
-              } else {
-                const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
-                process_fp8(std::integral_constant<int, 1>(), t, q16);
-              }
+              const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
+              process_fp8(std::integral_constant<int, 1>(), t, q16);
             } else {  // the two 16-token halves of a 32-token page
               const Tile8 t[2] = {{k0, v0, sc, sc + BS, min(16, valid)},
                                   {k0 + 16 * 128, v0 + 16 * 128, sc + 16, sc + BS + 16,
@@ -1250,14 +1224,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
             // the zeroing's generic writes precede the next tensor copy into the slot
             if (tail) fence_proxy_async_shared();
             __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(&empty_bar[own_slot]);
-              if (two) mbar_arrive(&empty_bar[slot2]);
-            }
+            if (lane == 0) mbar_arrive(&empty_bar[own_slot]);
           }
         }
         own_step(own_i, own_slot, own_phase);
-        if (two) own_step(own_i, own_slot, own_phase);
       } else {
         if (!abort) {
           // Fused cache append: the last page of a piece holds the sequence's
