@@ -23,12 +23,15 @@
 //
 //  * Math (tensor cores, bf16 m16n8k16, fp32 accumulate), with the page's
 //    tokens as the M dimension and the GQA group as N (8 heads per n-tile):
-//    S^T = K Q^T (K read with ldmatrix from the swizzled tile, Q^T held in
-//    registers for the whole piece), online softmax in fp32 on the
-//    accumulator fragments (BI-V100 design, section 2, Level 1: running max,
-//    exp-sum and weighted V), P^T turned into the B operand with movmatrix,
-//    then O^T += V^T P^T (V read with ldmatrix.trans).  Every K/V byte leaves
-//    HBM once and feeds all G heads of its group.
+//    S^T = K Q^T (K read with ldmatrix from the swizzled tile, Q^T with
+//    ldmatrix from the piece's query tile in shared memory), online softmax
+//    in fp32 on the accumulator fragments (BI-V100 design, section 2, Level
+//    1: running max, exp-sum and weighted V), P^T turned into the B operand
+//    with movmatrix, then O^T += V^T P^T (V read with ldmatrix.trans).  Every
+//    K/V byte leaves HBM once and feeds all G heads of its group.  The FP8,
+//    x-packed and multi-token variants change the operands' loads, the
+//    conversions and the query rows, not this structure (see process_fp8,
+//    the XP branches and qrow / row_limit).
 //
 //  * Merge (BI-V100 design, section 2, Levels 2 and 3): at the end of each
 //    (s, g) piece the consumer warps merge their states through shared
