@@ -56,10 +56,15 @@ namespace pagedattn {
 
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-// Two independent pipelines per SM; the one variant whose accumulators need the
-// whole register file (head_dim 256 with more than 8 heads per group) runs one.
-__host__ __device__ constexpr int ctas_per_sm(int D, bool g16) {
-  return (D >= 256 && g16) ? 1 : 2;
+// Two independent pipelines per SM, except (a) head_dim 256 with more than 8
+// query rows, whose accumulators need the whole register file, and (b) bf16
+// stages of 16 KB or more (head_dim 256, or 32-token pages): two CTAs could
+// hold only one ring slot per consumer warp, which then idles while its next
+// page loads; one CTA with two slots a warp and the registers of a whole SM
+// streams faster (Qwen-shaped 100K decode 246 -> 237 us, GQA-8 batch 306 -> 303
+// us).  FP8 stages are half as large and its consumers need the warps.
+__host__ __device__ constexpr int ctas_per_sm(int D, bool g16, int BS = 16, bool fp8 = false) {
+  return (D >= 256 && g16) || (!fp8 && D * BS * 2 * 2 >= (16 << 10)) ? 1 : 2;
 }
 constexpr int kMinPagesPerCta = 8;
 constexpr int kMaxStages = 16;  // ring depth cap (slot s belongs to consumer warp s % 4)
@@ -190,7 +195,7 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
 // MULTI: multi-token decode (DecodeParams::qo_indptr); compiled separately so
 // the single-token decode carries none of its row mapping or causal masking.
 template <int D, int BS, bool G16, int KV = kKvBf16, bool MULTI = false>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16))
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr bool FP8 = KV == kKvFp8;

@@ -171,7 +171,7 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
   // fewer sequences at a time.
   bool ok = false;
   int chunk = chunk0;
-  for (int occ = ctas_per_sm(D, pl->g16); occ >= 1 && !ok; --occ) {
+  for (int occ = ctas_per_sm(D, pl->g16, BS, fp8); occ >= 1 && !ok; --occ) {
     int budget = di.smem_per_sm / occ - 1024;  // 1 KB per CTA is reserved by the system
     if (budget > di.max_smem) budget = di.max_smem;
     chunk = chunk0;
