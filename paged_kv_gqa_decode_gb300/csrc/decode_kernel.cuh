@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr bool multi = MULTI;
-  const L lay{p.stages, multi ? p.rows : p.G, p.num_seqs, multi ? p.num_seqs + 1 : 0};
+  const L lay{p.stages, multi ? p.rows : p.G, p.num_seqs, multi ? p.num_seqs + 1 : 0,
+              multi ? p.chunks : 1};
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + lay.bars());
   uint64_t* empty_bar = full_bar + p.stages;
   uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
@@ -244,7 +245,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   const int G = p.G;
   const int R = multi ? p.rows : G;      // query rows of one piece
   const int QC = multi ? p.chunks : 1;   // pieces per (sequence, KV head)
-  const int H_v = H_kv * QC;             // pieces per sequence, walked like KV heads
+  // Multi-token decode with QC > 1 walks the sequences QC times, pass c for row
+  // chunk c of every KV head (chunk-major, so the passes over the same pages
+  // run at the same time on different CTAs and the repeated reads hit L2):
+  // walked sequence sw = c * N + s.
+  const int NW = N * QC;
   const int cap = p.maxb * BS;
 
   // ---- 0. Programmatic dependent launch: let the next kernel in the stream be
@@ -307,6 +312,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       for (int s = tid; s <= N; s += kThreads) sm_qo[s] = __ldg(p.qo_indptr + s);
     }
     __syncthreads();
+    if (multi && QC > 1) {  // page prefix of the later passes: offset by c * (all pages)
+      const int P = sm_prefix[N];
+      for (int i = tid; i < (QC - 1) * N; i += kThreads) {
+        const int c = 1 + i / N;
+        const int sq = i - (c - 1) * N;
+        sm_prefix[c * N + sq] = c * P + sm_prefix[sq];
+      }
+      if (tid == 0) sm_prefix[NW] = QC * P;
+      __syncthreads();
+    }
     if (multi && blockIdx.x == 0) {
       // rows a sequence cannot hold (q_len < 0, or more than the pieces carry) are
       // reported; they are never read or written
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     for (int i = tid; i < nr * p.H_q * D / 2; i += kThreads) o32[i] = 0u;
   }
 
-  const long long W = (long long)sm_prefix[N] * H_v;
+  const long long W = (long long)sm_prefix[NW] * H_kv;
   if (W == 0) return;
   if (p.stages < kConsumerWarps) {  // the host plan never launches fewer
     if (tid == 0) atomicOr(p.status, kStatusConfig);
@@ -357,14 +372,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     // stages, so the lanes of one wave always wait on distinct slots.
     const int issue_lanes = min(kMaxIssueLanes, p.stages);
     Walker wk;
-    if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, N, H_v);
+    if (u0 + lane < u1) wk.start(u0 + lane, sm_prefix, NW, H_kv);
     auto fetch = [&](long long u) -> int2 {
       // physical block and KV head of this lane's unit (block -1 past the range)
       if (u >= u1) return make_int2(-1, 0);
-      int pb = __ldg(p.block_tables + (size_t)wk.s * p.maxb + wk.p);
+      const int sq = multi && QC > 1 ? wk.s % N : wk.s;  // the walked sequence's sequence
+      int pb = __ldg(p.block_tables + (size_t)sq * p.maxb + wk.p);
       if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
         atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
-      return make_int2(pb, wk.g / QC);  // the piece's KV head
+      return make_int2(pb, wk.g);
     };
     int2 cur = fetch(u0 + lane);
     bool abort = false;
@@ -372,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
       if (ub + 32 + lane < u1) {
-        wk.advance(32, sm_prefix, N, H_v);
+        wk.advance(32, sm_prefix, NW, H_kv);
         nxt = fetch(ub + 32 + lane);
       }
       const int cnt = (int)min(32LL, u1 - ub);
@@ -455,22 +471,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // rows and the block id of its last page, so the warp that patches that page
   // finds them in shared memory.
   // Row of q / out ([rows, H_q, D] viewed as rows of D) that row r of piece
-  // (s, gv) stands for, or -1 for a padding row (never stored).  gv is the
-  // piece's index among its sequence's H_kv * QC pieces.
-  auto qrow = [&](int s, int gv, int r) -> long long {
-    if (!multi) return r < G ? (long long)s * p.H_q + (long long)gv * G + r : -1;
-    const int g = gv / QC;
-    const int rr = (gv - g * QC) * R + r;  // row within the KV head's q_len * G rows
+  // (sw, g) stands for, or -1 for a padding row (never stored): walked
+  // sequence sw = c * N + s holds row chunk c of sequence s.
+  auto qrow = [&](int sw, int g, int r) -> long long {
+    if (!multi) return r < G ? (long long)sw * p.H_q + (long long)g * G + r : -1;
+    const int c = sw / N;
+    const int s = sw - c * N;
+    const int rr = c * R + r;  // row within the KV head's q_len * G rows
     const int i = rr / G;
     const long long t = (long long)sm_qo[s] + i;  // the query's row of q / out
     if (r >= R || i >= sm_qo[s + 1] - sm_qo[s] || t < 0 || t >= p.total_q) return -1;
     return t * p.H_q + (long long)g * G + (rr - i * G);
   };
-  // Last token row r of piece (s, gv) attends (causal in multi-token decode).
-  auto row_limit = [&](int s, int gv, int r) -> int {
+  // Last token row r of piece (sw, g) attends (causal in multi-token decode).
+  auto row_limit = [&](int sw, int g, int r) -> int {
     if (!multi) return 0x7fffffff;
-    const int g = gv / QC;
-    const int i = ((gv - g * QC) * R + r) / G;
+    const int c = sw / N;
+    const int s = sw - c * N;
+    const int i = (c * R + r) / G;
     const int ql = sm_qo[s + 1] - sm_qo[s];
     return i < ql ? sm_len[s] - ql + i : 0x7fffffff;  // padding rows: anything
   };
@@ -1124,30 +1142,30 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   };
   auto next_piece = [&](Piece pc) -> Piece {
     const int n = sm_prefix[pc.s + 1] - sm_prefix[pc.s];
-    if (++pc.g == H_v) {
+    if (++pc.g == H_kv) {
       pc.g = 0;
       do {
         ++pc.s;
-      } while (pc.s < N && sm_prefix[pc.s + 1] == sm_prefix[pc.s]);
+      } while (pc.s < NW && sm_prefix[pc.s + 1] == sm_prefix[pc.s]);
     }
-    pc.sb = pc.s < N ? (long long)sm_prefix[pc.s] * H_v +
+    pc.sb = pc.s < NW ? (long long)sm_prefix[pc.s] * H_kv +
                            (long long)pc.g * (sm_prefix[pc.s + 1] - sm_prefix[pc.s])
                      : pc.sb + n;
     return pc;
   };
 
   Walker wk;
-  wk.start(u0, sm_prefix, N, H_v);
+  wk.start(u0, sm_prefix, NW, H_kv);
   // The range's first and last pieces (the only ones that can be split) and
   // their split descriptors, worked out now by thread 0 (off the critical path
   // at the end) and kept in shared memory, not in registers, through the loop.
   Split* const sm_split = reinterpret_cast<Split*>(sm_flag + 4);  // [0] first, [1] last
   int* const sm_split_flags = sm_flag + 4 + 2 * (int)(sizeof(Split) / sizeof(int));
   if (ctid == 0) {
-    const long long first_sb = (long long)sm_prefix[wk.s] * H_v + (long long)wk.g * wk.n;
+    const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
     Walker wl;
-    wl.start(u1 - 1, sm_prefix, N, H_v);
-    const long long last_sb = (long long)sm_prefix[wl.s] * H_v + (long long)wl.g * wl.n;
+    wl.start(u1 - 1, sm_prefix, NW, H_kv);
+    const long long last_sb = (long long)sm_prefix[wl.s] * H_kv + (long long)wl.g * wl.n;
     sm_split[0] = make_split(wk.s, wk.g, first_sb, first_sb + wk.n);
     sm_split[1] = make_split(wl.s, wl.g, last_sb, last_sb + wl.n);
     sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
@@ -1160,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   cp_async_wait_all();
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);
-  if (ahead.s < N && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
+  if (ahead.s < NW && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
   if constexpr (FP8) {
     convert_q(0);
     __syncwarp();
@@ -1192,6 +1210,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   long long ia = 0;  // the current piece's first unit (index within the range)
   for (;;) {
     const int s = wk.s, g = wk.g, n = wk.n, p0 = wk.p;
+    const int sq = multi && QC > 1 ? s % N : s;  // the walked sequence's sequence
     const long long ib = min(n_units, ia + (n - p0));  // one past its last unit here
     while (own_i < ib) {
       const int pg = p0 + (int)(own_i - ia);  // page of the sequence
@@ -1202,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             abort = true;
           } else {
-            const int valid = min(BS, sm_len[s] - pg * BS);
+            const int valid = min(BS, sm_len[sq] - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
             // Only the piece's last page can end early: zero its V rows past
             // the sequence (they may hold anything) so the V operand needs no mask.
@@ -1252,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             abort = true;
           } else {
-            const int valid = min(BS, sm_len[s] - pg * BS);
+            const int valid = min(BS, sm_len[sq] - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
             const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
             if (patch) {
@@ -1290,9 +1309,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       }
     }
     const bool last = ib == n_units;
-    if (!last) wk.advance((int)(ib - ia), sm_prefix, N, H_v);  // to the next piece
+    if (!last) wk.advance((int)(ib - ia), sm_prefix, NW, H_kv);  // to the next piece
     ia = ib;
-    const long long sb = (long long)sm_prefix[s] * H_v + (long long)g * n;
+    const long long sb = (long long)sm_prefix[s] * H_kv + (long long)g * n;
     if (!last) {
       // A split piece that is not the range's last is its first: store its
       // partial, then arrive and publish at once with a release add (the
@@ -1311,7 +1330,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         first_old = atom_add_release_gpu(p.counters + sm_split[0].c_first, 1 + (1 << 16));
       qbuf ^= 1;
       ahead = next_piece(ahead);
-      if (ahead.s < N && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
+      if (ahead.s < NW && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
       if constexpr (FP8) {
         convert_q(qbuf);
         __syncwarp();

@@ -110,13 +110,15 @@ struct Plan {
   size_t off_counters, off_partials, ws_bytes;
 };
 
-// G: query rows of one piece; qo: multi-token decode (room for chunk + 1 row offsets).
+// G: query rows of one piece; qchunks > 0: multi-token decode (room for chunk + 1
+// row offsets and the page prefixes of qchunks passes).
 template <int D, int BS, bool FP8>
-bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, bool qo, int* stages,
+bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, int qchunks, int* stages,
                size_t* smem) {
   using L = SmemLayout<D, BS, FP8>;
-  const int qo_entries = qo ? chunk + 1 : 0;
-  const L none{0, G, chunk, qo_entries};
+  const int qo_entries = qchunks > 0 ? chunk + 1 : 0;
+  const int walks = qchunks > 0 ? qchunks : 1;
+  const L none{0, G, chunk, qo_entries, walks};
   const long long fixed = none.total() + 2048;  // + alignment slack and static shared memory
   const long long per_stage = L::kStageBytes + L::kScaleBytes + 16;
   long long st = (max_smem - fixed) / per_stage;
@@ -124,32 +126,32 @@ bool plan_smem(int G, int chunk, int max_smem, long long ring_cap, bool qo, int*
   if (st > ring_cap / L::kStageBytes) st = ring_cap / L::kStageBytes;
   // At least one slot per consumer warp (slot s belongs to warp s % 4).
   if (st < kConsumerWarps) return false;
-  const L lay{(int)st, G, chunk, qo_entries};
+  const L lay{(int)st, G, chunk, qo_entries, walks};
   *stages = (int)st;
   *smem = (size_t)lay.total() + 1024;
   return *smem + 256 <= (size_t)max_smem;  // + the kernel's static shared memory
 }
 
 template <bool FP8>
-bool plan_smem_d(int D, int BS, int G, int chunk, int max_smem, long long ring_cap, bool qo,
-                 int* stages, size_t* smem) {
+bool plan_smem_d(int D, int BS, int G, int chunk, int max_smem, long long ring_cap,
+                 int qchunks, int* stages, size_t* smem) {
   if (D == 64) {
     if constexpr (FP8) return false;  // FP8 caches need head_dim 128 or 256
     else
-      return BS == 16 ? plan_smem<64, 16, false>(G, chunk, max_smem, ring_cap, qo, stages, smem)
-                      : plan_smem<64, 32, false>(G, chunk, max_smem, ring_cap, qo, stages, smem);
+      return BS == 16 ? plan_smem<64, 16, false>(G, chunk, max_smem, ring_cap, qchunks, stages, smem)
+                      : plan_smem<64, 32, false>(G, chunk, max_smem, ring_cap, qchunks, stages, smem);
   }
   if (D == 128)
-    return BS == 16 ? plan_smem<128, 16, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem)
-                    : plan_smem<128, 32, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem);
-  return BS == 16 ? plan_smem<256, 16, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem)
-                  : plan_smem<256, 32, FP8>(G, chunk, max_smem, ring_cap, qo, stages, smem);
+    return BS == 16 ? plan_smem<128, 16, FP8>(G, chunk, max_smem, ring_cap, qchunks, stages, smem)
+                    : plan_smem<128, 32, FP8>(G, chunk, max_smem, ring_cap, qchunks, stages, smem);
+  return BS == 16 ? plan_smem<256, 16, FP8>(G, chunk, max_smem, ring_cap, qchunks, stages, smem)
+                  : plan_smem<256, 32, FP8>(G, chunk, max_smem, ring_cap, qchunks, stages, smem);
 }
 
 bool plan_smem_any(int D, int BS, bool fp8, int G, int chunk, int max_smem, long long ring_cap,
-                   bool qo, int* stages, size_t* smem) {
-  return fp8 ? plan_smem_d<true>(D, BS, G, chunk, max_smem, ring_cap, qo, stages, smem)
-             : plan_smem_d<false>(D, BS, G, chunk, max_smem, ring_cap, qo, stages, smem);
+                   int qchunks, int* stages, size_t* smem) {
+  return fp8 ? plan_smem_d<true>(D, BS, G, chunk, max_smem, ring_cap, qchunks, stages, smem)
+             : plan_smem_d<false>(D, BS, G, chunk, max_smem, ring_cap, qchunks, stages, smem);
 }
 
 // rows > 0: multi-token decode with `rows` query rows per piece and `qchunks`
@@ -184,7 +186,7 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
       const long long pieces = (long long)chunk * H_kv * (pl->qchunks > 0 ? pl->qchunks : 1);
       const long long ring_cap =
           (pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces : kRingBytesPerSm) / occ;
-      if (plan_smem_any(D, BS, fp8, pl->rows, chunk, budget, ring_cap, pl->qchunks > 0,
+      if (plan_smem_any(D, BS, fp8, pl->rows, chunk, budget, ring_cap, pl->qchunks,
                         &pl->stages, &pl->smem) &&
           (pl->stages >= 4 || chunk <= 64)) {
         ok = true;

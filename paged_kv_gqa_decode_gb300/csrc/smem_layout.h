@@ -35,6 +35,7 @@ struct SmemLayout {
 
   int stages, G, num_seqs;  // G: query rows of one piece (the group size, or a chunk)
   int qo_entries = 0;       // multi-token decode: num_seqs + 1 query-row offsets
+  int walks = 1;            // multi-token decode: passes over the sequences (row chunks)
   // [0, bars): the ring of `stages` K/V pages (at the end of a range it holds the
   // partial states being combined); then the mbarriers full[stages],
   // empty[stages] and one for the combine's copies; FP8: the ring of row floats
@@ -58,7 +59,9 @@ struct SmemLayout {
     return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
   }
   PAGEDATTN_HD int prefix() const { return qtile() + 2 * q_slot_bytes(); }
-  PAGEDATTN_HD int lens() const { return prefix() + align_up((num_seqs + 1) * 4, 128); }
+  PAGEDATTN_HD int lens() const {
+    return prefix() + align_up((walks * num_seqs + 1) * 4, 128);  // page prefix of each pass
+  }
   PAGEDATTN_HD int qo() const { return align_up(lens() + num_seqs * 4, 16); }
   PAGEDATTN_HD int total() const { return qo() + qo_entries * 4; }
 };

@@ -33,8 +33,9 @@ void run() {
   for (int st = 4; st <= 16; ++st)
     for (int G = 1; G <= 16; ++G)
       for (int n : ns)
-      for (int qo : {0, n + 1}) {
-        const L l{st, G, n, qo};
+      for (int qo : {0, n + 1})
+      for (int walks : {1, 3}) {
+        const L l{st, G, n, qo, walks};
         CHECK(l.bars() % 1024 == 0, "bars D%d BS%d st%d\n", D, BS, st);
         CHECK(L::kStageBytes % 1024 == 0, "stage size D%d BS%d\n", D, BS);
         CHECK(l.merge_m() >= l.bars() + (2 * st + 1) * 8, "barrier overlap\n");
@@ -58,7 +59,7 @@ void run() {
         CHECK(l.q_slot_bytes() % 128 == 0, "q slot\n");
         CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
-        CHECK(l.lens() - l.prefix() >= (n + 1) * 4, "prefix size\n");
+        CHECK(l.lens() - l.prefix() >= (walks * n + 1) * 4, "prefix size\n");
         CHECK(l.qo() - l.lens() >= n * 4, "lens size\n");
         CHECK(l.qo() % 16 == 0, "qo alignment\n");
         CHECK(l.total() - l.qo() >= qo * 4, "qo size\n");
