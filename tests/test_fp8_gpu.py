@@ -95,3 +95,10 @@ def test_fp8_rejects_head_dim_64():
     with pytest.raises(pa.PagedAttnError) as e:
         run_fp8(f)
     assert e.value.status == -3
+
+
+def test_fp8_more_sequences_than_one_launch_holds():
+    lens = list(np.random.default_rng(14).integers(1, 70, size=5000))
+    sp = workloads.custom_spec("wide", len(lens), 4, 1, 128, 16, lens, max_len=80)
+    f = workloads.to_fp8(workloads.make(sp, seed=14, device="cuda", poison="nan"))
+    assert_parity(run_fp8(f), reference(f), "5000 sequences")

@@ -122,3 +122,13 @@ def test_multi_rejects_bad_arguments():
     assert lib.paged_attn_decode_multi(*args, 0, *tail) == -5          # max_q_len < 1
     assert lib.paged_attn_decode_multi(*args, 200, *tail) == -5        # q_len * G > 256
     assert lib.paged_attn_decode_multi(*(args[:4] + [0] + args[5:]), 2, *tail) == -1
+
+
+def test_multi_more_sequences_than_one_launch_holds():
+    """5,000 sequences (more than one launch takes), two row chunks per KV head."""
+    lens = list(np.random.default_rng(12).integers(1, 70, size=5000))
+    sp = workloads.custom_spec("wide", len(lens), 8, 1, 64, 16, lens, max_len=80)
+    w = workloads.make(sp, seed=12, device="cuda", poison="nan")
+    qlens = [int(min(3, L)) for L in lens]
+    q, qo = queries(w, qlens, 13)
+    assert_parity(run_multi(w, q, qo, 3), reference(w, q, qo), "5000 sequences")

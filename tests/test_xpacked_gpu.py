@@ -93,3 +93,11 @@ def test_xpacked_rejects_bad_arguments():
                                        x.q.data_ptr(), x.block_tables.data_ptr(),
                                        x.seq_lens.data_ptr(), 2, 4, 2, 96, 7, 16, 0.125, 0)
     assert rc == -3  # head_dim
+
+
+def test_xpacked_more_sequences_than_one_launch_holds():
+    lens = list(np.random.default_rng(15).integers(1, 70, size=5000))
+    sp = workloads.custom_spec("wide", len(lens), 4, 1, 64, 32, lens, max_len=96)
+    w = workloads.make(sp, seed=15, device="cuda", poison="nan")
+    x = workloads.to_xpacked(w)
+    assert_parity(run_xp(x), reference(x), "5000 sequences")
