@@ -519,21 +519,27 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     }
     cp_async_commit();
   };
-  // FP8: the slot's bf16 query tile (swizzled, as prefetched) -> f16 rows in
+  // FP8: the slot's bf16 query rows (swizzled, as prefetched) -> f16 rows in
   // natural order, padded (kQ16Stride) so the page loop's 8-byte reads of four
-  // rows x four lanes fall in distinct banks.
-  auto convert_q = [&](int buf) {
+  // rows x four lanes fall in distinct banks.  Each thread converts the 16-byte
+  // chunks it copied itself (the same index walk as prefetch_q), which its own
+  // cp.async.wait_all has made visible to it, so no barrier is needed between
+  // the copies landing and the conversion; the barrier after it publishes the
+  // f16 rows.
+  auto convert_own_q = [&](int buf) {
     const uint8_t* tile = sm_q + buf * kQSlotBytes;
     uint8_t* q16 = sm_q + buf * kQSlotBytes + kQTileBytes;
-    for (int i = ctid; i < kQRows * (D / 2); i += kConsumerThreads) {
-      const int h = i / (D / 2);
-      const int d = 2 * (i - h * (D / 2));
-      const int c = d / 8;
+    for (int i = ctid; i < kQRows * (D / 8); i += kConsumerThreads) {
+      const int h = i / (D / 8);
+      const int c = i - h * (D / 8);
       const int pc = (c & ~7) | ((c & 7) ^ (h & 7));
-      const uint32_t v =
-          *reinterpret_cast<const uint32_t*>(tile + h * (D * 2) + pc * 16 + (d % 8) * 2);
-      *reinterpret_cast<uint32_t*>(q16 + h * kQ16Stride + d * 2) =
-          pack_f16x2(bf16lo_to_f32(v), bf16hi_to_f32(v));
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + h * (D * 2) + pc * 16);
+      uint4 o;
+      o.x = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
+      o.y = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+      o.z = pack_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z));
+      o.w = pack_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+      *reinterpret_cast<uint4*>(q16 + h * kQ16Stride + c * 16) = o;
     }
   };
   int lim[kNH][2];  // last token each of this lane's query columns may see
@@ -1176,14 +1182,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   prefetch_q(0, wk.s, wk.g);
   ahead = next_piece(ahead);
   cp_async_wait_all();
+  if constexpr (FP8) convert_own_q(0);
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);
   if (ahead.s < NW && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
-  if constexpr (FP8) {
-    convert_q(0);
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-  }
   reset();
   set_limits(wk.s, wk.g);
   // Ring ownership: unit i of the range (i = u - u0) sits in slot i % stages,
@@ -1321,9 +1323,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       merge_warps(nullptr, nullptr);
       emit(s, g, split ? p.partials + (size_t)my_slot(sb) * R * kPartialRow : nullptr);
       // The next piece's query group was prefetched into the other tile: make
-      // every thread's copies visible, then prefetch the piece after it into
-      // the tile just freed.
+      // every thread's copies visible (FP8: after converting its own to f16),
+      // then prefetch the piece after it into the tile just freed.
       cp_async_wait_all();
+      if constexpr (FP8) convert_own_q(qbuf ^ 1);
       __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
       if (ctid == 0 && split)
@@ -1331,11 +1334,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       qbuf ^= 1;
       ahead = next_piece(ahead);
       if (ahead.s < NW && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
-      if constexpr (FP8) {
-        convert_q(qbuf);
-        __syncwarp();
-        named_barrier(kConsumerBarrier, kConsumerThreads);
-      }
       reset();
       set_limits(wk.s, wk.g);
       continue;
