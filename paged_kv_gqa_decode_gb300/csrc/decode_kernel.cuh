@@ -228,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   uint64_t* comb_bar = empty_bar + p.stages;  // the combine's partial-state copies
   float* sm_m = reinterpret_cast<float*>(smem + lay.merge_m());
   float* sm_l = reinterpret_cast<float*>(smem + lay.merge_l());
-  float* sm_final = reinterpret_cast<float*>(smem + lay.final_ml());  // [0,16) M, [16,32) L
   int* sm_flag = reinterpret_cast<int*>(smem + lay.flag());
   float* sm_o = reinterpret_cast<float*>(smem + lay.merge_o());
   uint8_t* sm_q = smem + lay.qtile();
@@ -1033,11 +1032,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   };
 
   // Merge the four consumer warps' states of a piece through shared memory
-  // (BI-V100 design, section 2, Level 2): afterwards sm_final holds each head's
-  // (M, L) and sm_o each warp's o rescaled to M.  When `arrive` is given,
-  // thread 0 arrives on that split counter (a relaxed add: nothing is published
-  // yet) as soon as every warp is done with the piece's pages, so the add's
-  // round trip overlaps the merge; its old value lands in *old.
+  // (BI-V100 design, section 2, Level 2), with one barrier: every warp stores
+  // its (m, l) per head and its unscaled o; emit() then combines the four per
+  // output element.  When `arrive` is given, thread 0 arrives on that split
+  // counter (a relaxed add: nothing is published yet) as soon as every warp is
+  // done with the piece's pages; its old value lands in *old.
   auto merge_warps = [&](int* arrive, int* old) {
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh)
@@ -1059,30 +1058,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
           sm_l[warp * 16 + h] = l_run[nh][e];
         }
     }
-    __syncwarp();
-    named_barrier(kConsumerBarrier, kConsumerThreads);
-    if (arrive != nullptr && ctid == 0) *old = atomicAdd(arrive, 1);
-    float f[kNH][2];
-#pragma unroll
-    for (int nh = 0; nh < kNH; ++nh)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int h = 8 * nh + 2 * quad + e;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 16 + h]);
-        float Lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = sm_m[w * 16 + h];
-          if (mw != -INFINITY) Lsum += sm_l[w * 16 + h] * fast_exp2(mw - M);
-        }
-        f[nh][e] = m_run[nh][e] == -INFINITY ? 0.f : fast_exp2(m_run[nh][e] - M);
-        if (warp == 0 && row == 0) {
-          sm_final[h] = M;
-          sm_final[16 + h] = Lsum;
-        }
-      }
 #pragma unroll
     for (int dt = 0; dt < kDT; ++dt)
 #pragma unroll
@@ -1091,32 +1066,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         for (int e = 0; e < 4; ++e) {
           const int h = 8 * nh + 2 * quad + (e & 1);
           const int d = acc_col(dt, e);
-          if (h < R) sm_o[(warp * R + h) * kRowStride + d] = o_acc[dt][nh][e] * f[nh][e & 1];
+          if (h < R) sm_o[(warp * R + h) * kRowStride + d] = o_acc[dt][nh][e];
         }
     __syncwarp();
     named_barrier(kConsumerBarrier, kConsumerThreads);
+    if (arrive != nullptr && ctid == 0) *old = atomicAdd(arrive, 1);
   };
 
-  // Sum the warps' rescaled o and write the piece's merged state: normalised
+  // Combine the warps' states and write the piece's merged state: normalised
   // bf16 rows of (s, g) (whole piece), or a partial row set [M, L, -, -, o]
-  // at `dst` (a workspace slot, or part 0 of the ring).
+  // at `dst` (a workspace slot, or part 0 of the ring).  Per row: M = max of
+  // the warps' m, each warp's weight 2^(m_w - M) (0 for a warp that saw no
+  // token), L and o the weighted sums in warp order.
   auto emit = [&](int s, int g, float* dst) {
     for (int i = ctid; i < R * (D / 4); i += kConsumerThreads) {
       const int r = i / (D / 4);
       const int d = 4 * (i - r * (D / 4));
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 16 + r]);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = sm_m[w * 16 + r];
+        const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+        if (mw != -INFINITY) lsum += sm_l[w * 16 + r] * f;
         const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * R + r) * kRowStride + d);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+        acc.x += v.x * f;
+        acc.y += v.y * f;
+        acc.z += v.z * f;
+        acc.w += v.w * f;
       }
       if (dst == nullptr) {
         const long long qr = qrow(s, g, r);
         if (qr < 0) continue;
-        const float lsum = sm_final[16 + r];
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // a row that saw no token: 0
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -1125,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       } else {
         float* prow = dst + r * kPartialRow;
         *reinterpret_cast<float4*>(prow + 4 + d) = acc;
-        if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(sm_final[r], sm_final[16 + r]);
+        if (d == 0) *reinterpret_cast<float2*>(prow) = make_float2(M, lsum);
       }
     }
   };
