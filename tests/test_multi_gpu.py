@@ -132,3 +132,23 @@ def test_multi_more_sequences_than_one_launch_holds():
     qlens = [int(min(3, L)) for L in lens]
     q, qo = queries(w, qlens, 13)
     assert_parity(run_multi(w, q, qo, 3), reference(w, q, qo), "5000 sequences")
+
+
+def test_queries_that_see_no_token_are_zero():
+    """q_len > seq_len: the first q_len - L queries of that sequence see no token
+    (zero rows); the others are the decode of the sequence cut at L - q_len + i + 1."""
+    sp = workloads.custom_spec("short", 3, 8, 2, 128, 16, [3, 40, 17], max_len=64)
+    w = workloads.make(sp, seed=16, device="cuda", poison="nan")
+    qlens = [5, 2, 1]  # sequence 0: queries 0 and 1 see nothing
+    q, qo = queries(w, qlens, 17)
+    out = run_multi(w, q, qo, 5)
+    assert torch.count_nonzero(out[0:2]).item() == 0
+    rows_s = np.repeat(np.arange(3), qlens)
+    rows_i = np.concatenate([np.arange(n) for n in qlens])
+    lens = np.array(w.lens_list)[rows_s]
+    cut = lens - (np.array(qlens)[rows_s] - rows_i - 1)
+    keep = cut > 0
+    single = oracle.Inputs(q.cpu()[keep], w.k_cache.cpu(), w.v_cache.cpu(),
+                           w.block_tables.cpu()[rows_s[keep]], torch.tensor(cut[keep], dtype=torch.int32),
+                           w.scale)
+    assert_parity(out[torch.tensor(keep)], oracle.decode(single), "visible rows")
