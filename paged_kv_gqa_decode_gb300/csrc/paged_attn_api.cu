@@ -20,8 +20,8 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr size_t kWsAlign = 256;
-constexpr int kAppendApartPieces = 4;
-constexpr int kMaxMultiRows = 256;  // multi-token decode: max q_len * G (16 pieces of 16 rows)  // (s, g) pieces per CTA from which the append runs apart
+constexpr int kAppendApartPieces = 4;  // (s, g) pieces per CTA from which the append runs apart
+constexpr int kMaxMultiRows = 256;      // multi-token decode: max q_len * G (16 pieces of 16 rows)
 constexpr long long kRingBytesPerSm = 128 << 10;            // K/V rings of one SM, few pieces per CTA
 constexpr long long kRingBytesPerSmManyPieces = 160 << 10;  // ... two or more pieces per CTA
 
