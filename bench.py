@@ -167,7 +167,9 @@ class ClockSampler:
 # ------------------------------------------------------------------ oracle timing
 
 def oracle_sample_run(w_host, spec, groups, threads):
-    """Run the FP64 oracle on the listed (s, g) groups; returns (seconds, bytes)."""
+    """Run the FP64 oracle on the listed (s, g) groups; returns (seconds, bytes, flops).
+
+    flops: 4 D per token and query head (q.K and p.V, a multiply and an add each)."""
     import oracle
 
     inp = oracle.Inputs.from_workload(w_host)
@@ -176,7 +178,8 @@ def oracle_sample_run(w_host, spec, groups, threads):
     t = time.perf_counter()
     oracle.decode(inp, pairs=pairs, num_threads=threads)
     dt = time.perf_counter() - t
-    return dt, sum(group_bytes(spec, lens[s]) for s, _ in groups)
+    flops = sum(lens[s] * spec.G * 4 * spec.D for s, _ in groups)
+    return dt, sum(group_bytes(spec, lens[s]) for s, _ in groups), flops
 
 
 def all_groups(spec, lens):
@@ -187,16 +190,17 @@ def oracle_baseline(w_host, spec, budget_s: float, threads: int):
     """Time the oracle on whole groups in round-robin order for about budget_s seconds."""
     lens = w_host.lens_list
     groups = all_groups(spec, lens)
-    done, secs, nbytes, i = 0, 0.0, 0, 0
+    done, secs, nbytes, nflops, i = 0, 0.0, 0, 0, 0
     batch = max(1, min(len(groups), 4 * threads))
     while secs < budget_s and done < 10**7:
         chunk = [groups[(i + k) % len(groups)] for k in range(batch)]
         i += batch
-        dt, b = oracle_sample_run(w_host, spec, chunk, threads)
+        dt, b, f = oracle_sample_run(w_host, spec, chunk, threads)
         secs += dt
         nbytes += b
+        nflops += f
         done += batch
-    return secs, nbytes, done, len(groups)
+    return secs, nbytes, done, len(groups), nflops
 
 
 # ------------------------------------------------------------------ arms
@@ -475,13 +479,14 @@ def run_ours(args, world, rank, local):
         if not args.no_cpu_baseline and args.kv == "bf16" and qlen == 1:  # the baseline leg times the bf16 oracle
             w_host = workloads.host_copy(w)
             threads = len(os.sched_getaffinity(0))
-            secs, b, ngroups, total_groups = oracle_baseline(w_host, spec, args.cpu_budget,
-                                                             threads)
+            secs, b, ngroups, total_groups, nflops = oracle_baseline(w_host, spec,
+                                                                     args.cpu_budget, threads)
             cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
                    "kind": "oracle",
                    "sample": f"{ngroups} (sequence, KV head) groups of the {args.config} "
                              f"workload ({total_groups} per step), round-robin, "
-                             f"{secs:.1f} s of FP64 CPU work"}
+                             f"{secs:.1f} s of FP64 CPU work",
+                   "gflop_per_s": round(nflops / secs / 1e9, 3)}
         result = {
             "metric": METRIC,
             "value": round(world * nbytes["total"] / per_step / 1e9, 2),
@@ -552,7 +557,7 @@ def run_reference(args, world, rank):
     budget_total = args.reference_budget
     # size each step so warmup + steps stay within the budget
     per_step_budget = budget_total / max(1, steps + args.warmup)
-    dt1, _ = oracle_sample_run(w, spec, groups[:threads], threads)
+    dt1, _, _ = oracle_sample_run(w, spec, groups[:threads], threads)
     per_group = dt1 / max(1, min(threads, len(groups)))
     per_step_groups = int(max(1, min(len(groups), per_step_budget / max(per_group, 1e-9))))
     i = 0
@@ -567,10 +572,12 @@ def run_reference(args, world, rank):
         step()
     secs = 0.0
     nbytes = 0
+    nflops = 0
     for _ in range(steps):
-        dt, b = step()
+        dt, b, f = step()
         secs += dt
         nbytes += b
+        nflops += f
     value = nbytes / secs / 1e9
     return {
         "impl": "reference",
@@ -582,7 +589,8 @@ def run_reference(args, world, rank):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{per_step_groups} of {len(groups)} (sequence, KV head) "
-                                   "groups per step, round-robin"},
+                                   "groups per step, round-robin",
+                         "gflop_per_s": round(nflops / secs / 1e9, 3)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

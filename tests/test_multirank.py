@@ -78,4 +78,8 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = lines[0]
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the oracle's flop rate: 4 D flops per token and query head against at least
+    # 4 D bytes of K and V per token and KV head, so at most G = 2 flops per byte
+    cb = line["cpu_baseline"]
+    assert 0 < cb["gflop_per_s"] <= 2 * cb["value"] * 1.001
     assert line["e2e"]["h2d_bytes_per_step"] == 0
