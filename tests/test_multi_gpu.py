@@ -152,3 +152,14 @@ def test_queries_that_see_no_token_are_zero():
                            w.block_tables.cpu()[rows_s[keep]], torch.tensor(cut[keep], dtype=torch.int32),
                            w.scale)
     assert_parity(out[torch.tensor(keep)], oracle.decode(single), "visible rows")
+
+
+def test_multi_largest_row_count():
+    """q_len 64 with G = 4: 256 query rows per KV head, the most one call takes
+    (16 pieces of 16 rows, each KV head's pages walked 16 times)."""
+    lens = [64, 700, 2000, 90]
+    sp = workloads.custom_spec("maxrows", len(lens), 8, 2, 128, 16, lens, max_len=2048)
+    w = workloads.make(sp, seed=21, device="cuda", poison="nan")
+    qlens = [64, 64, 33, 64]
+    q, qo = queries(w, qlens, 22)
+    assert_parity(run_multi(w, q, qo, 64), reference(w, q, qo), "256 rows")

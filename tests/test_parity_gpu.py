@@ -87,6 +87,45 @@ def test_shapes_and_ragged_tails(D, BS, H_q, H_kv):
     assert torch.count_nonzero(out[0]).item() == 0
 
 
+def test_one_token_returns_its_v_row_exactly():
+    """L = 1: the softmax weight is exactly 1, so out is the token's V row, bit for bit."""
+    sp = workloads.custom_spec("one_tok", 40, 8, 2, 128, 16, [1] * 40, max_len=32)
+    w = workloads.make(sp, seed=31, device="cuda", poison="nan")
+    out = run_gpu(w)
+    G = sp.H_q // sp.H_kv
+    blocks = w.block_tables[:, 0].long()
+    for h in range(sp.H_q):
+        v0 = w.v_cache[blocks, h // G, 0, :]  # [num_seqs, D]
+        assert torch.equal(out[:, h].view(torch.int16), v0.view(torch.int16)), f"head {h}"
+
+
+def test_zero_scale_gives_the_mean_of_v():
+    """scale = 0: every visible token weighs the same, out = mean of the V rows."""
+    lens = [1, 7, 16, 33, 300, 1000]
+    sp = workloads.custom_spec("mean", len(lens), 8, 2, 128, 16, lens, max_len=1024)
+    w = workloads.make(sp, seed=32, device="cuda", poison="nan")
+    out = pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, 0.0)
+    torch.cuda.synchronize()
+    G = sp.H_q // sp.H_kv
+    bs = sp.block_size
+    ref = np.zeros((len(lens), sp.H_q, sp.D))
+    vc = w.v_cache.double().cpu()
+    bt = w.block_tables.cpu()
+    for s, L in enumerate(lens):
+        t = torch.arange(L)
+        for g in range(sp.H_kv):
+            rows = vc[bt[s, t // bs].long(), g, t % bs, :]
+            ref[s, g * G:(g + 1) * G, :] = rows.mean(dim=0).numpy()
+    assert_parity(out, ref, "scale 0")
+
+
+def test_one_million_token_sequence():
+    """One sequence of 2^20 tokens (65,536 pages of one KV head) split over every CTA."""
+    sp = workloads.custom_spec("1m", 1, 4, 1, 64, 16, [1 << 20])
+    w = workloads.make(sp, seed=33, device="cuda", poison="none")
+    assert_parity(run_gpu(w), reference(w), "2^20 tokens")
+
+
 def test_single_long_sequence_splits_across_all_ctas():
     sp = workloads.custom_spec("one", 1, 8, 1, 128, 16, [60000])
     w = workloads.make(sp, seed=3, device="cuda")
