@@ -349,31 +349,29 @@ def run_ours(args, world, rank, local):
     clocks = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     time.sleep(0.3 if clocks else 0)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    # per-launch event pairs on the launching stream (for the kernel's own duration)
-    n_pairs = min(steps, 2000)
-    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n_pairs)]
-    pair_every = max(1, steps // n_pairs)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.monotonic()
     ev[0].record(stream)
-    j = 0
     for i in range(steps):
-        timed = i % pair_every == 0 and j < n_pairs
-        if timed:
-            k_ev[j][0].record(stream)
         step(i)
-        if timed:
-            k_ev[j][1].record(stream)
-            j += 1
     ev[1].record(stream)
     torch.cuda.synchronize()
     t1 = time.monotonic()
     barrier(world)
     elapsed = ev[0].elapsed_time(ev[1]) / 1e3
     elapsed = reduce_max(elapsed, world)
-    kernel_s = sum(a.elapsed_time(b) for a, b in k_ev[:j]) / max(1, j) / 1e3
+    # after the timed region: event pairs around single launches on the launching
+    # stream (each pair holds one step alone: no overlap with its neighbours)
+    j = min(steps, 2000)
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(j)]
+    for i in range(j):
+        k_ev[i][0].record(stream)
+        step(i)
+        k_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    kernel_s = sum(a.elapsed_time(b) for a, b in k_ev) / max(1, j) / 1e3
     clock_info = None
     if clocks:
         clocks.stop()
@@ -386,9 +384,10 @@ def run_ours(args, world, rank, local):
     # memory.  The copies run on two copy streams with double-buffered device
     # inputs and outputs, so step i + 1's inputs go up and step i - 1's result
     # comes down while step i computes (events order each buffer's reuse).
-    # Groups of 8 steps are captured once in a CUDA graph and replayed, so the
-    # host's per-step launch cost stays off the GPU's critical path; the timed
-    # region ends when the last result is on the host.
+    # Groups of 32 steps are captured once in a CUDA graph and replayed, so the
+    # host's per-step launch cost stays off the GPU's critical path (the pipeline
+    # fills and drains once per group); the timed region ends when the last
+    # result is on the host.
     host_q = q_in.cpu().pin_memory()
     host_bt = w.block_tables.cpu().pin_memory()
     host_sl = w.seq_lens.cpu().pin_memory()
@@ -406,7 +405,7 @@ def run_ours(args, world, rank, local):
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer uploaded
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step using the buffer computed
     ev_out = [torch.cuda.Event() for _ in range(2)]   # its result downloaded
-    per_graph = 8
+    per_graph = 32
 
     def e2e_group(cs):
         """per_graph steps issued on compute stream cs, the copy streams forked from
@@ -472,7 +471,15 @@ def run_ours(args, world, rank, local):
     result = None
     if rank == 0:
         peak, peak_src = measured_peaks()
-        achieved = nbytes["total"] / kernel_s / 1e9
+        # The kernel's average launch duration: with one launch per step, the
+        # timed region's events over its launches (back-to-back launches overlap
+        # one's prologue with the previous one's tail, as in a decode loop);
+        # otherwise the event pairs around single launches.  The pairs break that
+        # overlap and add the launch latency, so their figure is reported beside
+        # it as the isolated duration.
+        single = launches_per_step == 1
+        launch_s = per_step if single else kernel_s
+        achieved = nbytes["total"] / launch_s / 1e9
         plain = op == "decode" and args.kv == "bf16" and qlen == 1
         traffic = profile_traffic(args.config) if plain else None
         cpu = None
@@ -529,8 +536,13 @@ def run_ours(args, world, rank, local):
                                             "(one launch per step)",
                            "append_then_decode": "paged_kv_append_kernel + paged_decode_kernel "
                                                  "(two launches per step)"}[op],
-                "kernel_us": round(kernel_s * 1e6, 2),
-                "timing": f"CUDA events around {j} of the {steps} timed launches",
+                "kernel_us": round(launch_s * 1e6, 2),
+                "kernel_us_isolated": round(kernel_s * 1e6, 2),
+                "frac_isolated": round(nbytes["total"] / kernel_s / 1e9 / peak, 4),
+                "timing": (f"CUDA events over the timed region on the launching stream, "
+                           f"{steps} launches" if single else
+                           f"CUDA events around {j} of the {steps} timed launches") +
+                          f"; isolated: event pairs around {j} single launches after it",
             },
             "e2e": {"value": round(world * nbytes["total"] / e2e_time / 1e9, 2), "unit": "GB/s",
                     "us_per_step": round(e2e_time * 1e6, 2), "mode": e2e_mode,
