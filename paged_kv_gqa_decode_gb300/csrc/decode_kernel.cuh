@@ -747,11 +747,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // caller, so the V operand needs no mask.
   struct Tile8 {
     uint32_t k, v;        // shared-memory address of the tile's first K / V row
-    const float* ks;      // its 16 K row floats
-    const float* vs;      // its 16 V row floats
+    uint32_t ks, vs;      // shared-memory address of its 16 K / V row floats
     int valid;            // tokens of the tile inside the sequence (0..16)
   };
-  auto process_fp8 = [&](auto nt, const Tile8* tl, const uint8_t* q16) {
+  auto process_fp8 = [&](auto nt, const Tile8* tl, uint32_t q16) {
     constexpr int NT = decltype(nt)::value;
     const int li = lane >> 3;
     float s_acc[NT][kNH][4], s_odd[NT][kNH][4];
@@ -769,8 +768,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int nh = 0; nh < kNH; ++nh) {
-          const uint2 b = *reinterpret_cast<const uint2*>(
-              q16 + (8 * nh + row) * kQ16Stride + (16 * (2 * kk2 + x) + 4 * quad) * 2);
+          const uint2 b = lds_u32x2(
+              q16 + (uint32_t)((8 * nh + row) * kQ16Stride + (16 * (2 * kk2 + x) + 4 * quad) * 2));
           qf[x][nh][0] = b.x;
           qf[x][nh][1] = b.y;
         }
@@ -800,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
 #pragma unroll
     for (int tg = 0; tg < NT; ++tg) {
       const int valid = tl[tg].valid;
-      const float k_lo = p.scale_log2 * tl[tg].ks[row], k_hi = p.scale_log2 * tl[tg].ks[row + 8];
+      const float k_lo = p.scale_log2 * lds_f32(tl[tg].ks + 4 * row);
+      const float k_hi = p.scale_log2 * lds_f32(tl[tg].ks + 4 * (row + 8));
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
@@ -834,8 +834,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
 #pragma unroll
     for (int tg = 0; tg < NT; ++tg) {
       const int valid = tl[tg].valid;
-      const float v_lo = row < valid ? tl[tg].vs[row] : 0.f;  // masked rows may hold NaN floats
-      const float v_hi = row + 8 < valid ? tl[tg].vs[row + 8] : 0.f;
+      // masked rows may hold NaN floats
+      const float v_lo = row < valid ? lds_f32(tl[tg].vs + 4 * row) : 0.f;
+      const float v_hi = row + 8 < valid ? lds_f32(tl[tg].vs + 4 * (row + 8)) : 0.f;
 #pragma unroll
       for (int nh = 0; nh < kNH; ++nh) {
         const float e0 = fast_exp2(s_acc[tg][nh][0] - m_run[nh][0]);
@@ -1197,6 +1198,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   for (;;) {
     const int s = wk.s, g = wk.g, n = wk.n, p0 = wk.p;
     const int sq = multi && QC > 1 ? s % N : s;  // the walked sequence's sequence
+    const int len = sm_len[sq];  // read once per piece (the page waits below clobber memory)
     const long long ib = min(n_units, ia + (n - p0));  // one past its last unit here
     while (own_i < ib) {
       const int pg = p0 + (int)(own_i - ia);  // page of the sequence
@@ -1207,7 +1209,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             abort = true;
           } else {
-            const int valid = min(BS, sm_len[sq] - pg * BS);
+            const int valid = min(BS, len - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
             // Only the piece's last page can end early: zero its V rows past
             // the sequence (they may hold anything) so the V operand needs no mask.
@@ -1222,15 +1224,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
               }
               __syncwarp();
             }
-            const float* sc = sm_scales + (size_t)own_slot * 2 * BS;
-            const uint8_t* q16 = sm_q + qbuf * kQSlotBytes + kQTileBytes;
+            const uint32_t sc = smem_addr(sm_scales + (size_t)own_slot * 2 * BS);
+            const uint32_t q16 = smem_addr(sm_q + qbuf * kQSlotBytes + kQTileBytes);
             const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
             if constexpr (BS == 16) {
-              const Tile8 t[1] = {{k0, v0, sc, sc + BS, valid}};
+              const Tile8 t[1] = {{k0, v0, sc, sc + 4 * BS, valid}};
               process_fp8(std::integral_constant<int, 1>(), t, q16);
             } else {  // the two 16-token halves of a 32-token page
-              const Tile8 t[2] = {{k0, v0, sc, sc + BS, min(16, valid)},
-                                  {k0 + 16 * 128, v0 + 16 * 128, sc + 16, sc + BS + 16,
+              const Tile8 t[2] = {{k0, v0, sc, sc + 4 * BS, min(16, valid)},
+                                  {k0 + 16 * 128, v0 + 16 * 128, sc + 4 * 16, sc + 4 * (BS + 16),
                                    max(0, valid - 16)}};
               process_fp8(std::integral_constant<int, 2>(), t, q16);
             }
@@ -1257,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             abort = true;
           } else {
-            const int valid = min(BS, sm_len[sq] - pg * BS);
+            const int valid = min(BS, len - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
             const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
             if (patch) {
