@@ -34,6 +34,11 @@ def test_bench_prints_one_contract_line(extra):
     rl = d["roofline"]
     assert rl["bound"] == "hbm" and rl["unit"] == "GB/s" and rl["peak"] > 0
     assert abs(rl["frac"] - rl["achieved"] / rl["peak"]) < 1e-3
+    # one launch per step: the kernel's average launch duration is the step time,
+    # so achieved equals the headline value; single launches timed alone take longer
+    assert abs(rl["achieved"] - d["value"]) <= 1e-3 * d["value"]
+    assert abs(rl["kernel_us"] - d["us_per_step"]) <= 0.02
+    assert 0 < rl["frac_isolated"] <= rl["frac"] * 1.02
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] >= 20
