@@ -11,7 +11,12 @@ imports this package, and this package imports nothing from it.
 * ``append``       -- the cache write of each sequence's new token (the step
                       before the decode).
 * ``decode_fp8``   -- the definition over FP8 caches (e4m3 bytes and a dequant
-                      float per cache row).
+                      float per cache row); ``e4m3_table`` decodes the 256
+                      byte values from the format's bit fields.
+* ``decode_xpacked`` -- the definition over x-packed K ([blocks, H_kv, D/8,
+                      BS, 8]) and D-major V ([blocks, H_kv, D, BS]) caches.
+* ``decode_multi`` -- several causal query tokens per sequence (rows through
+                      ``qo_indptr``); query i of q_len sees t <= L - q_len + i.
 * ``combine`` / ``finish`` -- the merge of two partial softmax states and the
                       final normalisation, as "Paged Attention Kernel
                       Architecture for BI-V100" (section 2, Level 1: the
@@ -22,6 +27,10 @@ imports this package, and this package imports nothing from it.
 Pins (tests/test_oracle_pins.py) tie the oracle to a library routine
 (torch's float64 scaled_dot_product_attention on the un-paged layout), closed
 forms, invariances and a hand-derived golden example.
+
+Parity unpinned: the zero row for a sequence with no tokens (L = 0), and for a
+multi-token query that sees no token.  No page defines an empty softmax; the
+oracle and the kernels implement the same reading.
 """
 from __future__ import annotations
 

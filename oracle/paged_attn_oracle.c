@@ -32,7 +32,8 @@
  *   Every bf16 input is widened exactly to double; all arithmetic is double;
  *   scale is the float the caller passes, widened to double.  L = 0 gives a
  *   zero row (the pages never define an empty softmax; this is the reading
- *   the library documents).
+ *   the library documents), and so does a multi-token query that sees no
+ *   token: parity unpinned for both (no page fixes the value).
  *
  *   FP8 caches (the nvfp4-megamoe README, "Stage D: FP8 Paged KV Gather" and
  *   "FP8 KV Quantize/Dequant": e4m3 values with a dequant scale per position)
