@@ -376,71 +376,65 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       // physical block and KV head of this lane's unit (block -1 past the range)
       if (u >= u1) return make_int2(-1, 0);
       const int sq = multi && QC > 1 ? wk.s % N : wk.s;  // the walked sequence's sequence
-      return make_int2(__ldg(p.block_tables + (size_t)sq * p.maxb + wk.p), wk.g);
+      int pb = __ldg(p.block_tables + (size_t)sq * p.maxb + wk.p);
+      if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
+        atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
+      return make_int2(pb, wk.g);
     };
     int2 cur = fetch(u0 + lane);
     bool abort = false;
-    // One wave: lanes 0 .. issue_lanes - 1 issue units ub + j0 + lane of the batch
-    // whose block ids `cur` holds; returns whether any lane gave up waiting.
-    auto wave = [&](long long ub, int j0, int cnt, int2 cur) -> bool {
-      const int j = j0 + (lane < issue_lanes ? lane : 0);
-      const int pb = __shfl_sync(0xffffffffu, cur.x, j);
-      const int g = __shfl_sync(0xffffffffu, cur.y, j);
-      bool bad = false;
-      if (lane < issue_lanes && j0 + lane < cnt) {
-        if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
-          atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
-        const long long i = ub - u0 + j;  // unit index within this CTA
-        const int stage = (int)(i % p.stages);
-        const uint32_t phase = (uint32_t)((i / p.stages) & 1);
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
-          atomicOr(p.status, kStatusTimeout);
-          bad = true;
-        } else {
-          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
-          uint8_t* st = smem + stage * kStageBytes;
-          if constexpr (XP) {
-            // a page of one KV head is contiguous in both x-packed caches: K
-            // (and V of 16-token pages) come as one bulk copy each; V of 32-token
-            // pages through the tensor map, for the 64-byte swizzle (unswizzled
-            // 64-byte rows would cost 4-way bank conflicts in the V reads)
-            const size_t off = ((size_t)(pb < 0 ? 0 : pb) * H_kv + g) * (size_t)(D * BS);
-            bulk_load(st, p.k_cache + off, kPageBytes, &full_bar[stage]);
-            if constexpr (BS == 16)
-              bulk_load(st + kPageBytes, p.v_cache + off, kPageBytes, &full_bar[stage]);
-            else
-              tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, 0, g, pb, policy);
-          } else {
-            tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
-            tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
-          }
-          if constexpr (FP8) {
-            // the page's K and V row floats (a block outside a checked pool reads
-            // block 0's: its rows are zero-filled by the tensor copy anyway)
-            const long long b =
-                pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
-            const size_t row = ((size_t)b * H_kv + g) * BS;
-            float* sc = sm_scales + (size_t)stage * 2 * BS;
-            bulk_load(sc, p.k_scale + row, BS * 4, &full_bar[stage]);
-            bulk_load(sc + BS, p.v_scale + row, BS * 4, &full_bar[stage]);
-          }
-        }
-      }
-      return __any_sync(0xffffffffu, bad);
-    };
     for (long long ub = u0; ub < u1 && !abort; ub += 32) {
-      const int cnt = (int)min(32LL, u1 - ub);
-      abort = wave(ub, 0, cnt, cur);
-      // After the batch's first wave: advance this lane's walker to its unit of
-      // the next batch and start that block-table read; nothing waits for it
-      // before the next batch.
+      // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
       if (ub + 32 + lane < u1) {
         wk.advance(32, sm_prefix, NW, H_kv);
         nxt = fetch(ub + 32 + lane);
       }
-      for (int j0 = issue_lanes; j0 < cnt && !abort; j0 += issue_lanes)
-        abort = wave(ub, j0, cnt, cur);
+      const int cnt = (int)min(32LL, u1 - ub);
+      for (int j0 = 0; j0 < cnt && !abort; j0 += issue_lanes) {
+        const int j = j0 + (lane < issue_lanes ? lane : 0);
+        const int pb = __shfl_sync(0xffffffffu, cur.x, j);
+        const int g = __shfl_sync(0xffffffffu, cur.y, j);
+        bool bad = false;
+        if (lane < issue_lanes && j0 + lane < cnt) {
+          const long long i = ub - u0 + j;  // unit index within this CTA
+          const int stage = (int)(i % p.stages);
+          const uint32_t phase = (uint32_t)((i / p.stages) & 1);
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
+            atomicOr(p.status, kStatusTimeout);
+            bad = true;
+          } else {
+            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
+            uint8_t* st = smem + stage * kStageBytes;
+            if constexpr (XP) {
+              // a page of one KV head is contiguous in both x-packed caches: K
+              // (and V of 16-token pages) come as one bulk copy each; V of 32-token
+              // pages through the tensor map, for the 64-byte swizzle (unswizzled
+              // 64-byte rows would cost 4-way bank conflicts in the V reads)
+              const size_t off = ((size_t)(pb < 0 ? 0 : pb) * H_kv + g) * (size_t)(D * BS);
+              bulk_load(st, p.k_cache + off, kPageBytes, &full_bar[stage]);
+              if constexpr (BS == 16)
+                bulk_load(st + kPageBytes, p.v_cache + off, kPageBytes, &full_bar[stage]);
+              else
+                tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, 0, g, pb, policy);
+            } else {
+              tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
+              tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
+            }
+            if constexpr (FP8) {
+              // the page's K and V row floats (a block outside a checked pool reads
+              // block 0's: its rows are zero-filled by the tensor copy anyway)
+              const long long b =
+                  pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
+              const size_t row = ((size_t)b * H_kv + g) * BS;
+              float* sc = sm_scales + (size_t)stage * 2 * BS;
+              bulk_load(sc, p.k_scale + row, BS * 4, &full_bar[stage]);
+              bulk_load(sc + BS, p.v_scale + row, BS * 4, &full_bar[stage]);
+            }
+          }
+        }
+        abort = __any_sync(0xffffffffu, bad);
+      }
       cur = nxt;
     }
     // Drain: no tensor copy issued by this CTA may still be in flight when it exits.
