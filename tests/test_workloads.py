@@ -62,3 +62,17 @@ def test_custom_spec_lengths():
     w = workloads.make(sp, seed=5)
     assert w.lens_list == [0, 1, 16, 17]
     assert w.max_blocks_per_seq == 2
+
+
+def test_roofline_bytes_of_the_tiny_case():
+    """The roofline numerator for the tiny case, worked by hand: 137 tokens x 2
+    KV heads x (K + V) x 64 x 2 bytes = 70,144 B; q and out 2 x 4 heads x 64 x 2 B
+    each = 2,048 B; ceil(37/16) + ceil(100/16) = 10 block-table entries = 40 B."""
+    import bench
+
+    sp = workloads.spec("tiny")
+    w = workloads.make("tiny", device="cpu")
+    b = bench.algorithmic_bytes(sp, w.lens_list)
+    assert b == {"kv": 70144, "q_out": 2048, "block_table": 40, "total": 72232}
+    # the per-(sequence, KV head) split the CPU baseline uses adds up to the same
+    assert sum(bench.group_bytes(sp, L) for L in w.lens_list for _ in range(sp.H_kv)) == 72232
