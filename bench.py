@@ -307,6 +307,12 @@ def run_ours(args, world, rank, local):
         nbytes["q_out"] = spec.num_seqs * qlen * spec.H_q * spec.D * 2 * 2
         nbytes["total"] = nbytes["kv"] + nbytes["q_out"] + nbytes["block_table"]
 
+    # Early prologue (include/paged_attn.h): in every op but the unfused append,
+    # the work ahead of a decode launch writes at most q and the new rows, never
+    # the caches, tables or lengths, so the producer may start before it ends.
+    early = op != "append_then_decode"
+    pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE if early else 0)
+
     def run_op(q, bt, sl, cache, kn, vn, out=out, st=None):
         st = stream if st is None else st
         kc, vc, ksc, vsc = cache
@@ -520,6 +526,9 @@ def run_ours(args, world, rank, local):
                 "l2": f"inputs larger than L2: {reps} KV-cache replicas rotated "
                       f"({reps * kv_bytes / 1e9:.2f} GB vs 129 MB L2)",
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                "launch": "early prologue (the producer starts before the previous launch "
+                          "ends; caches, tables and lengths are not written between steps)"
+                if early else "plain (an append kernel writes the cache before each decode)",
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

@@ -74,6 +74,10 @@ extern "C" {
 #define PAGED_ATTN_ERR_WORKSPACE (-7)  /* workspace pointer null/misaligned or smaller than required */
 #define PAGED_ATTN_ERR_SCALE (-8)      /* scale is not finite */
 #define PAGED_ATTN_ERR_STATIC_SCRATCH (-9) /* sizes exceed paged_attn_decode_static's scratch */
+#define PAGED_ATTN_ERR_FLAGS (-10)     /* unknown bits in paged_attn_set_launch_flags */
+
+/* Launch flags (paged_attn_set_launch_flags). */
+#define PAGED_ATTN_FLAG_EARLY_PROLOGUE 1
 
 /*
  * Decode attention (the operation above).
@@ -284,6 +288,27 @@ PAGED_ATTN_API int paged_attn_append_decode(const void* q, const void* k_new, co
 
 /* Human-readable text for a PAGED_ATTN_* code (static storage). */
 PAGED_ATTN_API const char* paged_attn_status_string(int status);
+
+/*
+ * Launch flags for the decode calls made afterwards from the calling host
+ * thread (all entry points; 0, the default, restores the plain behaviour).
+ * Returns PAGED_ATTN_ERR_FLAGS, and changes nothing, for unknown bits.
+ *
+ * PAGED_ATTN_FLAG_EARLY_PROLOGUE: every decode launch waits for the work
+ * ahead of it in the stream (programmatic dependent launch) before touching
+ * global memory.  With this flag the caller guarantees that this earlier work,
+ * which may still be running, writes none of k_cache, v_cache (and their row
+ * floats), block_tables, seq_lens or qo_indptr.  Only q, the new K/V rows of
+ * the fused append and the output may be written by it.  The kernel then
+ * scans the lengths, translates the first pages and starts their tensor
+ * copies while that work finishes.  It waits for it only before reading q or
+ * the new rows, and before writing the output or the workspace.  In a
+ * layer-by-layer decode loop the kernel just before attention typically
+ * writes q, and with paged_attn_append_decode the new K/V rows too, but not
+ * the caches, tables or lengths.  With the separate paged_kv_append just
+ * before, the flag must stay off.  Results are those of the plain launch.
+ */
+PAGED_ATTN_API int paged_attn_set_launch_flags(int flags);
 
 /* The last cudaError_t / CUresult value behind a PAGED_ATTN_ERR_CUDA on this thread. */
 PAGED_ATTN_API int paged_attn_last_cuda_error(void);

@@ -28,6 +28,8 @@ __all__ = [
     "paged_attn_decode_multi",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
+    "paged_attn_set_launch_flags",
+    "FLAG_EARLY_PROLOGUE",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -47,9 +49,13 @@ EXPORTED_SYMBOLS = (
     "paged_attn_decode_xpacked",
     "paged_attn_decode_multi",
     "paged_attn_status_string",
+    "paged_attn_set_launch_flags",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
 )
+
+# Launch flags (include/paged_attn.h).
+FLAG_EARLY_PROLOGUE = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -103,6 +109,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_last_cuda_error.restype = I
         lib.paged_attn_version.argtypes = []
         lib.paged_attn_version.restype = I
+        lib.paged_attn_set_launch_flags.argtypes = [I]
+        lib.paged_attn_set_launch_flags.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -110,6 +118,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
 
 def paged_attn_status_string(status: int) -> str:
     return load().paged_attn_status_string(int(status)).decode()
+
+
+def paged_attn_set_launch_flags(flags: int) -> None:
+    """Launch flags for later decode calls from this host thread (0: the plain
+    launch).  FLAG_EARLY_PROLOGUE: the caller guarantees that the work ahead in
+    the stream writes none of the caches, block tables, lengths or query offsets
+    (see include/paged_attn.h)."""
+    _check(load().paged_attn_set_launch_flags(int(flags)))
 
 
 def _check(status: int) -> None:

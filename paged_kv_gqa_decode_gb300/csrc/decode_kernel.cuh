@@ -118,6 +118,13 @@ struct DecodeParams {
   int rows;
   int chunks;
   int total_q;  // rows of q and out (offsets outside [0, total_q) are never touched)
+  // Early prologue: the caller guarantees that the work still running ahead of
+  // this launch in the stream writes none of the caches (and their row floats),
+  // block tables, lengths or query offsets.  The producer then reads them and
+  // starts its tensor copies without waiting for that work; the consumers (the
+  // only ones to read q or the new rows, or to write out or the workspace)
+  // still wait for it.
+  int early;
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -254,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // ---- 0. Programmatic dependent launch: let the next kernel in the stream be
   // scheduled as this grid's CTAs retire, and wait for the previous kernel
   // (which may write any of the inputs) to complete before touching global
-  // memory.  Both are no-ops for a launch without the programmatic attribute.
+  // memory; with the early prologue only the consumers wait (below).  Both are
+  // no-ops for a launch without the programmatic attribute.
   griddep_launch_dependents();
   // Start the cold fetches that only depend on the arguments: the tensor maps
   // (kernel parameters, safe before the wait; needed by the first tensor copy)
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  griddep_wait();
+  if (!p.early) griddep_wait();
   {
     const size_t bt_bytes = (size_t)N * p.maxb * sizeof(int32_t);
     if (bt_bytes <= kBlockTablePrefetchBytes) {
@@ -331,18 +339,25 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     }
   }
 
-  // ---- 2. empty sequences get zero rows (spread over CTAs)
-  for (int s = blockIdx.x; s < N; s += gridDim.x) {
-    if (sm_len[s] != 0) continue;
-    const int r0 = multi ? min(max(sm_qo[s], 0), p.total_q) : s;
-    const int nr = multi ? max(0, min(min(sm_qo[s + 1] - sm_qo[s], R * QC / G), p.total_q - r0))
-                         : 1;
-    uint32_t* o32 = reinterpret_cast<uint32_t*>(p.out + (size_t)r0 * p.H_q * D);
-    for (int i = tid; i < nr * p.H_q * D / 2; i += kThreads) o32[i] = 0u;
-  }
+  // ---- 2. empty sequences get zero rows: sequence s by CTA s mod `ctas`,
+  // threads t0, t0 + nt, ... of it
+  auto zero_empty = [&](long long ctas, int t0, int nt) {
+    for (long long s = blockIdx.x; s < N; s += ctas) {
+      if (sm_len[s] != 0) continue;
+      const int r0 = multi ? min(max(sm_qo[s], 0), p.total_q) : (int)s;
+      const int nr = multi ? max(0, min(min(sm_qo[s + 1] - sm_qo[s], R * QC / G), p.total_q - r0))
+                           : 1;
+      uint32_t* o32 = reinterpret_cast<uint32_t*>(p.out + (size_t)r0 * p.H_q * D);
+      for (int i = t0; i < nr * p.H_q * D / 2; i += nt) o32[i] = 0u;
+    }
+  };
 
   const long long W = (long long)sm_prefix[NW] * H_kv;
-  if (W == 0) return;
+  if (W == 0) {  // nothing to stream: every CTA zeroes its share and leaves
+    if (p.early) griddep_wait();
+    zero_empty(gridDim.x, tid, kThreads);
+    return;
+  }
   if (p.stages < kConsumerWarps) {  // the host plan never launches fewer
     if (tid == 0) atomicOr(p.status, kStatusConfig);
     return;
@@ -350,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   const long long C =
       min((long long)gridDim.x, max(1LL, (W + kMinPagesPerCta - 1) / kMinPagesPerCta));
   if ((long long)blockIdx.x >= C) return;
+  // (with the early prologue the consumers zero them once they have waited)
+  if (!p.early) zero_empty(C, tid, kThreads);
   const long long u0 = range_begin(blockIdx.x, W, C);
   const long long u1 = range_begin(blockIdx.x + 1, W, C);
   if (u0 >= u1) return;
@@ -458,6 +475,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   const int ctid = tid;  // 0 .. kConsumerThreads-1
   bool abort = false;    // this warp gave up waiting for a page (status reports it)
   int first_old = -1;    // thread 0: counter value its first piece's arrival saw
+  if (p.early) {  // the producer went ahead; q, out and the workspace wait for the previous work
+    griddep_wait();
+    zero_empty(C, ctid, kConsumerThreads);
+  }
 
   float o_acc[kDT][kNH][4];   // O^T accumulators
   float m_run[kNH][2];        // running max per owned head (log2 domain)

@@ -17,6 +17,7 @@ namespace pagedattn {
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+thread_local int g_launch_flags = 0;  // paged_attn_set_launch_flags
 
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr size_t kWsAlign = 256;
@@ -373,6 +374,7 @@ int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache,
     p.counters = reinterpret_cast<int32_t*>(wsb + pl.off_counters);
     p.partials = reinterpret_cast<float*>(wsb + pl.off_partials);
     p.num_blocks = num_blocks;
+    p.early = (g_launch_flags & PAGED_ATTN_FLAG_EARLY_PROLOGUE) ? 1 : 0;
     p.k_new = k_new ? static_cast<const __nv_bfloat16*>(k_new) + (size_t)s0 * H_kv * pl.D
                     : nullptr;
     p.v_new = v_new ? static_cast<const __nv_bfloat16*>(v_new) + (size_t)s0 * H_kv * pl.D
@@ -719,8 +721,15 @@ const char* paged_attn_status_string(int status) {
     case PAGED_ATTN_ERR_SCALE: return "scale is not finite";
     case PAGED_ATTN_ERR_STATIC_SCRATCH:
       return "sizes need more scratch than paged_attn_decode_static's fixed 4 MiB array";
+    case PAGED_ATTN_ERR_FLAGS: return "unknown launch flag bits";
     default: return "unknown status";
   }
+}
+
+int paged_attn_set_launch_flags(int flags) {
+  if (flags & ~PAGED_ATTN_FLAG_EARLY_PROLOGUE) return PAGED_ATTN_ERR_FLAGS;
+  g_launch_flags = flags;
+  return PAGED_ATTN_OK;
 }
 
 int paged_attn_last_cuda_error(void) { return g_last_cuda_error; }

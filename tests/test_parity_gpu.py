@@ -315,3 +315,56 @@ def test_workspace_reuse_across_grids_of_one_and_two_ctas_per_sm():
             out = run_gpu(w)
             assert_parity(out, refs[i], f"call {i} round {rnd}")
     del ws_list
+
+
+def _with_flags(flags, fn):
+    pa.paged_attn_set_launch_flags(flags)
+    try:
+        return fn()
+    finally:
+        pa.paged_attn_set_launch_flags(0)
+
+
+def test_early_prologue_gives_the_same_bits():
+    """With the early-prologue flag the producer runs ahead of the previous
+    launch; results must be bit for bit those of the plain launch, including
+    the zero rows of empty sequences."""
+    lens = list(np.random.default_rng(41).integers(0, 600, size=90))
+    lens[3] = lens[17] = 0
+    sp = workloads.custom_spec("early", len(lens), 32, 8, 128, 16, lens, max_len=640)
+    w = workloads.make(sp, seed=41, device="cuda", poison="nan")
+    plain = run_gpu(w).clone()
+
+    def early():
+        outs = [torch.full_like(w.q, float("nan")) for _ in range(4)]
+        for o in outs:  # back to back: each launch's producer overlaps the previous one
+            pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                 w.scale, out=o)
+        torch.cuda.synchronize()
+        return outs
+
+    for o in _with_flags(pa.FLAG_EARLY_PROLOGUE, early):
+        assert torch.equal(o.view(torch.int16), plain.view(torch.int16))
+
+
+def test_early_prologue_waits_for_a_query_the_previous_launch_writes():
+    """A chain out_k = decode(q = out_{k-1}): each launch reads the query the
+    launch before it writes, which the early prologue must still wait for."""
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+
+    def chain():
+        q = w.q
+        for _ in range(4):
+            q = pa.paged_attn_decode(q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+        torch.cuda.synchronize()
+        return q
+
+    plain = chain()
+    assert torch.equal(_with_flags(pa.FLAG_EARLY_PROLOGUE, chain).view(torch.int16),
+                       plain.view(torch.int16))
+
+
+def test_unknown_launch_flags_are_rejected():
+    lib = pa.load()
+    assert lib.paged_attn_set_launch_flags(2) == -10
+    assert lib.paged_attn_set_launch_flags(0) == 0
