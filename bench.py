@@ -307,10 +307,11 @@ def run_ours(args, world, rank, local):
         nbytes["q_out"] = spec.num_seqs * qlen * spec.H_q * spec.D * 2 * 2
         nbytes["total"] = nbytes["kv"] + nbytes["q_out"] + nbytes["block_table"]
 
-    # Early prologue (include/paged_attn.h): in every op but the unfused append,
-    # the work ahead of a decode launch writes at most q and the new rows, never
-    # the caches, tables or lengths, so the producer may start before it ends.
-    early = op != "append_then_decode"
+    # Early prologue (include/paged_attn.h): in the plain decode ops the work
+    # ahead of a launch (the previous step) writes the output only, never the
+    # caches, tables or lengths, so the producer may start before it ends.  The
+    # append ops write the cache every step: plain launch.
+    early = op == "decode"
     pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE if early else 0)
 
     def run_op(q, bt, sl, cache, kn, vn, out=out, st=None):
@@ -528,7 +529,7 @@ def run_ours(args, world, rank, local):
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                 "launch": "early prologue (the producer starts before the previous launch "
                           "ends; caches, tables and lengths are not written between steps)"
-                if early else "plain (an append kernel writes the cache before each decode)",
+                if early else "plain (each step writes the cache)",
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
