@@ -124,7 +124,9 @@ def paged_attn_set_launch_flags(flags: int) -> None:
     """Launch flags for later decode calls from this host thread (0: the plain
     launch).  FLAG_EARLY_PROLOGUE: the caller guarantees that the work ahead in
     the stream writes none of the caches, block tables, lengths or query offsets
-    (see include/paged_attn.h)."""
+    (see include/paged_attn.h).  paged_kv_append and paged_attn_append_decode
+    write the cache, so a launch right after one of them on the same cache must
+    not use it."""
     _check(load().paged_attn_set_launch_flags(int(flags)))
 
 
