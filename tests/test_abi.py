@@ -61,7 +61,7 @@ def test_build_targets_sm103a_only():
 
 def test_status_strings(lib):
     assert pa.paged_attn_status_string(0) == "ok"
-    for code in range(-8, 0):
+    for code in range(-10, 0):
         assert pa.paged_attn_status_string(code) != "unknown status"
     assert lib.paged_attn_version() >= 100
 
@@ -108,3 +108,13 @@ def test_workspace_query_rejects_bad_sizes(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         pa.load(str(tmp_path / "nope.so"))
+
+
+def test_launch_flags_are_checked_on_the_host(lib):
+    """Only the early-prologue bit is known; a rejected call changes nothing."""
+    assert lib.paged_attn_set_launch_flags(1) == 0
+    assert lib.paged_attn_set_launch_flags(2) == -10
+    assert lib.paged_attn_set_launch_flags(-1) == -10
+    assert lib.paged_attn_set_launch_flags(0) == 0
+    with pytest.raises(pa.PagedAttnError):
+        pa.paged_attn_set_launch_flags(4)
