@@ -9,7 +9,11 @@ imports this package, and this package imports nothing from it.
                       source ``paged_attn_oracle.c`` states it in full.
 * ``pieces``       -- the per-range softmax pieces (M, l, o) of rows.
 * ``append``       -- the cache write of each sequence's new token (the step
-                      before the decode).
+                      before the decode); ``append_multi`` the write of several
+                      new tokens per sequence along ``qo_indptr``.
+* ``append_fp8``   -- the cache write into FP8 caches: each new row quantized
+                      to e4m3 with its own dequant float (``quantize_rows_e4m3``;
+                      ``e4m3_encode`` is the nearest-code rounding it uses).
 * ``decode_fp8``   -- the definition over FP8 caches (e4m3 bytes and a dequant
                       float per cache row); ``e4m3_table`` decodes the 256
                       byte values from the format's bit fields.
@@ -104,6 +108,10 @@ def _load():
             lib.oracle_decode_multi.restype = I
             lib.oracle_e4m3_table.argtypes = [P]
             lib.oracle_e4m3_table.restype = None
+            lib.oracle_e4m3_encode.argtypes = [P, I, P]
+            lib.oracle_e4m3_encode.restype = None
+            lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, P, P]
+            lib.oracle_quantize_rows_e4m3.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             _lib = lib
@@ -428,3 +436,100 @@ def finish(state) -> np.ndarray:
     if l == 0.0:
         return np.zeros_like(o)
     return o / l
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """e4m3 codes of float32 values: the nearest e4m3 value, ties to the even
+    code, magnitudes beyond 448 saturating to 448's code, NaN to 0x7F."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32).reshape(-1))
+    out = np.zeros(a.shape[0], dtype=np.uint8)
+    _load().oracle_e4m3_encode(_ptr(a), a.shape[0], _ptr(out))
+    return out.reshape(np.shape(x))
+
+
+def quantize_rows_e4m3(rows):
+    """FP8 quantization of bf16 rows (last axis = one row): returns (codes uint8
+    of the same shape, float32 dequant factor per row).  The factor is
+    max|x| / 448 in float32 (1 for an all-zero row) and code = e4m3(x / factor)
+    with a float32 quotient; see the C source for the reading of the pages."""
+    b = _bits(rows)
+    D = b.shape[-1]
+    flat = np.ascontiguousarray(b.reshape(-1, D))
+    codes = np.zeros(flat.shape, dtype=np.uint8)
+    f = np.zeros(flat.shape[0], dtype=np.float32)
+    _load().oracle_quantize_rows_e4m3(_ptr(flat), flat.shape[0], D, _ptr(codes), _ptr(f))
+    return codes.reshape(b.shape), f.reshape(b.shape[:-1])
+
+
+def append_fp8(x, k_new, v_new) -> "Fp8Inputs":
+    """Cache append into FP8 caches: the write of ``append`` (the new token of
+    sequence s is position L_s - 1), each new K and V row of every KV head
+    quantized by ``quantize_rows_e4m3`` into its e4m3 bytes and its row float.
+    ``k_new`` / ``v_new`` are [num_seqs, H_kv, D] bf16.  Returns new Fp8Inputs
+    with those rows written (the input is not modified)."""
+    inp = x if isinstance(x, Fp8Inputs) else Fp8Inputs.from_workload(x)
+    kn = _bits(k_new)
+    vn = _bits(v_new)
+    if kn.shape != (inp.num_seqs, inp.H_kv, inp.D) or vn.shape != kn.shape:
+        raise ValueError("k_new and v_new must be [num_seqs, H_kv, D]")
+    kc, kf = quantize_rows_e4m3(kn)
+    vc, vf = quantize_rows_e4m3(vn)
+    out = copy.copy(inp)
+    out.k8, out.v8 = inp.k8.copy(), inp.v8.copy()
+    out.ks, out.vs = inp.ks.copy(), inp.vs.copy()
+    for s in range(inp.num_seqs):
+        L = int(inp.lens[s])
+        if L <= 0:
+            continue
+        if L > inp.maxb * inp.BS:
+            raise OracleError(f"oracle rejected the input: {ERRORS[-3]}")
+        t = L - 1
+        b = int(inp.bt[s, t // inp.BS])
+        if not 0 <= b < inp.num_blocks:
+            raise OracleError(f"oracle rejected the input: {ERRORS[-4]}")
+        out.k8[b, :, t % inp.BS, :] = kc[s]
+        out.v8[b, :, t % inp.BS, :] = vc[s]
+        out.ks[b, :, t % inp.BS] = kf[s]
+        out.vs[b, :, t % inp.BS] = vf[s]
+    return out
+
+
+def append_multi(x, qo_indptr, k_new, v_new) -> Inputs:
+    """Cache append of several new tokens per sequence (the multi-token decode's
+    write; rows located through qo_indptr as on AstrAI's CUDA Kernels page, "Q
+    Scheduling and KV Addressing").  Sequence s owns rows qo_indptr[s] ..
+    qo_indptr[s+1] - 1 of ``k_new`` / ``v_new`` ([total_q, H_kv, D] bf16): its
+    last q_len tokens, row qo_indptr[s] + i being token t = L_s - q_len + i, so
+
+        k_cache[bt[s, t // BS], g, t % BS, :] = k_new[qo_indptr[s] + i, g, :]
+
+    for every KV head g (v alike).  Rows with t < 0 (more new rows than the
+    sequence holds) write nothing.  Returns new Inputs with those rows written."""
+    inp = _as_inputs(x)
+    qo = _i32(qo_indptr)
+    kn = _bits(k_new)
+    vn = _bits(v_new)
+    if qo.shape != (inp.num_seqs + 1,) or qo[0] != 0 or np.any(np.diff(qo) < 0):
+        raise ValueError("qo_indptr must be [num_seqs + 1], non-decreasing from 0")
+    total_q = int(qo[-1])
+    if kn.shape != (total_q, inp.H_kv, inp.D) or vn.shape != kn.shape:
+        raise ValueError("k_new and v_new must be [total_q, H_kv, D]")
+    out = copy.copy(inp)
+    out.k = inp.k.copy()
+    out.v = inp.v.copy()
+    for s in range(inp.num_seqs):
+        L = int(inp.lens[s])
+        if L > inp.maxb * inp.BS:
+            raise OracleError(f"oracle rejected the input: {ERRORS[-3]}")
+        ql = int(qo[s + 1] - qo[s])
+        for i in range(ql):
+            t = L - ql + i
+            if t < 0:
+                continue
+            b = int(inp.bt[s, t // inp.BS])
+            if not 0 <= b < inp.num_blocks:
+                raise OracleError(f"oracle rejected the input: {ERRORS[-4]}")
+            r = int(qo[s]) + i
+            out.k[b, :, t % inp.BS, :] = kn[r]
+            out.v[b, :, t % inp.BS, :] = vn[r]
+    return out

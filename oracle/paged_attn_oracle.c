@@ -61,6 +61,15 @@
  *   tokens t <= L - q_len + i (its own position and everything before); without
  *   it, all L tokens.  Each query row is the definition above over the tokens
  *   it sees; a row that sees none is zero.
+ *
+ *   FP8 cache write (nvfp4-megamoe README, "FP8 KV Quantize/Dequant" and "Paged
+ *   KV cache read/write"; the pages fix neither the row float nor the
+ *   rounding, so this is a reading): a bf16 row x of D values is stored as the
+ *   e4m3 codes of x[d] / f, with f = max_d |x[d]| / 448 computed in float32
+ *   (f = 1 for an all-zero row) and each quotient a float32 division; the code
+ *   is the e4m3 value nearest the quotient, a tie going to the code whose
+ *   mantissa is even, and a magnitude beyond 448 takes 448's code.  The
+ *   decision is taken in float32, the precision the library's kernel uses.
  */
 #include <math.h>
 #include <stdint.h>
@@ -411,4 +420,46 @@ int oracle_decode_multi(const uint16_t* q, const uint16_t* k_cache, const uint16
         free(z);
     }
     return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/*
+ * e4m3 code of a float32 value (the FP8 cache write above): the finite code
+ * whose value is nearest |v|, searched over all of them, ties to the even code,
+ * the sign carried over; NaN gives 0x7F.
+ */
+static uint8_t e4m3_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void oracle_e4m3_encode(const float* x, int n, uint8_t* out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+
+/* Quantize n_rows bf16 rows of D values: codes [n_rows, D], one float per row. */
+void oracle_quantize_rows_e4m3(const uint16_t* rows, int n_rows, int D, uint8_t* codes,
+                               float* f_out) {
+    for (int r = 0; r < n_rows; ++r) {
+        const uint16_t* x = rows + (size_t)r * D;
+        float amax = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float a = fabsf((float)widen_bf16(x[d]));
+            if (a > amax) amax = a;
+        }
+        const float f = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int d = 0; d < D; ++d)
+            codes[(size_t)r * D + d] = e4m3_encode((float)widen_bf16(x[d]) / f);
+        f_out[r] = f;
+    }
 }

@@ -803,3 +803,359 @@ def test_multi_pins_catch_planted_mistakes(name, old, new, tmp_path):
 
 def test_unmutated_oracle_passes_the_multi_pins():
     assert _multi_pins_pass()
+
+
+# ---------------------------------------------------------------- FP8 cache write
+# nvfp4-megamoe README, "FP8 KV Quantize/Dequant" and "Paged KV cache
+# read/write".  Reading: a bf16 row x is stored as e4m3(x / f), f = max|x| / 448
+# in float32 (1 for an all-zero row), rounding to the nearest e4m3 value with
+# ties to the even code and saturation at 448.
+
+def _finite_code_values():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    return codes, vals
+
+
+def test_e4m3_encoding_matches_torch_float8_rounding():
+    """The oracle's nearest-code search rounds as torch's float8_e4m3fn cast does
+    (round to nearest even) on random values over the whole range, on every code
+    value, on every midpoint between neighbouring codes (the ties) and just off
+    each midpoint.  torch turns magnitudes past the tie at 464 into NaN where the
+    reading saturates, so the comparison stops at 464."""
+    rng = np.random.default_rng(0)
+    parts = [rng.standard_normal(20000).astype(np.float32) * np.float32(2.0) ** e
+             for e in range(-14, 9, 2)]
+    _, vals = _finite_code_values()
+    pos = np.unique(np.abs(vals))
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (pos[:-1].astype(np.float64) + pos[1:]) / 2)
+    off = np.concatenate([np.nextafter(mids, np.float32(np.inf)),
+                          np.nextafter(mids, np.float32(0))])
+    x = np.concatenate(parts + [vals, mids, -mids, off, -off,
+                                np.array([0.0, -0.0, 448.0, 460.0, 464.0], np.float32)])
+    x = x[np.abs(x) <= 464]
+    got = oracle.e4m3_encode(x)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:10]
+
+
+def test_e4m3_encoding_saturates_and_round_trips_every_code():
+    codes, vals = _finite_code_values()
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)  # every code is its own nearest
+    big = np.array([465.0, 1e4, 3e38, np.inf], np.float32)
+    assert np.array_equal(oracle.e4m3_encode(big), np.full(4, 0x7E, np.uint8))
+    assert np.array_equal(oracle.e4m3_encode(-big), np.full(4, 0xFE, np.uint8))
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+
+
+def _bf16_rows(x):
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+
+
+def test_quantized_rows_decode_within_half_an_e4m3_step():
+    """Decoding code x row float gives back x to within half an e4m3 step (2^-4
+    relative in the normal range, 2^-10 of the row float below it); the largest
+    magnitude of each row lands on +-448 exactly, and the float is that
+    magnitude / 448 to within float32 rounding."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((64, 128)).astype(np.float32) * \
+        (np.float32(2.0) ** rng.integers(-20, 12, size=(64, 1))).astype(np.float32)
+    xb = _bf16_rows(x)
+    xd = xb.double().numpy()
+    codes, f = oracle.quantize_rows_e4m3(xb)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * \
+        f.astype(np.float64)[:, None]
+    q = np.abs(xd) / f.astype(np.float64)[:, None]
+    normal = q >= 2.0 ** -6
+    err = np.abs(dec - xd)
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(xd[normal]) * (1 + 1e-6))
+    assert np.all(err[~normal] <= 2.0 ** -10 * np.broadcast_to(f[:, None], x.shape)[~normal])
+    amax = np.abs(xd).max(axis=1)
+    assert np.all(np.abs(f.astype(np.float64) * 448 - amax) <= amax * 2.0 ** -23)
+    top = np.abs(xd).argmax(axis=1)
+    assert np.all((codes[np.arange(64), top] & 0x7F) == 0x7E)
+
+
+def test_rows_of_e4m3_values_quantize_exactly():
+    """A row made of e4m3 values times 2^k with one element at +-448 * 2^k has row
+    float 2^k and comes back code for code (the -0 code included)."""
+    rng = np.random.default_rng(2)
+    codes_all, _ = _finite_code_values()
+    codes = rng.choice(codes_all, size=(40, 256)).astype(np.uint8)
+    codes[np.arange(40), rng.integers(0, 256, 40)] = rng.choice([0x7E, 0xFE], 40)
+    k = rng.integers(-12, 8, size=40)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double() * \
+        torch.from_numpy(np.ldexp(1.0, k))[:, None]
+    xb = vals.to(torch.bfloat16)
+    assert torch.equal(xb.double(), vals)
+    got, f = oracle.quantize_rows_e4m3(xb)
+    assert np.array_equal(f, np.ldexp(1.0, k).astype(np.float32))
+    assert np.array_equal(got, codes)
+
+
+def test_all_zero_row_has_float_one():
+    got, f = oracle.quantize_rows_e4m3(torch.zeros(3, 128, dtype=torch.bfloat16))
+    assert np.array_equal(f, np.ones(3, np.float32)) and not got.any()
+
+
+def _fp8_write_pins_pass() -> bool:
+    try:
+        test_e4m3_encoding_matches_torch_float8_rounding()
+        test_e4m3_encoding_saturates_and_round_trips_every_code()
+        test_quantized_rows_decode_within_half_an_e4m3_step()
+        test_rows_of_e4m3_values_quantize_exactly()
+        test_all_zero_row_has_float_one()
+    except (AssertionError, oracle.OracleError, FloatingPointError, ValueError):
+        return False
+    return True
+
+
+FP8_WRITE_MUTANTS = [
+    ("ties to the odd code", "(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    ("rounds toward zero", "const double err = fabs(e4m3_value((uint8_t)c) - a);",
+     "const double err = e4m3_value((uint8_t)c) <= a ? a - e4m3_value((uint8_t)c) : INFINITY;"),
+    ("row float from 240", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    ("zero row float 0", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 448.0f : 0.0f"),
+    ("multiplies by the float", "e4m3_encode((float)widen_bf16(x[d]) / f)",
+     "e4m3_encode((float)widen_bf16(x[d]) * f)"),
+    ("sign dropped", "return (uint8_t)(sign | best);", "return (uint8_t)best;"),
+    ("amax of the signed values", "const float a = fabsf((float)widen_bf16(x[d]));",
+     "const float a = (float)widen_bf16(x[d]);"),
+]
+
+_FP8_WRITE_MUTANT_RUNNER = _MUTANT_RUNNER.replace(
+    '("oracle_decode", "oracle_decode_pairs", "oracle_partial_pairs")',
+    '("oracle_e4m3_encode", "oracle_quantize_rows_e4m3")').replace(
+    "T._pins_pass()", "T._fp8_write_pins_pass()")
+
+
+@pytest.mark.parametrize("name,old,new", FP8_WRITE_MUTANTS, ids=[m[0] for m in FP8_WRITE_MUTANTS])
+def test_fp8_write_pins_catch_planted_mistakes(name, old, new, tmp_path):
+    import subprocess
+    import sys
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, name
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutant), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _FP8_WRITE_MUTANT_RUNNER.format(root=os.path.dirname(here), tests=here, so=str(so))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode < 0 or "PINS_FAIL" in r.stdout, \
+        f"no pin noticed the planted mistake: {name}\n{r.stdout}\n{r.stderr[-2000:]}"
+
+
+def test_unmutated_oracle_passes_the_fp8_write_pins():
+    assert _fp8_write_pins_pass()
+
+
+def _fp8_exact_cache(seed, lens, H_kv=2, D=128, BS=16):
+    """An FP8 problem whose every cache row is e4m3 codes x 2^k with one element at
+    +-448 x 2^k (so quantizing its decoded values gives the row back exactly)."""
+    spec = workloads.custom_spec("fp8exact", len(lens), 4 * H_kv, H_kv, D, BS, list(lens))
+    w = workloads.make(spec, seed=seed, poison="none")
+    rng = np.random.default_rng(seed)
+    shape = tuple(w.k_cache.shape)
+    codes_all, _ = _finite_code_values()
+    codes = rng.choice(codes_all, size=(2,) + shape).astype(np.uint8)
+    flat = codes.reshape(-1, D)
+    flat[np.arange(flat.shape[0]), rng.integers(0, D, flat.shape[0])] = 0x7E
+    scales = np.ldexp(1.0, rng.integers(-6, 4, size=(2,) + shape[:3])).astype(np.float32)
+    f8 = oracle.Fp8Inputs(w.q, codes[0], codes[1], scales[0], scales[1], w.block_tables,
+                          w.seq_lens, w.scale)
+    return w, f8
+
+
+def _newest_fp8_rows(f8):
+    """Each sequence's newest K and V rows as bf16 values, read through the un-paged view."""
+    vals = []
+    for c8, sc in ((f8.k8, f8.ks), (f8.v8, f8.vs)):
+        dec = torch.from_numpy(c8).view(torch.float8_e4m3fn).double() * \
+            torch.from_numpy(sc).double().unsqueeze(-1)
+        rows = torch.zeros(f8.num_seqs, f8.H_kv, f8.D, dtype=torch.float64)
+        for s in range(f8.num_seqs):
+            L = int(f8.lens[s])
+            if L:
+                pages = [int(f8.bt[s, i]) for i in range(-(-L // f8.BS))]
+                flat = torch.cat([dec[b] for b in pages], dim=1)  # [H_kv, pages*BS, D]
+                rows[s] = flat[:, L - 1]
+        vals.append(rows.to(torch.bfloat16))
+    return vals
+
+
+def _fp8_append_round_trip(append_fp8):
+    """Take each newest row out of an exact FP8 cache, poison its bytes and float,
+    append its values back: bytes and floats come back bit for bit, nothing else moves."""
+    _, f8 = _fp8_exact_cache(3, [1, 15, 16, 17, 40, 0, 33])
+    k_new, v_new = _newest_fp8_rows(f8)
+    hole = copy_fp8(f8)
+    for s in range(hole.num_seqs):
+        L = int(hole.lens[s])
+        if L:
+            b = int(hole.bt[s, (L - 1) // hole.BS])
+            hole.k8[b, :, (L - 1) % hole.BS] = 0x7F
+            hole.v8[b, :, (L - 1) % hole.BS] = 0x7F
+            hole.ks[b, :, (L - 1) % hole.BS] = np.nan
+            hole.vs[b, :, (L - 1) % hole.BS] = np.nan
+    back = append_fp8(hole, k_new, v_new)
+    assert np.array_equal(back.k8, f8.k8) and np.array_equal(back.v8, f8.v8)
+    assert np.array_equal(back.ks, f8.ks) and np.array_equal(back.vs, f8.vs)
+
+
+def copy_fp8(f8):
+    import copy as _copy
+
+    c = _copy.copy(f8)
+    c.k8, c.v8, c.ks, c.vs = f8.k8.copy(), f8.v8.copy(), f8.ks.copy(), f8.vs.copy()
+    return c
+
+
+def _fp8_append_pins_pass(append_fp8) -> bool:
+    try:
+        _fp8_append_round_trip(append_fp8)
+    except (AssertionError, oracle.OracleError, IndexError, ValueError):
+        return False
+    return True
+
+
+def test_fp8_append_round_trip_restores_bytes_and_floats():
+    _fp8_append_round_trip(oracle.append_fp8)
+
+
+FP8_APPEND_MUTANTS = [
+    ("slot from L", "out.k8[b, :, t % inp.BS, :] = kc[s]", "out.k8[b, :, L % inp.BS, :] = kc[s]"),
+    ("float of V from K", "out.vs[b, :, t % inp.BS] = vf[s]", "out.vs[b, :, t % inp.BS] = kf[s]"),
+    ("page of the next token", "b = int(inp.bt[s, t // inp.BS])", "b = int(inp.bt[s, L // inp.BS])"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", FP8_APPEND_MUTANTS, ids=[m[0] for m in FP8_APPEND_MUTANTS])
+def test_fp8_append_pins_catch_planted_mistakes(name, old, new):
+    import inspect
+
+    src = inspect.getsource(oracle.append_fp8)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    assert not _fp8_append_pins_pass(ns["append_fp8"]), f"no pin noticed: {name}"
+
+
+# ---------------------------------------------------------------- multi-token append
+
+MULTI_APPEND_LENS = [1, 15, 16, 17, 40, 0, 33, 5]
+MULTI_APPEND_QLENS = [1, 3, 16, 2, 17, 0, 8, 7]
+
+
+def _multi_append_problem(seed=12):
+    spec = workloads.custom_spec("mapp", len(MULTI_APPEND_LENS), 8, 2, 64, 16, MULTI_APPEND_LENS)
+    w = workloads.make(spec, seed=seed, poison="nan")
+    qo = np.concatenate([[0], np.cumsum(MULTI_APPEND_QLENS)]).astype(np.int32)
+    return oracle.Inputs.from_workload(w), qo
+
+
+def _newest_rows(inp, qo):
+    """Each sequence's last q_len cached rows (fewer when L < q_len: those rows stay
+    zero), [total_q, H_kv, D], read through the un-paged view."""
+    k = np.zeros((int(qo[-1]), inp.H_kv, inp.D), dtype=np.uint16)
+    v = np.zeros_like(k)
+    for s in range(inp.num_seqs):
+        L, ql = int(inp.lens[s]), int(qo[s + 1] - qo[s])
+        if L == 0:
+            continue
+        pages = [inp.bt[s, i] for i in range(-(-L // inp.BS))]
+        fk = np.concatenate([inp.k[b] for b in pages], axis=1)
+        fv = np.concatenate([inp.v[b] for b in pages], axis=1)
+        for i in range(ql):
+            t = L - ql + i
+            if t >= 0:
+                k[qo[s] + i], v[qo[s] + i] = fk[:, t], fv[:, t]
+    return k, v
+
+
+def _multi_append_pins(append_multi):
+    inp, qo = _multi_append_problem()
+    # one new token each: the single-token append
+    ones = np.arange(inp.num_seqs + 1, dtype=np.int32)
+    rng = np.random.default_rng(4)
+    kn = rng.integers(0x4700, 0x4780, size=(inp.num_seqs, inp.H_kv, inp.D), dtype=np.uint16)
+    vn = rng.integers(0xC700, 0xC780, size=kn.shape, dtype=np.uint16)
+    a, b = append_multi(inp, ones, kn, vn), oracle.append(inp, kn, vn)
+    assert np.array_equal(a.k, b.k) and np.array_equal(a.v, b.v)
+    # round trip: the newest q_len rows taken out, poisoned and appended back
+    k_new, v_new = _newest_rows(inp, qo)
+    hole = oracle.Inputs.from_workload(workloads.make(workloads.custom_spec(
+        "mapp", len(MULTI_APPEND_LENS), 8, 2, 64, 16, MULTI_APPEND_LENS), seed=12, poison="nan"))
+    hole.k, hole.v = hole.k.copy(), hole.v.copy()
+    for s in range(hole.num_seqs):
+        L, ql = int(hole.lens[s]), int(qo[s + 1] - qo[s])
+        for t in range(max(0, L - ql), L):
+            bb = int(hole.bt[s, t // hole.BS])
+            hole.k[bb, :, t % hole.BS] = 0x7FC0
+            hole.v[bb, :, t % hole.BS] = 0x7FC0
+    back = append_multi(hole, qo, k_new, v_new)
+    assert np.array_equal(back.k, inp.k) and np.array_equal(back.v, inp.v)
+    # exactly min(q_len, L) rows per sequence change
+    big_k = rng.integers(0x4700, 0x4780, size=k_new.shape, dtype=np.uint16)
+    big_v = rng.integers(0xC700, 0xC780, size=k_new.shape, dtype=np.uint16)
+    out = append_multi(inp, qo, big_k, big_v)
+    rows = sum(min(L, q) for L, q in zip(MULTI_APPEND_LENS, MULTI_APPEND_QLENS))
+    assert int((out.k != inp.k).sum()) == rows * inp.H_kv * inp.D
+    assert int((out.v != inp.v).sum()) == rows * inp.H_kv * inp.D
+    got_k, _ = _newest_rows(out, qo)
+    for s in range(inp.num_seqs):
+        L, ql = int(inp.lens[s]), int(qo[s + 1] - qo[s])
+        for i in range(ql):
+            if L - ql + i >= 0:
+                assert np.array_equal(got_k[qo[s] + i], big_k[qo[s] + i])
+
+
+def _multi_append_pins_pass(append_multi) -> bool:
+    try:
+        _multi_append_pins(append_multi)
+    except (AssertionError, oracle.OracleError, IndexError, ValueError):
+        return False
+    return True
+
+
+def test_multi_append_is_the_append_for_one_token_and_round_trips():
+    _multi_append_pins(oracle.append_multi)
+
+
+MULTI_APPEND_MUTANTS = [
+    ("one token later", "t = L - ql + i\n", "t = L - ql + i + 1\n"),
+    ("row of the sequence index", "r = int(qo[s]) + i", "r = s + i"),
+    ("negative tokens written", "if t < 0:\n                continue", "if t < -99:\n                continue"),
+    ("v from k", "out.v[b, :, t % inp.BS, :] = vn[r]", "out.v[b, :, t % inp.BS, :] = kn[r]"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MULTI_APPEND_MUTANTS,
+                         ids=[m[0] for m in MULTI_APPEND_MUTANTS])
+def test_multi_append_pins_catch_planted_mistakes(name, old, new):
+    import inspect
+
+    src = inspect.getsource(oracle.append_multi)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    assert not _multi_append_pins_pass(ns["append_multi"]), f"no pin noticed: {name}"
+
+
+def test_noncausal_multi_matches_torch_sdpa_without_a_mask():
+    """Without the causal mask every query row of a sequence attends all its tokens:
+    torch float64 SDPA over the un-paged K/V, no mask."""
+    lens, qlens, H_q, H_kv, D, BS = [5, 40, 17], [2, 7, 17], 6, 2, 32, 16
+    q, K, V, kc, vc, bt, sl = _random_problem(21, lens, H_q, H_kv, D, BS)
+    g = torch.Generator().manual_seed(22)
+    qm = _bf16(torch.randn(sum(qlens), H_q, D, generator=g))
+    qo = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    x = oracle.MultiInputs(qm, kc, vc, bt, sl, 0.125)
+    got = oracle.decode_multi(x, qo, causal=False)
+    for s in range(len(lens)):
+        rows = qm[qo[s]:qo[s + 1]]
+        want = _sdpa(rows, [K[s]] * len(rows), [V[s]] * len(rows), 0.125)
+        assert np.allclose(got[qo[s]:qo[s + 1]], want, rtol=0, atol=1e-12)
