@@ -37,9 +37,9 @@
  * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), never synchronises, and never allocates except
  * where an entry point says so.  Block ids outside the caller's pool are not
- * detected by paged_attn_decode / paged_attn_decode_ws (the tensor memory
- * access reads whatever lies at that address); paged_attn_decode_checked
- * detects them.
+ * detected unless checks are on: paged_attn_decode_checked checks its own
+ * call, and paged_attn_set_checks turns the same checks on for every later
+ * call of the calling thread (all decode and append entry points).
  *
  * Errors: every entry point returns PAGED_ATTN_OK (0) or a negative
  * PAGED_ATTN_ERR_* code.  Argument errors are detected on the host before any
@@ -125,7 +125,13 @@ PAGED_ATTN_API int paged_attn_decode_ws(const void* q, const void* k_cache, cons
  * clamped, and no memory outside the pool is read.  Bit 2 reports that a
  * pipeline wait in the kernel ran out of its iteration limit and bit 3 that
  * the kernel rejected its launch configuration (library faults, never
- * expected).  Uses the library-owned workspace like paged_attn_decode.
+ * expected; the output of such a call is undefined, the workspace stays
+ * usable unless a combine wait ran out, in which case the workspace must be
+ * zero-filled again before its next use: paged_attn_reset_workspace for the
+ * library-owned one).  The
+ * kernel writes *d_status only after the work ahead of it in the stream has
+ * completed, so that work may zero-fill it.  Uses the library-owned workspace
+ * like paged_attn_decode.
  */
 PAGED_ATTN_API int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
                               const int32_t* block_tables, const int32_t* seq_lens,
@@ -159,6 +165,21 @@ PAGED_ATTN_API int paged_attn_decode_static(const void* q, const void* k_cache, 
                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                              int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
                              int block_size, float scale, void* stream);
+
+/*
+ * Device-side checks for every later call of the calling thread: with
+ * num_blocks > 0, every decode and append entry point validates the block ids
+ * it uses against [0, num_blocks) and reports into *d_status (a device int32,
+ * 4-byte aligned, that the caller zero-fills) as paged_attn_decode_checked
+ * does: bit 0 for a bad block id (a decode reads zero rows for it through the
+ * tensor copies of the standard and FP8 layouts, block 0's rows through the
+ * bulk copies of the x-packed layout; an append skips that row), bit 1 for a
+ * bad length or a multi-token sequence with more query rows than the call
+ * allows, bits 2 and 3 as there.  (0, NULL) turns the checks off.  Returns
+ * PAGED_ATTN_ERR_SIZES for num_blocks outside [1, 2^31) and
+ * PAGED_ATTN_ERR_POINTER for a null or misaligned d_status, changing nothing.
+ */
+PAGED_ATTN_API int paged_attn_set_checks(long long num_blocks, int32_t* d_status);
 
 /*
  * The same operation over FP8 caches: the nvfp4-megamoe README's FP8 KV path
@@ -218,6 +239,27 @@ PAGED_ATTN_API int paged_attn_decode_multi(const void* q, const void* k_cache,
                                            int max_q_len, int H_q, int H_kv, int head_dim,
                                            int max_blocks_per_seq, int block_size, float scale,
                                            void* stream);
+
+/*
+ * paged_attn_decode_multi with the causal mask chosen by the caller (AstrAI's
+ * CUDA Kernels page, "Python Wrappers": is_causal).  is_causal != 0 is
+ * paged_attn_decode_multi; is_causal = 0 lets every query row of sequence s
+ * attend all its tokens t < seq_lens[s]:
+ *
+ *   out[qo[s] + i, h, :] = softmax_t(scale * q[qo[s] + i, h, :] . K_t) . V_t,
+ *                          t in [0, seq_lens[s])
+ *
+ * Everything else as paged_attn_decode_multi.
+ */
+PAGED_ATTN_API int paged_attn_decode_multi_ex(const void* q, const void* k_cache,
+                                              const void* v_cache, void* out,
+                                              const int32_t* qo_indptr,
+                                              const int32_t* block_tables,
+                                              const int32_t* seq_lens, int num_seqs,
+                                              int total_q, int max_q_len, int H_q, int H_kv,
+                                              int head_dim, int max_blocks_per_seq,
+                                              int block_size, float scale, int is_causal,
+                                              void* stream);
 
 /*
  * The same operation over bf16 caches in the x-packed layout ("Paged Attention
@@ -286,6 +328,80 @@ PAGED_ATTN_API int paged_attn_append_decode(const void* q, const void* k_new, co
                                             int max_blocks_per_seq, int block_size, float scale,
                                             void* stream);
 
+/*
+ * Cache append of several new tokens per sequence, the write that precedes the
+ * multi-token decode: the rows of k_new / v_new ([total_q, H_kv, head_dim]
+ * bf16, 16-byte aligned) follow qo_indptr as the queries do (AstrAI's CUDA
+ * Kernels page, "Q Scheduling and KV Addressing"): row qo_indptr[s] + i is
+ * token t = seq_lens[s] - q_len + i of sequence s (q_len = qo_indptr[s+1] -
+ * qo_indptr[s]; seq_lens counts the new tokens), and for every KV head g
+ *
+ *   k_cache[block_tables[s, t / block_size], g, t % block_size, :] = k_new[qo_indptr[s] + i, g, :]
+ *
+ * (v alike).  Rows with t < 0 (more new rows than the sequence holds), of a
+ * sequence with a length outside [1, max_blocks_per_seq * block_size], or
+ * outside [qo_indptr[0], qo_indptr[num_seqs]) write nothing.  Sizes and errors
+ * as paged_kv_append, plus PAGED_ATTN_ERR_SIZES for total_q < 0.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+PAGED_ATTN_API int paged_kv_append_multi(const void* k_new, const void* v_new, void* k_cache,
+                                         void* v_cache, const int32_t* qo_indptr,
+                                         const int32_t* block_tables, const int32_t* seq_lens,
+                                         int num_seqs, int total_q, int H_kv, int head_dim,
+                                         int max_blocks_per_seq, int block_size, void* stream);
+
+/*
+ * paged_kv_append_multi followed by paged_attn_decode_multi_ex, as two
+ * launches on `stream` (the decode waits for the append to complete before it
+ * reads anything, whatever the launch flags).  Arguments as the two calls.
+ */
+PAGED_ATTN_API int paged_attn_append_decode_multi(const void* q, const void* k_new,
+                                                  const void* v_new, void* k_cache,
+                                                  void* v_cache, void* out,
+                                                  const int32_t* qo_indptr,
+                                                  const int32_t* block_tables,
+                                                  const int32_t* seq_lens, int num_seqs,
+                                                  int total_q, int max_q_len, int H_q, int H_kv,
+                                                  int head_dim, int max_blocks_per_seq,
+                                                  int block_size, float scale, int is_causal,
+                                                  void* stream);
+
+/*
+ * Cache append into FP8 caches (quantize on write; nvfp4-megamoe README, "FP8
+ * KV Quantize/Dequant" and "Paged KV cache read/write"): the new token's K and
+ * V rows of every sequence and KV head, bf16 [num_seqs, H_kv, head_dim], are
+ * quantized one row at a time and written where paged_kv_append writes:
+ *
+ *   f        = max_d |x[d]| / 448   in float32 (f = 1 for an all-zero row)
+ *   byte[d]  = e4m3(x[d] / f)       float32 quotient, rounded to nearest even,
+ *                                   saturated to +-448
+ *   k_cache[b, g, slot, :] = byte,  k_scale[b, g, slot] = f   (v alike)
+ *
+ * so that paged_attn_decode_fp8 reads x[d] as e4m3(byte[d]) * f.  k_cache /
+ * v_cache hold e4m3 bytes, k_scale / v_scale float32 [num_blocks, H_kv,
+ * block_size]; head_dim 128 or 256 (PAGED_ATTN_ERR_HEAD_DIM otherwise).
+ * Which sequences write, sizes, errors: as paged_kv_append.  Asynchronous on
+ * `stream`; allocates nothing.
+ */
+PAGED_ATTN_API int paged_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, float* k_scale, float* v_scale,
+                                       const int32_t* block_tables, const int32_t* seq_lens,
+                                       int num_seqs, int H_kv, int head_dim,
+                                       int max_blocks_per_seq, int block_size, void* stream);
+
+/*
+ * paged_kv_append_fp8 followed by paged_attn_decode_fp8, as two launches on
+ * `stream` (the decode waits for the append to complete before it reads
+ * anything, whatever the launch flags).  Arguments as the two calls.
+ */
+PAGED_ATTN_API int paged_attn_append_decode_fp8(const void* q, const void* k_new,
+                                                const void* v_new, void* k_cache, void* v_cache,
+                                                float* k_scale, float* v_scale, void* out,
+                                                const int32_t* block_tables,
+                                                const int32_t* seq_lens, int num_seqs, int H_q,
+                                                int H_kv, int head_dim, int max_blocks_per_seq,
+                                                int block_size, float scale, void* stream);
+
 /* Human-readable text for a PAGED_ATTN_* code (static storage). */
 PAGED_ATTN_API const char* paged_attn_status_string(int status);
 
@@ -302,13 +418,24 @@ PAGED_ATTN_API const char* paged_attn_status_string(int status);
  * the fused append and the output may be written by it.  The kernel then
  * scans the lengths, translates the first pages and starts their tensor
  * copies while that work finishes.  It waits for it only before reading q or
- * the new rows, and before writing the output or the workspace.  In a
- * layer-by-layer decode loop the kernel just before attention typically
- * writes q, and with paged_attn_append_decode the new K/V rows too, but not
- * the caches, tables or lengths.  With the separate paged_kv_append just
- * before, the flag must stay off.  Results are those of the plain launch.
+ * the new rows, and before writing the output, the workspace or a status
+ * word.  In a layer-by-layer decode loop the kernel just before attention
+ * typically writes q, and with paged_attn_append_decode the new K/V rows too,
+ * but not the caches, tables or lengths.  With the caller's own
+ * paged_kv_append (or any other write of the caches) just before, the flag
+ * must stay off.  The append-and-decode entry points never let their own
+ * append break the guarantee: where the append is a launch of its own, the
+ * decode after it is a plain launch whatever the flag says.  Results are
+ * those of the plain launch.
  */
 PAGED_ATTN_API int paged_attn_set_launch_flags(int flags);
+
+/*
+ * Zero-fills the library-owned workspace of the current device on `stream`
+ * (nothing to do when none exists yet).  Needed only after a call reported a
+ * combine wait that ran out (status bit 2), which can leave split counters set.
+ */
+PAGED_ATTN_API int paged_attn_reset_workspace(void* stream);
 
 /* The last cudaError_t / CUresult value behind a PAGED_ATTN_ERR_CUDA on this thread. */
 PAGED_ATTN_API int paged_attn_last_cuda_error(void);

@@ -26,9 +26,15 @@ __all__ = [
     "paged_attn_decode_fp8",
     "paged_attn_decode_xpacked",
     "paged_attn_decode_multi",
+    "paged_kv_append_multi",
+    "paged_attn_append_decode_multi",
+    "paged_kv_append_fp8",
+    "paged_attn_append_decode_fp8",
     "paged_attn_workspace_bytes",
     "paged_attn_status_string",
     "paged_attn_set_launch_flags",
+    "paged_attn_set_checks",
+    "paged_attn_reset_workspace",
     "FLAG_EARLY_PROLOGUE",
     "EXPORTED_SYMBOLS",
 ]
@@ -48,8 +54,15 @@ EXPORTED_SYMBOLS = (
     "paged_attn_decode_fp8",
     "paged_attn_decode_xpacked",
     "paged_attn_decode_multi",
+    "paged_attn_decode_multi_ex",
+    "paged_kv_append_multi",
+    "paged_attn_append_decode_multi",
+    "paged_kv_append_fp8",
+    "paged_attn_append_decode_fp8",
     "paged_attn_status_string",
     "paged_attn_set_launch_flags",
+    "paged_attn_set_checks",
+    "paged_attn_reset_workspace",
     "paged_attn_last_cuda_error",
     "paged_attn_version",
 )
@@ -103,6 +116,23 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.paged_attn_decode_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                 P]
         lib.paged_attn_decode_multi.restype = I
+        lib.paged_attn_decode_multi_ex.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                                   F, I, P]
+        lib.paged_attn_decode_multi_ex.restype = I
+        lib.paged_kv_append_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+        lib.paged_kv_append_multi.restype = I
+        lib.paged_attn_append_decode_multi.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                                       I, I, I, F, I, P]
+        lib.paged_attn_append_decode_multi.restype = I
+        lib.paged_kv_append_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P]
+        lib.paged_kv_append_fp8.restype = I
+        lib.paged_attn_append_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                                     I, F, P]
+        lib.paged_attn_append_decode_fp8.restype = I
+        lib.paged_attn_set_checks.argtypes = [LL, P]
+        lib.paged_attn_set_checks.restype = I
+        lib.paged_attn_reset_workspace.argtypes = [P]
+        lib.paged_attn_reset_workspace.restype = I
         lib.paged_attn_status_string.argtypes = [I]
         lib.paged_attn_status_string.restype = ctypes.c_char_p
         lib.paged_attn_last_cuda_error.argtypes = []
@@ -128,6 +158,20 @@ def paged_attn_set_launch_flags(flags: int) -> None:
     write the cache, so a launch right after one of them on the same cache must
     not use it."""
     _check(load().paged_attn_set_launch_flags(int(flags)))
+
+
+def paged_attn_set_checks(num_blocks: int = 0, status=None) -> None:
+    """Device-side checks for later calls from this host thread: block ids are
+    validated against [0, num_blocks) and problems reported into ``status`` (an
+    int32 device tensor of one element the caller zero-fills); ``(0, None)``
+    turns them off (see include/paged_attn.h)."""
+    _check(load().paged_attn_set_checks(int(num_blocks), _ptr(status)))
+
+
+def paged_attn_reset_workspace(stream=None) -> None:
+    """Zero-fill the library-owned workspace of the current device (needed only
+    after a call reported a combine wait that ran out)."""
+    _check(load().paged_attn_reset_workspace(_stream(stream)))
 
 
 def _check(status: int) -> None:
@@ -258,15 +302,10 @@ def paged_attn_decode_xpacked(q, kx, vt, block_tables, seq_lens, scale: float, o
     return out
 
 
-def paged_attn_decode_multi(q, k_cache, v_cache, qo_indptr, block_tables, seq_lens,
-                            scale: float, max_q_len: int, out=None, stream=None):
-    """Multi-token decode (see paged_attn.h): q [total_q, H_q, D], sequence s owning
-    rows qo_indptr[s] .. qo_indptr[s+1] - 1 (its last tokens, causal)."""
+def _multi_sizes(q, k_cache, qo_indptr, block_tables, seq_lens, contiguous):
     import torch
 
-    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
-                    ("qo_indptr", qo_indptr), ("block_tables", block_tables),
-                    ("seq_lens", seq_lens)):
+    for name, t in contiguous.items():
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     total_q, H_q, D = (int(x) for x in q.shape)
@@ -276,13 +315,63 @@ def paged_attn_decode_multi(q, k_cache, v_cache, qo_indptr, block_tables, seq_le
     num_seqs = int(seq_lens.shape[0])
     if tuple(qo_indptr.shape) != (num_seqs + 1,) or qo_indptr.dtype != torch.int32:
         raise ValueError("qo_indptr must be int32 [num_seqs + 1]")
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    return num_seqs, total_q, H_q, H_kv, D, maxb, BS
+
+
+def paged_attn_decode_multi(q, k_cache, v_cache, qo_indptr, block_tables, seq_lens,
+                            scale: float, max_q_len: int, out=None, stream=None,
+                            causal: bool = True):
+    """Multi-token decode (see paged_attn.h): q [total_q, H_q, D], sequence s owning
+    rows qo_indptr[s] .. qo_indptr[s+1] - 1 (its last tokens); causal, or every
+    row attending all of the sequence's tokens with ``causal=False``."""
+    import torch
+
+    num_seqs, total_q, H_q, H_kv, D, maxb, BS = _multi_sizes(
+        q, k_cache, qo_indptr, block_tables, seq_lens,
+        dict(q=q, k_cache=k_cache, v_cache=v_cache, qo_indptr=qo_indptr,
+             block_tables=block_tables, seq_lens=seq_lens))
     if out is None:
         out = torch.empty_like(q)
-    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
-    _check(load().paged_attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
-                                          _ptr(qo_indptr), _ptr(block_tables), _ptr(seq_lens),
-                                          num_seqs, total_q, int(max_q_len), H_q, H_kv, D, maxb,
-                                          BS, float(scale), _stream(stream)))
+    _check(load().paged_attn_decode_multi_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                             _ptr(qo_indptr), _ptr(block_tables),
+                                             _ptr(seq_lens), num_seqs, total_q, int(max_q_len),
+                                             H_q, H_kv, D, maxb, BS, float(scale),
+                                             1 if causal else 0, _stream(stream)))
+    return out
+
+
+def paged_kv_append_multi(k_new, v_new, k_cache, v_cache, qo_indptr, block_tables, seq_lens,
+                          stream=None):
+    """Write several new tokens per sequence into the paged caches (see paged_attn.h):
+    k_new, v_new [total_q, H_kv, head_dim] bf16, row qo_indptr[s] + i being token
+    seq_lens[s] - q_len + i of sequence s."""
+    _check_rows(k_new, v_new, None, k_cache)
+    num_seqs, total_q, _, H_kv, D, maxb, BS = _multi_sizes(
+        k_new, k_cache, qo_indptr, block_tables, seq_lens,
+        dict(qo_indptr=qo_indptr, block_tables=block_tables, seq_lens=seq_lens))
+    _check(load().paged_kv_append_multi(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(qo_indptr), _ptr(block_tables), _ptr(seq_lens),
+                                        num_seqs, total_q, H_kv, D, maxb, BS, _stream(stream)))
+
+
+def paged_attn_append_decode_multi(q, k_new, v_new, k_cache, v_cache, qo_indptr, block_tables,
+                                   seq_lens, scale: float, max_q_len: int, out=None,
+                                   stream=None, causal: bool = True):
+    """paged_kv_append_multi then paged_attn_decode_multi (see paged_attn.h)."""
+    import torch
+
+    _check_rows(k_new, v_new, q, k_cache)
+    num_seqs, total_q, H_q, H_kv, D, maxb, BS = _multi_sizes(
+        q, k_cache, qo_indptr, block_tables, seq_lens,
+        dict(q=q, k_cache=k_cache, v_cache=v_cache, qo_indptr=qo_indptr,
+             block_tables=block_tables, seq_lens=seq_lens))
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().paged_attn_append_decode_multi(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+        _ptr(qo_indptr), _ptr(block_tables), _ptr(seq_lens), num_seqs, total_q, int(max_q_len),
+        H_q, H_kv, D, maxb, BS, float(scale), 1 if causal else 0, _stream(stream)))
     return out
 
 
@@ -344,4 +433,49 @@ def paged_attn_decode_fp8(q, k8, v8, k_scale, v_scale, block_tables, seq_lens, s
     # (q, k8, v8, k_scale, v_scale, out, tables, lens, sizes..., scale)
     _check(load().paged_attn_decode_fp8(a[0], a[1], a[2], _ptr(k_scale), _ptr(v_scale), a[3],
                                         *a[4:], _stream(stream)))
+    return out
+
+
+def _check_fp8_cache(k8, v8, k_scale, v_scale):
+    import torch
+
+    for name, t in (("k8", k8), ("v8", v8), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if k8.dtype != torch.uint8 or v8.dtype != torch.uint8:
+        raise ValueError("k8 / v8 must be uint8 (e4m3 bytes)")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32 or \
+            tuple(k_scale.shape) != tuple(k8.shape[:3]) or k_scale.shape != v_scale.shape:
+        raise ValueError("k_scale / v_scale must be float32 [num_blocks, H_kv, block_size]")
+
+
+def paged_kv_append_fp8(k_new, v_new, k8, v8, k_scale, v_scale, block_tables, seq_lens,
+                        stream=None):
+    """Quantize each sequence's new K / V rows (bf16 [num_seqs, H_kv, head_dim]) to
+    e4m3 with one dequant float per row and write them into the FP8 caches at
+    position seq_lens[s] - 1 (see paged_attn.h)."""
+    _check_fp8_cache(k8, v8, k_scale, v_scale)
+    _check_rows(k_new, v_new, None, k8)
+    num_blocks, H_kv, BS, D = (int(x) for x in k8.shape)
+    maxb = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(load().paged_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k8), _ptr(v8),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                      _ptr(seq_lens), int(k_new.shape[0]), H_kv, D, maxb, BS,
+                                      _stream(stream)))
+
+
+def paged_attn_append_decode_fp8(q, k_new, v_new, k8, v8, k_scale, v_scale, block_tables,
+                                 seq_lens, scale: float, out=None, stream=None):
+    """paged_kv_append_fp8 then paged_attn_decode_fp8 (see paged_attn.h)."""
+    import torch
+
+    _check_fp8_cache(k8, v8, k_scale, v_scale)
+    _check_rows(k_new, v_new, q, k8)
+    if out is None:
+        out = torch.empty_like(q)
+    a = _args(q, k8, v8, out, block_tables, seq_lens, scale)
+    # (q, k_new, v_new, k8, v8, k_scale, v_scale, out, tables, lens, sizes..., scale)
+    _check(load().paged_attn_append_decode_fp8(a[0], _ptr(k_new), _ptr(v_new), a[1], a[2],
+                                               _ptr(k_scale), _ptr(v_scale), a[3], *a[4:],
+                                               _stream(stream)))
     return out

@@ -94,5 +94,48 @@ def build(verbose: bool = False, force: bool = False) -> str:
     return LIB_PATH
 
 
+# A test build of the library for the bounded-wait tests only: the bf16 head_dim-128
+# kernels compiled with wait limits of a few milliseconds and two hooks that make
+# a wait run out (a ring slot left without its copy, a combiner waiting for one
+# more published part than exists).  Never loaded by the product path.
+WAIT_TEST_LIB = os.path.join(LIB_DIR, "libpaged_kv_gqa_decode_waittest.so")
+WAIT_TEST_SOURCES = ["paged_attn_api.cu", "append.cu", "decode_d128.cu"]
+WAIT_TEST_DEFINES = ["-DPAGED_ATTN_WAIT_TEST", "-DPAGED_ATTN_MBAR_SLEEPS=(1u<<14)",
+                     "-DPAGED_ATTN_PUBLISH_POLLS=(1u<<15)"]
+
+
+def build_wait_test(force: bool = False) -> str:
+    os.makedirs(LIB_DIR, exist_ok=True)
+    obj_dir = os.path.join(LIB_DIR, "obj_waittest")
+    os.makedirs(obj_dir, exist_ok=True)
+    digest = source_digest() + " " + " ".join(WAIT_TEST_DEFINES)
+    stamp = os.path.join(LIB_DIR, "build_waittest.sha256")
+    if not force and os.path.exists(WAIT_TEST_LIB) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return WAIT_TEST_LIB
+    cc = nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        cmd = [cc] + _flags() + WAIT_TEST_DEFINES + ["-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(WAIT_TEST_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, WAIT_TEST_SOURCES))
+    tmp = WAIT_TEST_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([cc] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, WAIT_TEST_LIB)
+    with open(stamp, "w") as f:
+        f.write(digest + "\n")
+    return WAIT_TEST_LIB
+
+
 if __name__ == "__main__":
     build(verbose=True, force="--force" in sys.argv)

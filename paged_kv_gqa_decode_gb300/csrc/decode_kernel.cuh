@@ -84,6 +84,14 @@ constexpr int kStatusBadLength = 2;
 constexpr int kStatusTimeout = 4;
 constexpr int kStatusConfig = 8;
 
+// Polls before the combiner gives up waiting for the other parts of a split to
+// be published (each poll sleeps ~64 ns: about 0.3 s in all).  The test build
+// of the library uses a few thousand, so that a test can make it run out fast.
+#ifndef PAGED_ATTN_PUBLISH_POLLS
+#define PAGED_ATTN_PUBLISH_POLLS (1u << 22)
+#endif
+constexpr uint32_t kPublishPolls = PAGED_ATTN_PUBLISH_POLLS;
+
 struct DecodeParams {
   const __nv_bfloat16* q;       // [num_seqs, H_q, D]
   __nv_bfloat16* out;           // [num_seqs, H_q, D]
@@ -118,6 +126,7 @@ struct DecodeParams {
   int rows;
   int chunks;
   int total_q;  // rows of q and out (offsets outside [0, total_q) are never touched)
+  int causal;   // multi-token decode: 1 = query i sees t <= seq_len - q_len + i; 0 = all t < seq_len
   // Early prologue: the caller guarantees that the work still running ahead of
   // this launch in the stream writes none of the caches (and their row floats),
   // block tables, lengths or query offsets.  The producer then reads them and
@@ -125,6 +134,14 @@ struct DecodeParams {
   // only ones to read q or the new rows, or to write out or the workspace)
   // still wait for it.
   int early;
+#ifdef PAGED_ATTN_WAIT_TEST
+  // Test build only: CTA 0 arms the ring slot of its unit `test_skip_unit` but
+  // issues no copy into it, so the consumer's bounded wait for that page runs
+  // out; CTA `test_skip_publish` never publishes its partial state, so the
+  // combiner's bounded wait for it runs out.  -1: off.
+  int test_skip_unit;
+  int test_skip_publish;
+#endif
 };
 
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
@@ -257,6 +274,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // walked sequence sw = c * N + s.
   const int NW = N * QC;
   const int cap = p.maxb * BS;
+  // Status bits are written only after the work ahead in the stream has
+  // completed: with the early prologue the producer runs before that point,
+  // and a caller that zero-fills the status word in that work must not erase
+  // what this launch reports.  (A no-op wait once it has returned, and for a
+  // launch without the programmatic attribute.)
+  auto report = [&](int bits) {
+    if (p.early) griddep_wait();
+    atomicOr(p.status, bits);
+  };
 
   // ---- 0. Programmatic dependent launch: let the next kernel in the stream be
   // scheduled as this grid's CTAs retire, and wait for the previous kernel
@@ -292,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     for (int s = s0; s < s1; ++s) {
       int len = __ldg(p.seq_lens + s);
       if (len < 0 || len > cap) {
-        if (p.num_blocks > 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        if (p.num_blocks > 0 && blockIdx.x == 0) report(kStatusBadLength);
         len = min(max(len, 0), cap);
       }
       sm_len[s] = len;
@@ -334,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       // reported; they are never read or written
       for (int s = tid; s < N; s += kThreads) {
         const int ql = sm_qo[s + 1] - sm_qo[s];
-        if (ql < 0 || (long long)ql * G > (long long)R * QC) atomicOr(p.status, kStatusBadLength);
+        if (ql < 0 || (long long)ql * G > (long long)R * QC) report(kStatusBadLength);
       }
     }
   }
@@ -359,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     return;
   }
   if (p.stages < kConsumerWarps) {  // the host plan never launches fewer
-    if (tid == 0) atomicOr(p.status, kStatusConfig);
+    if (tid == 0) report(kStatusConfig);
     return;
   }
   const long long C =
@@ -395,11 +421,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       const int sq = multi && QC > 1 ? wk.s % N : wk.s;  // the walked sequence's sequence
       int pb = __ldg(p.block_tables + (size_t)sq * p.maxb + wk.p);
       if (p.num_blocks > 0 && (pb < 0 || (long long)pb >= p.num_blocks))
-        atomicOr(p.status, kStatusBadBlock);  // the TMA bounds check reads it as zeros
+        report(kStatusBadBlock);  // the TMA bounds check reads it as zeros
       return make_int2(pb, wk.g);
     };
     int2 cur = fetch(u0 + lane);
     bool abort = false;
+    long long issued_end = u1 - u0;  // units [0, issued_end) were all issued
+    long long my_extra = -1;         // a unit past issued_end this lane issued
     for (long long ub = u0; ub < u1 && !abort; ub += 32) {
       // advance this lane's walker to its unit of the next batch and start that load
       int2 nxt = make_int2(-1, 0);
@@ -412,15 +440,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         const int j = j0 + (lane < issue_lanes ? lane : 0);
         const int pb = __shfl_sync(0xffffffffu, cur.x, j);
         const int g = __shfl_sync(0xffffffffu, cur.y, j);
-        bool bad = false;
+        bool bad = false, issued = false;
+        const long long i = ub - u0 + j;  // unit index within this CTA
         if (lane < issue_lanes && j0 + lane < cnt) {
-          const long long i = ub - u0 + j;  // unit index within this CTA
           const int stage = (int)(i % p.stages);
           const uint32_t phase = (uint32_t)((i / p.stages) & 1);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u)) {
-            atomicOr(p.status, kStatusTimeout);
+            report(kStatusTimeout);
             bad = true;
-          } else {
+          }
+#ifdef PAGED_ATTN_WAIT_TEST
+          else if (blockIdx.x == 0 && i == p.test_skip_unit) {
+            // the slot is neither armed nor filled: its consumer's wait runs out
+          }
+#endif
+          else {
+            issued = true;
             mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
             uint8_t* st = smem + stage * kStageBytes;
             if constexpr (XP) {
@@ -428,7 +463,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
               // (and V of 16-token pages) come as one bulk copy each; V of 32-token
               // pages through the tensor map, for the 64-byte swizzle (unswizzled
               // 64-byte rows would cost 4-way bank conflicts in the V reads)
-              const size_t off = ((size_t)(pb < 0 ? 0 : pb) * H_kv + g) * (size_t)(D * BS);
+              // (a block id outside a checked pool, or negative, reads block 0:
+              // a bulk copy has no bounds check of its own)
+              const long long b =
+                  pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
+              const size_t off = ((size_t)b * H_kv + g) * (size_t)(D * BS);
               bulk_load(st, p.k_cache + off, kPageBytes, &full_bar[stage]);
               if constexpr (BS == 16)
                 bulk_load(st + kPageBytes, p.v_cache + off, kPageBytes, &full_bar[stage]);
@@ -451,19 +490,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
           }
         }
         abort = __any_sync(0xffffffffu, bad);
+        if (abort) {  // a wait ran out: this wave is the last
+          issued_end = ub - u0 + j0;
+          if (issued) my_extra = i;
+        }
       }
       cur = nxt;
     }
-    // Drain: no tensor copy issued by this CTA may still be in flight when it exits.
+    // Drain: no copy issued by this CTA may still be in flight when it exits.
+    // A unit before issued_end - stages was released by its consumer (its slot
+    // was reused only after that); the last `stages` units before issued_end
+    // were issued, and so were the units of the wave that ran out whose lanes
+    // got their slot.  Every wait is bounded.
     if (lane == 0) {
-      const long long n = u1 - u0;
-      for (long long i = n > p.stages ? n - p.stages : 0; i < n; ++i) {
+      for (long long i = issued_end > p.stages ? issued_end - p.stages : 0; i < issued_end; ++i) {
+#ifdef PAGED_ATTN_WAIT_TEST
+        if (blockIdx.x == 0 && i == p.test_skip_unit) continue;  // never issued
+#endif
         if (!mbar_wait(&full_bar[i % p.stages], (uint32_t)((i / p.stages) & 1))) {
-          atomicOr(p.status, kStatusTimeout);
+          report(kStatusTimeout);
           break;
         }
       }
     }
+    if (my_extra >= 0 &&
+        !mbar_wait(&full_bar[my_extra % p.stages], (uint32_t)((my_extra / p.stages) & 1)))
+      report(kStatusTimeout);
     return;
   }
 
@@ -510,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     const int s = sw - c * N;
     const int i = (c * R + r) / G;
     const int ql = sm_qo[s + 1] - sm_qo[s];
-    return i < ql ? sm_len[s] - ql + i : 0x7fffffff;  // padding rows: anything
+    // padding rows, and every row without the causal mask: no limit
+    return i < ql && p.causal ? sm_len[s] - ql + i : 0x7fffffff;
   };
   auto prefetch_q = [&](int buf, int s, int g) {
     uint8_t* tile = sm_q + buf * kQSlotBytes;
@@ -997,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     const int part_bytes = R * kPartialRow * 4;
     const int per_round = (p.stages * kStageBytes) / part_bytes;  // >= 3 for ring >= 4 stages
     if (per_round < 1) {
-      if (ctid == 0) atomicOr(p.status, kStatusConfig);
+      if (ctid == 0) report(kStatusConfig);
       return;
     }
     const int n0 = x0.c_last - x0.c_first + 1;
@@ -1032,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       ++comb_phase;
       // one verdict for all consumer warps, so they leave (or go on) together
       if (named_barrier_or(kConsumerBarrier, kConsumerThreads, !ok)) {
-        if (ctid == 0) atomicOr(p.status, kStatusTimeout);
+        if (ctid == 0) report(kStatusTimeout);
         return;
       }
       for (int t = t0; t < t0 + nt;) {
@@ -1140,7 +1193,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // counter reaches `want`, with acquire ordering.  Only CTAs that have already
   // arrived are waited for, and they publish without waiting on anyone.
   auto wait_published = [&](const int* word, int want) -> bool {
-    for (uint32_t k = 0; k < (1u << 22); ++k) {
+    for (uint32_t k = 0; k < kPublishPolls; ++k) {
       if ((ld_acquire_gpu(word) >> 16) >= want) return true;
       __nanosleep(64);
     }
@@ -1227,7 +1280,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         if (!abort) {
           const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase));
           if (!ready) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            if (lane == 0) report(kStatusTimeout);
             abort = true;
           } else {
             const int valid = min(BS, len - pg * BS);
@@ -1277,7 +1330,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
           // makes the outcome uniform.
           const bool ready = __all_sync(0xffffffffu, mbar_wait(&full_bar[own_slot], own_phase));
           if (!ready) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            if (lane == 0) report(kStatusTimeout);
             abort = true;
           } else {
             const int valid = min(BS, len - pg * BS);
@@ -1363,7 +1416,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       sm_flag[1] = last_split && (old_l & 0xffff) == n_l - 1 ? 1 : 0;
     }
     __syncwarp();
-    if (named_barrier_or(kConsumerBarrier, kConsumerThreads, abort)) break;
+    // A CTA whose page wait ran out (status bit 2; its state is garbage) still
+    // stores, publishes and combines like the others, so every split's counter
+    // completes and is reset: the workspace stays fit for the next call.
+    named_barrier(kConsumerBarrier, kConsumerThreads);
     const bool cf = sm_flag[0] != 0, cl = sm_flag[1] != 0;
     // this CTA's part of the last piece: its place among the split's parts, and
     // whether the combine can take it from the ring instead of the workspace
@@ -1385,9 +1441,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     if (!cf && !cl) break;
     if (ctid == 0) {
       bool ok = true;
-      if (cl) ok = wait_published(word_l, n_l - 1);  // every other part
-      if (cf && ok) ok = wait_published(word_f, n_f);
-      if (!ok) atomicOr(p.status, kStatusTimeout);
+#ifdef PAGED_ATTN_WAIT_TEST
+      const int extra = p.test_skip_publish > 0 ? 1 : 0;  // one part more than exist
+#else
+      constexpr int extra = 0;
+#endif
+      if (cl) ok = wait_published(word_l, n_l - 1 + extra);  // every other part
+      if (cf && ok) ok = wait_published(word_f, n_f + extra);
+      if (!ok) report(kStatusTimeout);
       sm_flag[2] = ok ? 1 : 0;
     }
     __syncwarp();

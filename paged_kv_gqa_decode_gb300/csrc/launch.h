@@ -2,6 +2,7 @@
 // translation units (each instantiates the decode kernel for one head_dim).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 
 #include <cuda.h>
@@ -56,15 +57,25 @@ cudaError_t launch_decode_fp8_d256(int block_size, bool g16, const CUtensorMap& 
 template <int D, int BS, bool G16, int KV, bool MULTI = false>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, size_t smem, cudaStream_t stream) {
-  static int limit_set[64] = {0};
+  // The first launch of this instantiation on a device raises its dynamic
+  // shared-memory limit to all the device allows next to its static shared
+  // memory; host threads may race here, and every racer sets the same value.
+  static std::atomic<bool> limit_raised[64];
   auto kernel = paged_decode_kernel<D, BS, G16, KV, MULTI>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || limit_set[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (dev < 0 || dev >= 64 || !limit_raised[dev].load(std::memory_order_acquire)) {
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) limit_set[dev] = (int)smem;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) limit_raised[dev].store(true, std::memory_order_release);
   }
   // Programmatic stream serialization: this launch may begin while the previous
   // kernel in the stream finishes; the kernel waits for it (griddepcontrol.wait)

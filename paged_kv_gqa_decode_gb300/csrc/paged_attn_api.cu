@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <mutex>
 
 #include <cuda.h>
@@ -18,6 +19,14 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 thread_local int g_launch_flags = 0;  // paged_attn_set_launch_flags
+// paged_attn_set_checks: pool size and device status word for every call of
+// this thread (0 / null: no checks)
+thread_local long long g_check_blocks = 0;
+thread_local int32_t* g_check_status = nullptr;
+#ifdef PAGED_ATTN_WAIT_TEST
+thread_local int g_test_skip_unit = -1;
+thread_local int g_test_skip_publish = 0;
+#endif
 
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr size_t kWsAlign = 256;
@@ -72,12 +81,22 @@ int current_device(int* dev) {
   return PAGED_ATTN_OK;
 }
 
-int device_info(DeviceInfo* out) {
+int device_info(DeviceInfo* out, int* dev_out = nullptr) {
   int dev = 0;
   int rc = current_device(&dev);
   if (rc != PAGED_ATTN_OK) return rc;
+  if (dev_out) *dev_out = dev;
+  thread_local DeviceInfo tl_info[kMaxDevices];  // this thread's copy of g_info
+  if (tl_info[dev].sms > 0) {
+    *out = tl_info[dev];
+    return PAGED_ATTN_OK;
+  }
   cudaError_t e;
   std::lock_guard<std::mutex> lk(g_mu);
+  if (g_info[dev].sms > 0) {
+    *out = tl_info[dev] = g_info[dev];
+    return PAGED_ATTN_OK;
+  }
   if (g_info[dev].sms > 0) {
     *out = g_info[dev];
     return PAGED_ATTN_OK;
@@ -91,7 +110,7 @@ int device_info(DeviceInfo* out) {
   if ((e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
                                   dev)) != cudaSuccess)
     return cuda_fail(e);
-  g_info[dev] = di;
+  g_info[dev] = tl_info[dev] = di;
   *out = di;
   return PAGED_ATTN_OK;
 }
@@ -212,6 +231,33 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
   return PAGED_ATTN_OK;
 }
 
+// make_plan through a small per-thread cache: the plan depends only on the
+// sizes, the variant and the device, so a decode loop plans once.
+int cached_plan(int num_seqs, int H_q, int H_kv, int D, int BS, int dev, const DeviceInfo& di,
+                Plan* pl, bool fp8 = false, int rows = 0, int qchunks = 0) {
+  struct Entry {
+    int key[9];
+    Plan plan;
+    bool used;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry tl_plans[kEntries] = {};
+  const int key[9] = {num_seqs, H_q, H_kv, D, BS, fp8 ? 1 : 0, rows, qchunks, dev};
+  uint32_t h = 2166136261u;
+  for (int k : key) h = (h ^ (uint32_t)k) * 16777619u;
+  Entry& e = tl_plans[h % kEntries];
+  if (e.used && std::memcmp(e.key, key, sizeof key) == 0) {
+    *pl = e.plan;
+    return PAGED_ATTN_OK;
+  }
+  int rc = make_plan(num_seqs, H_q, H_kv, D, BS, di, pl, fp8, rows, qchunks);
+  if (rc != PAGED_ATTN_OK) return rc;
+  std::memcpy(e.key, key, sizeof key);
+  e.plan = *pl;
+  e.used = true;
+  return PAGED_ATTN_OK;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -303,6 +349,11 @@ int encode_xpacked_maps(const void* v, int D, int BS, int H_kv, long long num_bl
 cudaError_t launch_dim(int D, int BS, bool g16, bool fp8, bool xp, const CUtensorMap& tk,
                        const CUtensorMap& tv, const DecodeParams& p, int grid, size_t smem,
                        cudaStream_t st) {
+#ifdef PAGED_ATTN_WAIT_TEST
+  // the test build carries the single-token bf16 head_dim-128 kernels only
+  if (p.qo_indptr != nullptr || xp || fp8 || D != 128) return cudaErrorNotSupported;
+  return launch_decode_d128(BS, g16, tk, tv, p, grid, smem, st);
+#endif
   if (p.qo_indptr != nullptr) {
     if (D == 64) return launch_decode_multi_d64(BS, g16, tk, tv, p, grid, smem, st);
     if (D == 128) return launch_decode_multi_d128(BS, g16, tk, tv, p, grid, smem, st);
@@ -329,60 +380,143 @@ int check_pointers(const void* q, const void* k, const void* v, const void* out,
   return PAGED_ATTN_OK;
 }
 
+// The tensor maps of a call through a per-thread direct-mapped cache: a map
+// depends only on the base address and the sizes it describes, so a decode
+// loop over the same caches encodes each once.
+enum MapKind { kMapBf16 = 0, kMapFp8 = 1, kMapXpackedV = 2 };
+
+int cached_map(const void* base, int D, int BS, int H_kv, long long num_blocks, MapKind kind,
+               CUtensorMap* out) {
+  struct Entry {
+    CUtensorMap map;
+    const void* base;
+    long long num_blocks;
+    int D, BS, H_kv, kind;
+    bool used;
+  };
+  constexpr int kEntries = 256;
+  thread_local std::unique_ptr<Entry[]> tl_maps;
+  if (!tl_maps) tl_maps.reset(new Entry[kEntries]());
+  const uint64_t a = reinterpret_cast<uintptr_t>(base);
+  const uint64_t h = (a >> 8) * 0x9E3779B97F4A7C15ull ^ ((uint64_t)kind << 1) ^
+                     ((uint64_t)D * 31 + (uint64_t)BS * 7 + (uint64_t)H_kv);
+  Entry& e = tl_maps[(h >> 32) % kEntries];
+  if (e.used && e.base == base && e.num_blocks == num_blocks && e.D == D && e.BS == BS &&
+      e.H_kv == H_kv && e.kind == kind) {
+    *out = e.map;
+    return PAGED_ATTN_OK;
+  }
+  CUtensorMap m;
+  int rc;
+  if (kind == kMapXpackedV) {
+    CUtensorMap unused;
+    rc = encode_xpacked_maps(base, D, BS, H_kv, num_blocks, &unused, &m);
+  } else {
+    rc = encode_cache_map(base, D, BS, H_kv, num_blocks, &m, kind == kMapFp8);
+  }
+  if (rc != PAGED_ATTN_OK) return rc;
+  e.map = m;
+  e.base = base;
+  e.num_blocks = num_blocks;
+  e.D = D;
+  e.BS = BS;
+  e.H_kv = H_kv;
+  e.kind = kind;
+  e.used = true;
+  *out = m;
+  return PAGED_ATTN_OK;
+}
+
+// Everything one decode call hands to its launches.
+struct Operands {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  void* out;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  int num_seqs, H_q, H_kv, maxb;
+  float scale;
+  void* ws;                         // workspace (status word, counters, partials)
+  int32_t* status = nullptr;        // caller status word (null: the workspace's)
+  long long num_blocks = 0;         // > 0: block ids checked against the pool
+  bool early = false;               // early-prologue launch (caller's guarantee holds)
+  const void* k_new = nullptr;      // fused cache append (bf16)
+  const void* v_new = nullptr;
+  const float* k_scale = nullptr;   // FP8 row floats
+  const float* v_scale = nullptr;
+  const int32_t* qo_indptr = nullptr;  // multi-token decode
+  int total_q = 0;
+  int causal = 1;
+};
+
+// The calling thread's device-side checks (paged_attn_set_checks), if any.
+void apply_checks(Operands* o) {
+  if (g_check_blocks > 0) {
+    o->num_blocks = g_check_blocks;
+    o->status = g_check_status;
+  }
+}
+
+// The early prologue applies when the caller asked for it on this thread and
+// nothing the library itself launched just before writes what the producer
+// reads ahead of the wait.
+bool early_requested() { return (g_launch_flags & PAGED_ATTN_FLAG_EARLY_PROLOGUE) != 0; }
+
 // Runs the whole operation in chunks of plan.chunk sequences on `stream`.
-// With k_new / v_new (else null), each sequence's new token is first written
-// into the caches by the decode kernel itself (fused cache append).
-int run(const Plan& pl, const void* q, const void* k_cache, const void* v_cache, void* out,
-        const int32_t* bt, const int32_t* seq_lens, int num_seqs, int H_q, int H_kv,
-        int max_blocks_per_seq, float scale, void* ws, int32_t* status, long long num_blocks,
-        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
-        const float* k_scale = nullptr, const float* v_scale = nullptr,
-        const int32_t* qo_indptr = nullptr, int total_q = 0) {
+int run(const Plan& pl, const Operands& o, cudaStream_t stream) {
   CUtensorMap tk, tv;
   int rc;
   if (pl.xp) {
-    rc = encode_xpacked_maps(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, &tv);
+    rc = cached_map(o.v_cache, pl.D, pl.BS, o.H_kv, o.num_blocks, kMapXpackedV, &tv);
     if (rc != PAGED_ATTN_OK) return rc;
+    tk = tv;  // unused by the x-packed kernel
   } else {
-    rc = encode_cache_map(k_cache, pl.D, pl.BS, H_kv, num_blocks, &tk, pl.fp8);
+    const MapKind kind = pl.fp8 ? kMapFp8 : kMapBf16;
+    rc = cached_map(o.k_cache, pl.D, pl.BS, o.H_kv, o.num_blocks, kind, &tk);
     if (rc != PAGED_ATTN_OK) return rc;
-    rc = encode_cache_map(v_cache, pl.D, pl.BS, H_kv, num_blocks, &tv, pl.fp8);
+    rc = cached_map(o.v_cache, pl.D, pl.BS, o.H_kv, o.num_blocks, kind, &tv);
     if (rc != PAGED_ATTN_OK) return rc;
   }
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  for (int s0 = 0; s0 < num_seqs; s0 += pl.chunk) {
-    const int n = num_seqs - s0 < pl.chunk ? num_seqs - s0 : pl.chunk;
+  uint8_t* wsb = static_cast<uint8_t*>(o.ws);
+  for (int s0 = 0; s0 < o.num_seqs; s0 += pl.chunk) {
+    const int n = o.num_seqs - s0 < pl.chunk ? o.num_seqs - s0 : pl.chunk;
     DecodeParams p;
     // multi-token decode: q and out rows are found through qo_indptr (absolute)
-    const size_t row0 = qo_indptr ? 0 : (size_t)s0;
-    p.q = static_cast<const __nv_bfloat16*>(q) + row0 * H_q * pl.D;
-    p.out = static_cast<__nv_bfloat16*>(out) + row0 * H_q * pl.D;
-    p.qo_indptr = qo_indptr ? qo_indptr + s0 : nullptr;
+    const size_t row0 = o.qo_indptr ? 0 : (size_t)s0;
+    p.q = static_cast<const __nv_bfloat16*>(o.q) + row0 * o.H_q * pl.D;
+    p.out = static_cast<__nv_bfloat16*>(o.out) + row0 * o.H_q * pl.D;
+    p.qo_indptr = o.qo_indptr ? o.qo_indptr + s0 : nullptr;
     p.rows = pl.rows;
     p.chunks = pl.qchunks > 0 ? pl.qchunks : 1;
-    p.total_q = total_q;
-    p.block_tables = bt + (size_t)s0 * max_blocks_per_seq;
-    p.seq_lens = seq_lens + s0;
+    p.total_q = o.total_q;
+    p.causal = o.causal;
+    p.block_tables = o.bt + (size_t)s0 * o.maxb;
+    p.seq_lens = o.seq_lens + s0;
     p.num_seqs = n;
-    p.H_q = H_q;
-    p.H_kv = H_kv;
+    p.H_q = o.H_q;
+    p.H_kv = o.H_kv;
     p.G = pl.G;
-    p.maxb = max_blocks_per_seq;
+    p.maxb = o.maxb;
     p.stages = pl.stages;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.status = status ? status : reinterpret_cast<int32_t*>(wsb);
+    p.scale_log2 = o.scale * 1.4426950408889634f;
+    p.status = o.status ? o.status : reinterpret_cast<int32_t*>(wsb);
     p.counters = reinterpret_cast<int32_t*>(wsb + pl.off_counters);
     p.partials = reinterpret_cast<float*>(wsb + pl.off_partials);
-    p.num_blocks = num_blocks;
-    p.early = (g_launch_flags & PAGED_ATTN_FLAG_EARLY_PROLOGUE) ? 1 : 0;
-    p.k_new = k_new ? static_cast<const __nv_bfloat16*>(k_new) + (size_t)s0 * H_kv * pl.D
-                    : nullptr;
-    p.v_new = v_new ? static_cast<const __nv_bfloat16*>(v_new) + (size_t)s0 * H_kv * pl.D
-                    : nullptr;
-    p.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
-    p.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
+    p.num_blocks = o.num_blocks;
+    p.early = o.early ? 1 : 0;
+    p.k_new = o.k_new ? static_cast<const __nv_bfloat16*>(o.k_new) + (size_t)s0 * o.H_kv * pl.D
+                      : nullptr;
+    p.v_new = o.v_new ? static_cast<const __nv_bfloat16*>(o.v_new) + (size_t)s0 * o.H_kv * pl.D
+                      : nullptr;
+    p.k_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(o.k_cache));
+    p.v_cache = static_cast<__nv_bfloat16*>(const_cast<void*>(o.v_cache));
+    p.k_scale = o.k_scale;
+    p.v_scale = o.v_scale;
+#ifdef PAGED_ATTN_WAIT_TEST
+    p.test_skip_unit = g_test_skip_unit;
+    p.test_skip_publish = g_test_skip_publish;
+#endif
     cudaError_t e =
         launch_dim(pl.D, pl.BS, pl.g16, pl.fp8, pl.xp, tk, tv, p, pl.grid, pl.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -453,6 +587,125 @@ int common_checks(const void* q, const void* k, const void* v, const void* out, 
   return check_pointers(q, k, v, out, bt, sl);
 }
 
+// A decode call's operands with the caller's pointers and sizes.
+Operands operands(const void* q, const void* k_cache, const void* v_cache, void* out,
+                  const int32_t* bt, const int32_t* sl, int num_seqs, int H_q, int H_kv,
+                  int max_blocks_per_seq, float scale) {
+  Operands o;
+  o.q = q;
+  o.k_cache = k_cache;
+  o.v_cache = v_cache;
+  o.out = out;
+  o.bt = bt;
+  o.seq_lens = sl;
+  o.num_seqs = num_seqs;
+  o.H_q = H_q;
+  o.H_kv = H_kv;
+  o.maxb = max_blocks_per_seq;
+  o.scale = scale;
+  o.ws = nullptr;
+  return o;
+}
+
+// Plans a decode launch on the current device and runs it in the library-owned
+// workspace (o.ws null) or the one given.  rows > 0: multi-token pieces.
+int plan_and_run(Operands& o, int head_dim, int block_size, bool fp8, bool xp, int rows,
+                 int qchunks, cudaStream_t st) {
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(&di, &dev);
+  if (rc != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  rc = cached_plan(o.num_seqs, o.H_q, o.H_kv, head_dim, block_size, dev, di, &pl, fp8, rows,
+                   qchunks);
+  if (rc != PAGED_ATTN_OK) return rc;
+  pl.xp = xp;  // same shared-memory plan as the bf16 layout
+  if (o.ws == nullptr && (rc = owned_workspace(pl.ws_bytes, st, &o.ws)) != PAGED_ATTN_OK)
+    return rc;
+  return run(pl, o, st);
+}
+
+AppendParams append_params(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const int32_t* bt, const int32_t* sl, int num_seqs, int H_kv,
+                           int head_dim, int max_blocks_per_seq, int block_size) {
+  AppendParams a;
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = nullptr;
+  a.v_scale = nullptr;
+  a.block_tables = bt;
+  a.seq_lens = sl;
+  a.qo_indptr = nullptr;
+  a.num_seqs = num_seqs;
+  a.total_q = 0;
+  a.H_kv = H_kv;
+  a.D = head_dim;
+  a.maxb = max_blocks_per_seq;
+  a.BS = block_size;
+  a.num_blocks = g_check_blocks;
+  a.status = g_check_blocks > 0 ? g_check_status : nullptr;
+  return a;
+}
+
+int sms_of_device(int* sms) {
+  DeviceInfo di;
+  int rc = device_info(&di);
+  if (rc == PAGED_ATTN_OK) *sms = di.sms;
+  return rc;
+}
+
+int multi_checks(const void* q, const void* k_cache, const void* v_cache, const void* out,
+                 const int32_t* qo_indptr, const int32_t* bt, const int32_t* sl, int num_seqs,
+                 int total_q, int max_q_len, int H_q, int H_kv, int head_dim,
+                 int max_blocks_per_seq, int block_size, float scale) {
+  int rc = validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return PAGED_ATTN_ERR_SCALE;
+  const int G = H_q / H_kv;
+  if (total_q < 0 || max_q_len < 1 || (long long)max_q_len * G > kMaxMultiRows ||
+      (long long)total_q * H_q * head_dim >= (1LL << 40))
+    return PAGED_ATTN_ERR_SIZES;
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  rc = check_pointers(q, k_cache, v_cache, out, bt, sl);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (!aligned16(qo_indptr)) return PAGED_ATTN_ERR_POINTER;
+  return PAGED_ATTN_OK;
+}
+
+int decode_multi_impl(const void* q, const void* k_cache, const void* v_cache, void* out,
+                      const int32_t* qo_indptr, const int32_t* bt, const int32_t* sl,
+                      int num_seqs, int total_q, int max_q_len, int H_q, int H_kv, int head_dim,
+                      int max_blocks_per_seq, int block_size, float scale, int causal, bool early,
+                      cudaStream_t st) {
+  Operands o = operands(q, k_cache, v_cache, out, bt, sl, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.qo_indptr = qo_indptr;
+  o.total_q = total_q;
+  o.causal = causal ? 1 : 0;
+  o.early = early;
+  apply_checks(&o);
+  // one n8 MMA tile of rows when a KV head's q_len * G rows fit, else pieces of 16
+  const int G = H_q / H_kv;
+  const int rows = max_q_len * G <= 8 ? 8 : 16;
+  const int qchunks = (max_q_len * G + rows - 1) / rows;
+  return plan_and_run(o, head_dim, block_size, false, false, rows, qchunks, st);
+}
+
+int fp8_checks(const void* q, const void* k8, const void* v8, const void* k_scale,
+               const void* v_scale, const void* out, const int32_t* bt, const int32_t* sl,
+               int num_seqs, int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+               int block_size, float scale) {
+  int rc = common_checks(q, k8, v8, out, bt, sl, num_seqs, H_q, H_kv, head_dim,
+                         max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (head_dim == 64) return PAGED_ATTN_ERR_HEAD_DIM;  // FP8 pages need 128-byte rows
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  if (!aligned16(k_scale) || !aligned16(v_scale)) return PAGED_ATTN_ERR_POINTER;
+  return PAGED_ATTN_OK;
+}
+
 }  // namespace
 }  // namespace pagedattn
 
@@ -467,16 +720,12 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache, v
   int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
                          head_dim, max_blocks_per_seq, block_size, scale);
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
-    return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.early = early_requested();
+  apply_checks(&o);
+  return plan_and_run(o, head_dim, block_size, false, false, 0, 0,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_decode_multi(const void* q, const void* k_cache, const void* v_cache, void* out,
@@ -484,32 +733,24 @@ int paged_attn_decode_multi(const void* q, const void* k_cache, const void* v_ca
                             const int32_t* seq_lens, int num_seqs, int total_q, int max_q_len,
                             int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
                             int block_size, float scale, void* stream) {
-  int rc = validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size);
-  if (rc != PAGED_ATTN_OK) return rc;
-  if (!std::isfinite(scale)) return PAGED_ATTN_ERR_SCALE;
-  const int G = H_q / H_kv;
-  if (total_q < 0 || max_q_len < 1 || (long long)max_q_len * G > kMaxMultiRows ||
-      (long long)total_q * H_q * head_dim >= (1LL << 40))
-    return PAGED_ATTN_ERR_SIZES;
-  if (num_seqs == 0) return PAGED_ATTN_OK;
-  rc = check_pointers(q, k_cache, v_cache, out, block_tables, seq_lens);
-  if (rc != PAGED_ATTN_OK) return rc;
-  if (!aligned16(qo_indptr)) return PAGED_ATTN_ERR_POINTER;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  // one n8 MMA tile of rows when a KV head's q_len * G rows fit, else pieces of 16
-  const int rows = max_q_len * G <= 8 ? 8 : 16;
-  const int qchunks = (max_q_len * G + rows - 1) / rows;
-  Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl, false, rows,
-                      qchunks)) != PAGED_ATTN_OK)
-    return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st, nullptr, nullptr, nullptr, nullptr,
-             qo_indptr, total_q);
+  return paged_attn_decode_multi_ex(q, k_cache, v_cache, out, qo_indptr, block_tables, seq_lens,
+                                    num_seqs, total_q, max_q_len, H_q, H_kv, head_dim,
+                                    max_blocks_per_seq, block_size, scale, 1, stream);
+}
+
+int paged_attn_decode_multi_ex(const void* q, const void* k_cache, const void* v_cache,
+                               void* out, const int32_t* qo_indptr, const int32_t* block_tables,
+                               const int32_t* seq_lens, int num_seqs, int total_q, int max_q_len,
+                               int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
+                               int block_size, float scale, int is_causal, void* stream) {
+  int rc = multi_checks(q, k_cache, v_cache, out, qo_indptr, block_tables, seq_lens, num_seqs,
+                        total_q, max_q_len, H_q, H_kv, head_dim, max_blocks_per_seq, block_size,
+                        scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  return decode_multi_impl(q, k_cache, v_cache, out, qo_indptr, block_tables, seq_lens, num_seqs,
+                           total_q, max_q_len, H_q, H_kv, head_dim, max_blocks_per_seq,
+                           block_size, scale, is_causal, early_requested(),
+                           static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_decode_xpacked(const void* q, const void* k_cache, const void* v_cache, void* out,
@@ -519,17 +760,12 @@ int paged_attn_decode_xpacked(const void* q, const void* k_cache, const void* v_
   int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
                          head_dim, max_blocks_per_seq, block_size, scale);
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
-    return rc;
-  pl.xp = true;  // same shared-memory plan as the bf16 layout
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.early = early_requested();
+  apply_checks(&o);
+  return plan_and_run(o, head_dim, block_size, false, true, 0, 0,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
@@ -537,23 +773,17 @@ int paged_attn_decode_fp8(const void* q, const void* k_cache, const void* v_cach
                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                           int H_q, int H_kv, int head_dim, int max_blocks_per_seq,
                           int block_size, float scale, void* stream) {
-  int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-                         head_dim, max_blocks_per_seq, block_size, scale);
-  if (rc != PAGED_ATTN_OK) return rc;
-  if (head_dim == 64) return PAGED_ATTN_ERR_HEAD_DIM;  // FP8 pages need 128-byte rows
-  if (num_seqs == 0) return PAGED_ATTN_OK;
-  if (!aligned16(k_scale) || !aligned16(v_scale)) return PAGED_ATTN_ERR_POINTER;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl, true)) !=
-      PAGED_ATTN_OK)
-    return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st, nullptr, nullptr, k_scale, v_scale);
+  int rc = fp8_checks(q, k_cache, v_cache, k_scale, v_scale, out, block_tables, seq_lens,
+                      num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.k_scale = k_scale;
+  o.v_scale = v_scale;
+  o.early = early_requested();
+  apply_checks(&o);
+  return plan_and_run(o, head_dim, block_size, true, false, 0, 0,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -565,14 +795,18 @@ int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new
                          head_dim, max_blocks_per_seq, block_size, scale);
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
   if (!aligned16(k_new) || !aligned16(v_new)) return PAGED_ATTN_ERR_POINTER;
+  int dev = 0;
   DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  if ((rc = device_info(&di, &dev)) != PAGED_ATTN_OK) return rc;
   Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+  if ((rc = cached_plan(num_seqs, H_q, H_kv, head_dim, block_size, dev, di, &pl)) !=
+      PAGED_ATTN_OK)
     return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  apply_checks(&o);
+  if ((rc = owned_workspace(pl.ws_bytes, st, &o.ws)) != PAGED_ATTN_OK) return rc;
   // Fused, the warp that reads a piece's last page patches the new rows into it,
   // a small cost per piece on that CTA's path.  When CTAs average kAppendApartPieces
   // or more (s, g) pieces, the CTA crossing the most short sequences sets the
@@ -580,26 +814,21 @@ int paged_attn_append_decode(const void* q, const void* k_new, const void* v_new
   // (ragged 256-sequence batch: decode 619 us, fused 630, apart 622; LLaMA-shaped
   // batch: decode 51.3, fused 51.6, apart 53.4).  Both give the same bits.
   if ((long long)num_seqs * H_kv >= (long long)kAppendApartPieces * pl.grid) {
-    AppendParams a;
-    a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-    a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-    a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-    a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.num_seqs = num_seqs;
-    a.H_kv = H_kv;
-    a.D = head_dim;
-    a.maxb = max_blocks_per_seq;
-    a.BS = block_size;
-    a.num_blocks = 0;
+    AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                   num_seqs, H_kv, head_dim, max_blocks_per_seq, block_size);
     cudaError_t e = launch_append(a, di.sms, st);
     if (e != cudaSuccess) return cuda_fail(e);
-    return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-               max_blocks_per_seq, scale, ws, nullptr, 0, st);
+    // The append just written is what the decode's producer reads first: the
+    // decode waits for it before any global access (no early prologue).
+    o.early = false;
+    return run(pl, o, st);
   }
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st, k_new, v_new);
+  // Fused: the new rows are patched into the pages in shared memory, whatever
+  // the producer's copy brought, so the early prologue stays as requested.
+  o.early = early_requested();
+  o.k_new = k_new;
+  o.v_new = v_new;
+  return run(pl, o, st);
 }
 
 int paged_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
@@ -611,23 +840,113 @@ int paged_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(block_tables) || !aligned16(seq_lens))
     return PAGED_ATTN_ERR_POINTER;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  AppendParams a;
-  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  a.block_tables = block_tables;
-  a.seq_lens = seq_lens;
-  a.num_seqs = num_seqs;
-  a.H_kv = H_kv;
-  a.D = head_dim;
-  a.maxb = max_blocks_per_seq;
-  a.BS = block_size;
-  a.num_blocks = 0;
-  cudaError_t e = launch_append(a, di.sms, static_cast<cudaStream_t>(stream));
+  int sms = 0;
+  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                 H_kv, head_dim, max_blocks_per_seq, block_size);
+  cudaError_t e = launch_append(a, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PAGED_ATTN_OK : cuda_fail(e);
+}
+
+int paged_kv_append_multi(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const int32_t* qo_indptr, const int32_t* block_tables,
+                          const int32_t* seq_lens, int num_seqs, int total_q, int H_kv,
+                          int head_dim, int max_blocks_per_seq, int block_size, void* stream) {
+  int rc = validate_sizes(num_seqs, H_kv, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (total_q < 0 || (long long)total_q * H_kv * head_dim >= (1LL << 40))
+    return PAGED_ATTN_ERR_SIZES;
+  if (num_seqs == 0 || total_q == 0) return PAGED_ATTN_OK;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(qo_indptr) || !aligned16(block_tables) || !aligned16(seq_lens))
+    return PAGED_ATTN_ERR_POINTER;
+  int sms = 0;
+  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                 H_kv, head_dim, max_blocks_per_seq, block_size);
+  a.qo_indptr = qo_indptr;
+  a.total_q = total_q;
+  cudaError_t e = launch_append(a, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PAGED_ATTN_OK : cuda_fail(e);
+}
+
+int paged_attn_append_decode_multi(const void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, void* out,
+                                   const int32_t* qo_indptr, const int32_t* block_tables,
+                                   const int32_t* seq_lens, int num_seqs, int total_q,
+                                   int max_q_len, int H_q, int H_kv, int head_dim,
+                                   int max_blocks_per_seq, int block_size, float scale,
+                                   int is_causal, void* stream) {
+  int rc = multi_checks(q, k_cache, v_cache, out, qo_indptr, block_tables, seq_lens, num_seqs,
+                        total_q, max_q_len, H_q, H_kv, head_dim, max_blocks_per_seq, block_size,
+                        scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PAGED_ATTN_ERR_POINTER;
+  int sms = 0;
+  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (total_q > 0) {
+    AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                   num_seqs, H_kv, head_dim, max_blocks_per_seq, block_size);
+    a.qo_indptr = qo_indptr;
+    a.total_q = total_q;
+    cudaError_t e = launch_append(a, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // the decode reads the rows just appended: plain launch (no early prologue)
+  return decode_multi_impl(q, k_cache, v_cache, out, qo_indptr, block_tables, seq_lens, num_seqs,
+                           total_q, max_q_len, H_q, H_kv, head_dim, max_blocks_per_seq,
+                           block_size, scale, is_causal, false, st);
+}
+
+int paged_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                        float* k_scale, float* v_scale, const int32_t* block_tables,
+                        const int32_t* seq_lens, int num_seqs, int H_kv, int head_dim,
+                        int max_blocks_per_seq, int block_size, void* stream) {
+  int rc = validate_sizes(num_seqs, H_kv, H_kv, head_dim, max_blocks_per_seq, block_size);
+  if (rc != PAGED_ATTN_OK) return rc;
+  if (head_dim == 64) return PAGED_ATTN_ERR_HEAD_DIM;  // as the FP8 decode
+  if (num_seqs == 0) return PAGED_ATTN_OK;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scale) || !aligned16(v_scale) || !aligned16(block_tables) ||
+      !aligned16(seq_lens))
+    return PAGED_ATTN_ERR_POINTER;
+  int sms = 0;
+  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                 H_kv, head_dim, max_blocks_per_seq, block_size);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  cudaError_t e = launch_append_fp8(a, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PAGED_ATTN_OK : cuda_fail(e);
+}
+
+int paged_attn_append_decode_fp8(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                 void* out, const int32_t* block_tables, const int32_t* seq_lens,
+                                 int num_seqs, int H_q, int H_kv, int head_dim,
+                                 int max_blocks_per_seq, int block_size, float scale,
+                                 void* stream) {
+  int rc = fp8_checks(q, k_cache, v_cache, k_scale, v_scale, out, block_tables, seq_lens,
+                      num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size, scale);
+  if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PAGED_ATTN_ERR_POINTER;
+  int sms = 0;
+  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                 H_kv, head_dim, max_blocks_per_seq, block_size);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  cudaError_t e = launch_append_fp8(a, sms, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.k_scale = k_scale;
+  o.v_scale = v_scale;
+  o.early = false;  // the decode reads the rows just appended
+  apply_checks(&o);
+  return plan_and_run(o, head_dim, block_size, true, false, 0, 0, st);
 }
 
 size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
@@ -635,10 +954,12 @@ size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,
   if (validate_sizes(num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size) !=
       PAGED_ATTN_OK)
     return 0;
+  int dev = 0;
   DeviceInfo di;
-  if (device_info(&di) != PAGED_ATTN_OK) return 0;
+  if (device_info(&di, &dev) != PAGED_ATTN_OK) return 0;
   Plan pl;
-  if (make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl) != PAGED_ATTN_OK) return 0;
+  if (cached_plan(num_seqs, H_q, H_kv, head_dim, block_size, dev, di, &pl) != PAGED_ATTN_OK)
+    return 0;
   return pl.ws_bytes;
 }
 
@@ -651,14 +972,20 @@ int paged_attn_decode_ws(const void* q, const void* k_cache, const void* v_cache
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0)
     return PAGED_ATTN_ERR_WORKSPACE;
+  int dev = 0;
   DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  if ((rc = device_info(&di, &dev)) != PAGED_ATTN_OK) return rc;
   Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+  if ((rc = cached_plan(num_seqs, H_q, H_kv, head_dim, block_size, dev, di, &pl)) !=
+      PAGED_ATTN_OK)
     return rc;
   if (workspace_bytes < pl.ws_bytes) return PAGED_ATTN_ERR_WORKSPACE;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, workspace, nullptr, 0, static_cast<cudaStream_t>(stream));
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.ws = workspace;
+  o.early = early_requested();
+  apply_checks(&o);
+  return run(pl, o, static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_cache, void* out,
@@ -672,16 +999,13 @@ int paged_attn_decode_checked(const void* q, const void* k_cache, const void* v_
   if (num_blocks <= 0 || num_blocks > 0x7fffffffLL) return PAGED_ATTN_ERR_SIZES;
   if (d_status == nullptr || (reinterpret_cast<uintptr_t>(d_status) & 3) != 0)
     return PAGED_ATTN_ERR_POINTER;
-  DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
-  Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
-    return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  if ((rc = owned_workspace(pl.ws_bytes, st, &ws)) != PAGED_ATTN_OK) return rc;
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, d_status, num_blocks, st);
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.num_blocks = num_blocks;
+  o.status = d_status;
+  o.early = early_requested();
+  return plan_and_run(o, head_dim, block_size, false, false, 0, 0,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
@@ -691,21 +1015,29 @@ int paged_attn_decode_static(const void* q, const void* k_cache, const void* v_c
   int rc = common_checks(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
                          head_dim, max_blocks_per_seq, block_size, scale);
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
+  int dev = 0;
   DeviceInfo di;
-  if ((rc = device_info(&di)) != PAGED_ATTN_OK) return rc;
+  if ((rc = device_info(&di, &dev)) != PAGED_ATTN_OK) return rc;
   Plan pl;
-  if ((rc = make_plan(num_seqs, H_q, H_kv, head_dim, block_size, di, &pl)) != PAGED_ATTN_OK)
+  if ((rc = cached_plan(num_seqs, H_q, H_kv, head_dim, block_size, dev, di, &pl)) !=
+      PAGED_ATTN_OK)
     return rc;
   if (pl.ws_bytes > kStaticScratchBytes) return PAGED_ATTN_ERR_STATIC_SCRATCH;
   void* ws = nullptr;
   if ((rc = static_scratch_address(&ws)) != PAGED_ATTN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left; the status word and the
-  // combine counters must start at zero.
+  // combine counters must start at zero.  The memset is a plain stream
+  // operation ahead of the launch, which then waits for it before touching the
+  // array (the early prologue only reads the caller's tables and caches early).
   cudaError_t e = cudaMemsetAsync(ws, 0, pl.off_partials, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  return run(pl, q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
-             max_blocks_per_seq, scale, ws, nullptr, 0, st);
+  Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
+                        max_blocks_per_seq, scale);
+  o.ws = ws;
+  o.early = early_requested();
+  apply_checks(&o);
+  return run(pl, o, st);
 }
 
 const char* paged_attn_status_string(int status) {
@@ -732,8 +1064,46 @@ int paged_attn_set_launch_flags(int flags) {
   return PAGED_ATTN_OK;
 }
 
+int paged_attn_set_checks(long long num_blocks, int32_t* d_status) {
+  if (num_blocks <= 0 && d_status == nullptr) {
+    g_check_blocks = 0;
+    g_check_status = nullptr;
+    return PAGED_ATTN_OK;
+  }
+  if (num_blocks <= 0 || num_blocks > 0x7fffffffLL) return PAGED_ATTN_ERR_SIZES;
+  if (d_status == nullptr || (reinterpret_cast<uintptr_t>(d_status) & 3) != 0)
+    return PAGED_ATTN_ERR_POINTER;
+  g_check_blocks = num_blocks;
+  g_check_status = d_status;
+  return PAGED_ATTN_OK;
+}
+
+int paged_attn_reset_workspace(void* stream) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != PAGED_ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const OwnedWorkspace& w = g_ws[dev];
+  if (w.ptr == nullptr) return PAGED_ATTN_OK;
+  cudaError_t e = cudaMemsetAsync(w.ptr, 0, w.bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PAGED_ATTN_OK : cuda_fail(e);
+}
+
 int paged_attn_last_cuda_error(void) { return g_last_cuda_error; }
 
-int paged_attn_version(void) { return 100; }
+int paged_attn_version(void) { return 200; }
+
+#ifdef PAGED_ATTN_WAIT_TEST
+// Test build only (not in include/paged_attn.h): the next decode launches of
+// this thread leave unit `skip_unit` of CTA 0's range without a copy (-1: off)
+// and, with skip_publish != 0, make every combiner wait for one more published
+// part than exists, so the bounded waits run out.
+__attribute__((visibility("default"))) int paged_attn_test_set_wait_faults(int skip_unit,
+                                                                           int skip_publish) {
+  g_test_skip_unit = skip_unit;
+  g_test_skip_publish = skip_publish;
+  return PAGED_ATTN_OK;
+}
+#endif
 
 }  // extern "C"

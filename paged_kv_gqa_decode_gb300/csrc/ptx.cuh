@@ -49,12 +49,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Sleeping polls of an mbarrier wait before it gives up (each sleeps ~256 ns:
+// about a second in all).  The test build of the library uses a few thousand,
+// so that a test can make a wait run out fast.
+#ifndef PAGED_ATTN_MBAR_SLEEPS
+#define PAGED_ATTN_MBAR_SLEEPS (1u << 22)
+#endif
+
 // Waits for the phase with the given parity to complete.  Gives up after a
-// bounded number of polls (a few seconds) and returns false, so a lost
-// arrival can never hang the GPU.
+// bounded number of polls and returns false, so a lost arrival can never hang
+// the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   constexpr uint32_t kSpins = 1u << 12;
-  constexpr uint32_t kSleeps = 1u << 22;
+  constexpr uint32_t kSleeps = PAGED_ATTN_MBAR_SLEEPS;
   for (uint32_t i = 0; i < kSpins; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kSleeps; ++i) {

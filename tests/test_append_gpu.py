@@ -136,3 +136,153 @@ def test_append_rejects_bad_arguments():
                              w.v_cache.data_ptr(), w.block_tables.data_ptr(),
                              w.seq_lens.data_ptr(), 2, 2, 96, 7, 16, 0)
     assert rc == -3  # head_dim
+
+
+# ---------------------------------------------------------------- early prologue
+# With FLAG_EARLY_PROLOGUE the decode's producer reads the tables and starts its
+# page copies before the work ahead of it has finished.  The append-and-decode
+# call must not let its own append break that: where the append is a launch of
+# its own (many (sequence, KV head) pieces per CTA, e.g. the ragged 256-sequence
+# batch) the decode after it is a plain launch; where the append is fused (the
+# LLaMA-shaped batch) the new rows are patched in shared memory.
+
+@pytest.mark.parametrize("name", ["ragged256", "llama8b"])
+def test_append_decode_with_early_prologue_back_to_back(name):
+    """Two append-and-decode steps back to back under the early prologue, each after
+    a kernel that writes q (the usual layer loop), against the oracle and bit for
+    bit against the same steps with the flag off."""
+    results = []
+    for flag in (pa.FLAG_EARLY_PROLOGUE, 0):
+        w = workloads.make(name, seed=31, device="cuda", poison="nan")
+        before = workloads.host_copy(w)
+        q0 = w.q.clone()
+        k1, v1 = new_rows(w, 32)
+        k2, v2 = new_rows(w, 33)
+        pa.paged_attn_set_launch_flags(flag)
+        try:
+            w.q.copy_(q0 * 2)  # the kernel ahead writes q
+            o1 = pa.paged_attn_append_decode(w.q, k1, v1, w.k_cache, w.v_cache,
+                                             w.block_tables, w.seq_lens, w.scale)
+            o1 = o1.clone()
+            w.q.copy_(q0)
+            o2 = pa.paged_attn_append_decode(w.q, k2, v2, w.k_cache, w.v_cache,
+                                             w.block_tables, w.seq_lens, w.scale)
+            torch.cuda.synchronize()
+        finally:
+            pa.paged_attn_set_launch_flags(0)
+        results.append((o1, o2, w.k_cache, w.v_cache))
+        if flag:
+            step1 = oracle.append(before, k1, v1)
+            step1.q = oracle.Inputs(q0 * 2, w.k_cache[:1], w.v_cache[:1], w.block_tables,
+                                    w.seq_lens, w.scale).q
+            assert_parity(o1, oracle.decode(step1), f"{name} first step")
+            step2 = oracle.append(step1, k2, v2)
+            step2.q = oracle.Inputs(q0, w.k_cache[:1], w.v_cache[:1], w.block_tables,
+                                    w.seq_lens, w.scale).q
+            assert np.array_equal(cache_bits(w.k_cache), step2.k)
+            assert np.array_equal(cache_bits(w.v_cache), step2.v)
+            assert_parity(o2, oracle.decode(step2), f"{name} second step")
+    for a, b in zip(results[0], results[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------- multi-token append
+
+def multi_rows(w, qlens, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    qo = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
+    shape = (int(qo[-1]), w.spec.H_kv, w.spec.D)
+    k = torch.randn(shape, generator=g).to(torch.bfloat16)
+    v = torch.randn(shape, generator=g).to(torch.bfloat16)
+    q = torch.randn(int(qo[-1]), w.spec.H_q, w.spec.D, generator=g).to(torch.bfloat16)
+    return q.cuda(), k.cuda(), v.cuda(), qo.cuda()
+
+
+MULTI_EDGE = workloads.custom_spec("multi_append_edges", 9, 8, 2, 128, 16,
+                                   [1, 15, 16, 17, 31, 33, 0, 48, 1000], max_len=1024)
+
+
+@pytest.mark.parametrize("name,qlen", [("edges", 17), ("llama8b", 4), ("gqa8", 3),
+                                       ("qwen100k", 2), ("tiny", 5)])
+def test_multi_append_writes_exactly_the_oracle_rows(name, qlen):
+    """q_len new rows per sequence (more than a page, and more than some sequences
+    hold) land where the oracle puts them, bit for bit, and nothing else moves."""
+    w = workloads.make(MULTI_EDGE if name == "edges" else name, seed=34, device="cuda",
+                       poison="nan")
+    rng = np.random.default_rng(34)
+    qlens = [int(rng.integers(0, qlen + 1)) for _ in w.lens_list]
+    q, k_new, v_new, qo = multi_rows(w, qlens, 35)
+    exp = oracle.append_multi(workloads.host_copy(w), qo.cpu(), k_new.cpu(), v_new.cpu())
+    pa.paged_kv_append_multi(k_new, v_new, w.k_cache, w.v_cache, qo, w.block_tables, w.seq_lens)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(w.k_cache), exp.k)
+    assert np.array_equal(cache_bits(w.v_cache), exp.v)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("name,qlen", [("edges", 17), ("llama8b", 4)])
+def test_multi_append_decode_matches_oracle(name, qlen, causal):
+    w = workloads.make(MULTI_EDGE if name == "edges" else name, seed=36, device="cuda",
+                       poison="nan")
+    qlens = [min(qlen, L) for L in w.lens_list]
+    q, k_new, v_new, qo = multi_rows(w, qlens, 37)
+    exp = oracle.append_multi(workloads.host_copy(w), qo.cpu(), k_new.cpu(), v_new.cpu())
+    pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE)  # must not matter here
+    try:
+        out = pa.paged_attn_append_decode_multi(q, k_new, v_new, w.k_cache, w.v_cache, qo,
+                                                w.block_tables, w.seq_lens, w.scale, qlen,
+                                                causal=causal)
+        torch.cuda.synchronize()
+    finally:
+        pa.paged_attn_set_launch_flags(0)
+    assert np.array_equal(cache_bits(w.k_cache), exp.k)
+    x = oracle.MultiInputs(q.cpu(), exp.k, exp.v, exp.bt, exp.lens, w.scale)
+    assert_parity(out, oracle.decode_multi(x, qo.cpu(), causal=causal), f"{name} {causal}")
+
+
+# ---------------------------------------------------------------- FP8 append
+
+def fp8_bits(f):
+    return (f.k8.cpu().numpy(), f.v8.cpu().numpy(), f.k_scale.cpu().numpy(),
+            f.v_scale.cpu().numpy())
+
+
+@pytest.mark.parametrize("name", ["edges", "llama8b", "qwen100k", "ragged256"])
+def test_fp8_append_writes_the_oracle_bytes_and_floats(name):
+    """Quantize-on-append: the e4m3 bytes and the row floats the kernel writes are
+    the oracle's bit for bit (the rounding decision is taken in float32 on both
+    sides), and every other byte and float is left as it was."""
+    w = workloads.make(EDGE if name == "edges" else name, seed=38, device="cuda", poison="nan")
+    f = workloads.to_fp8(w)
+    k_new, v_new = new_rows(w, 39)
+    k_new[0].zero_()  # an all-zero K row: float 1
+    host = oracle.Fp8Inputs(f.q.cpu(), f.k8.cpu(), f.v8.cpu(), f.k_scale.cpu(),
+                            f.v_scale.cpu(), f.block_tables.cpu(), f.seq_lens.cpu(), f.scale)
+    exp = oracle.append_fp8(host, k_new.cpu(), v_new.cpu())
+    pa.paged_kv_append_fp8(k_new, v_new, f.k8, f.v8, f.k_scale, f.v_scale, f.block_tables,
+                           f.seq_lens)
+    torch.cuda.synchronize()
+    k8, v8, ks, vs = fp8_bits(f)
+    assert np.array_equal(k8, exp.k8) and np.array_equal(v8, exp.v8)
+    # floats compared as bit patterns (NaN floats of unread rows included)
+    assert np.array_equal(ks.view(np.uint32), exp.ks.view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), exp.vs.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["edges", "llama8b", "ragged256"])
+def test_fp8_append_decode_matches_oracle(name):
+    w = workloads.make(EDGE if name == "edges" else name, seed=40, device="cuda", poison="nan")
+    f = workloads.to_fp8(w)
+    k_new, v_new = new_rows(w, 41)
+    host = oracle.Fp8Inputs(f.q.cpu(), f.k8.cpu(), f.v8.cpu(), f.k_scale.cpu(),
+                            f.v_scale.cpu(), f.block_tables.cpu(), f.seq_lens.cpu(), f.scale)
+    exp = oracle.append_fp8(host, k_new.cpu(), v_new.cpu())
+    pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE)  # must not matter here
+    try:
+        out = pa.paged_attn_append_decode_fp8(f.q, k_new, v_new, f.k8, f.v8, f.k_scale,
+                                              f.v_scale, f.block_tables, f.seq_lens, f.scale)
+        torch.cuda.synchronize()
+    finally:
+        pa.paged_attn_set_launch_flags(0)
+    assert np.array_equal(f.k8.cpu().numpy(), exp.k8)
+    assert_parity(out, oracle.decode_fp8(exp), name)

@@ -163,3 +163,59 @@ def test_multi_largest_row_count():
     qlens = [64, 64, 33, 64]
     q, qo = queries(w, qlens, 22)
     assert_parity(run_multi(w, q, qo, 64), reference(w, q, qo), "256 rows")
+
+
+# ---------------------------------------------------------------- without the causal mask
+# AstrAI's CUDA Kernels page, "Python Wrappers": is_causal True/False.  Without
+# the mask every query row of a sequence attends all of its tokens.
+
+def reference_noncausal(w, q, qo):
+    x = oracle.MultiInputs(q.cpu(), w.k_cache.cpu(), w.v_cache.cpu(), w.block_tables.cpu(),
+                           w.seq_lens.cpu(), w.scale)
+    return oracle.decode_multi(x, qo.cpu(), causal=False)
+
+
+@pytest.mark.parametrize("name,qlen", [("llama8b", 4), ("llama8b", 8), ("qwen100k", 3),
+                                       ("gqa8", 2), ("tiny", 5), ("ragged256", 2)])
+def test_noncausal_multi_matches_oracle(name, qlen):
+    w = workloads.make(name, device="cuda", poison="nan")
+    qlens = [min(qlen, L) for L in w.lens_list]
+    q, qo = queries(w, qlens, 61)
+    out = pa.paged_attn_decode_multi(q, w.k_cache, w.v_cache, qo, w.block_tables, w.seq_lens,
+                                     w.scale, qlen, causal=False)
+    torch.cuda.synchronize()
+    assert_parity(out, reference_noncausal(w, q, qo), f"{name} q_len {qlen} non-causal")
+
+
+def test_noncausal_rows_equal_the_decode_of_each_query():
+    """Without the mask, every query row of a sequence is the single-token decode of
+    that query over the whole sequence: bit for bit when each query is decoded
+    alone in a batch of the same shape (q_len 1, whose walk is the decode's)."""
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    qlens = [3] * len(w.lens_list)
+    q, qo = queries(w, qlens, 62)
+    out = pa.paged_attn_decode_multi(q, w.k_cache, w.v_cache, qo, w.block_tables, w.seq_lens,
+                                     w.scale, 3, causal=False)
+    ref = reference_noncausal(w, q, qo)
+    for i in range(3):
+        qi = q[i::3].contiguous()
+        one = torch.arange(len(w.lens_list) + 1, dtype=torch.int32, device="cuda")
+        o1 = pa.paged_attn_decode_multi(qi, w.k_cache, w.v_cache, one, w.block_tables,
+                                        w.seq_lens, w.scale, 1, causal=False)
+        torch.cuda.synchronize()
+        assert_parity(o1, ref[i::3], f"query {i}")
+    assert_parity(out, ref, "all")
+
+
+@pytest.mark.parametrize("D,BS,G,qlen", [(64, 16, 2, 9), (128, 32, 4, 5), (256, 16, 6, 3),
+                                         (128, 16, 16, 2), (64, 32, 1, 17)])
+def test_noncausal_sweep(D, BS, G, qlen):
+    lens = [1, 15, 16, 17, 100, 257, 3, 40]
+    sp = workloads.custom_spec("nc_sweep", len(lens), 2 * G, 2, D, BS, lens)
+    w = workloads.make(sp, seed=63, device="cuda", poison="nan")
+    qlens = [min(qlen, L) for L in lens]
+    q, qo = queries(w, qlens, 64)
+    out = pa.paged_attn_decode_multi(q, w.k_cache, w.v_cache, qo, w.block_tables, w.seq_lens,
+                                     w.scale, qlen, causal=False)
+    torch.cuda.synchronize()
+    assert_parity(out, reference_noncausal(w, q, qo), f"D {D} BS {BS} G {G} q_len {qlen}")

@@ -89,3 +89,117 @@ def test_static_scratch_rejects_sizes_beyond_its_limit(lib):
     assert rc == STATIC_SCRATCH_ERROR
     torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0  # nothing was launched
+
+
+_FRESH = r"""
+import ctypes, json, sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+torch.cuda.init()
+import oracle
+import workloads
+import paged_kv_gqa_decode_gb300 as pa
+
+lib = pa.load()  # nothing of the library has run on the device yet
+early = {early}
+if early:
+    assert lib.paged_attn_set_launch_flags(1) == 0
+res = {{}}
+work = [workloads.make(n, device="cuda", poison="nan") for n in ("tiny", "llama8b", "qwen100k")]
+outs = [torch.full_like(w.q, float("nan")) for w in work]
+torch.cuda.synchronize()
+free = [torch.cuda.mem_get_info()[0]]
+for w, out in zip(work, outs):
+    num_seqs, H_q, D = w.q.shape
+    _, H_kv, BS, _ = w.k_cache.shape
+    rc = lib.paged_attn_decode_static(
+        w.q.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(), out.data_ptr(),
+        w.block_tables.data_ptr(), w.seq_lens.data_ptr(), int(num_seqs), int(H_q), int(H_kv),
+        int(D), int(w.block_tables.shape[1]), int(BS), ctypes.c_float(w.scale),
+        torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+# the allocating entry point, first use of its own workspace: the measurement
+# sees an allocation of that size
+w = work[2]
+num_seqs, H_q, D = w.q.shape
+_, H_kv, BS, _ = w.k_cache.shape
+rc = lib.paged_attn_decode(
+    w.q.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(), outs[2].data_ptr(),
+    w.block_tables.data_ptr(), w.seq_lens.data_ptr(), int(num_seqs), int(H_q), int(H_kv), int(D),
+    int(w.block_tables.shape[1]), int(BS), ctypes.c_float(w.scale),
+    torch.cuda.current_stream().cuda_stream)
+assert rc == 0, rc
+torch.cuda.synchronize()
+free.append(torch.cuda.mem_get_info()[0])
+res["free"] = free
+errs = []
+for w, out in zip(work, outs):
+    host = workloads.host_copy(w)
+    if w.spec.name == "qwen100k":  # sampled rows: every sequence, first and last head
+        pairs = [(s, h) for s in range(4) for h in (0, 23)]
+        ref = oracle.decode(host, pairs=pairs)
+        got = np.stack([out[s, h].float().cpu().double().numpy() for s, h in pairs])
+    else:
+        ref = oracle.decode(host)
+        got = out.float().cpu().double().numpy()
+    err = np.abs(got - ref)
+    errs.append([float(err.max()), float(err.mean()), bool(np.isfinite(got).all())])
+res["errs"] = errs
+print("RESULT " + json.dumps(res))
+"""
+
+
+@pytest.mark.parametrize("early", [False, True])
+def test_static_entry_point_first_in_a_fresh_process_allocates_nothing(lib, early):
+    """The first library call of a fresh process is paged_attn_decode_static (so it
+    looks up the scratch array's address itself).  With the kernels loaded eagerly,
+    that first call takes device memory once (the library's code and its 4 MiB
+    array); the static calls after it, on larger problems that would grow an
+    allocated workspace, leave the free device memory exactly where it was, while
+    the allocating entry point's first call afterwards visibly takes some.  Every
+    output matches the oracle, with and without the early-prologue launch flag."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = _FRESH.format(root=root, early=early)
+    env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    import json
+
+    res = json.loads(r.stdout.split("RESULT ", 1)[1])
+    free = res["free"]
+    assert free[2] == free[1] and free[3] == free[2], free  # no allocation after the first
+    assert free[4] < free[3], free  # an allocation would have shown
+    # the first call's drop is the library's code and the 4 MiB array being loaded
+    so_bytes = os.path.getsize(os.path.join(root, "paged_kv_gqa_decode_gb300", "lib",
+                                            "libpaged_kv_gqa_decode.so"))
+    assert free[0] - free[1] <= so_bytes + (4 << 20) + (8 << 20), free
+    for mx, mean, finite in res["errs"]:
+        assert finite and mx <= MAX_ABS and mean <= MEAN_ABS, res["errs"]
+
+
+def test_static_entry_point_with_the_early_prologue_back_to_back(lib):
+    """Two static calls back to back under the early prologue (the memset that
+    clears the array sits between them in the stream) give what the allocating
+    entry point gives."""
+    w = workloads.make("llama8b", device="cuda", poison="nan")
+    stream = torch.cuda.current_stream()
+    ref = torch.empty_like(w.q)
+    assert _c_call(lib, "paged_attn_decode", w, ref, stream) == 0
+    assert lib.paged_attn_set_launch_flags(1) == 0
+    try:
+        outs = [torch.full_like(w.q, float("nan")) for _ in range(2)]
+        for out in outs:
+            assert _c_call(lib, "paged_attn_decode_static", w, out, stream) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.paged_attn_set_launch_flags(0)
+    for out in outs:
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
