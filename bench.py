@@ -164,6 +164,86 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (read-only queries,
+    libnvidia-ml loaded with ctypes), polled as fast as a background thread can
+    while the timed region runs, so that even a region of a millisecond holds
+    samples.  Changes no GPU setting."""
+
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device: int):
+        import ctypes
+
+        self.ok = False
+        self.samples = []  # (monotonic time, sm MHz, reason bits)
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.handle = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+                return
+            self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = None
+            if self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = self.sample() is not None
+        except Exception:
+            self.ok = False
+        self._stop = None
+
+    def sample(self):
+        import ctypes
+
+        mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, self.SM, ctypes.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn(self.handle, ctypes.byref(bits)) != 0:
+            return None
+        s = (time.monotonic(), mhz.value, bits.value)
+        self.samples.append(s)
+        return s
+
+    def start(self):
+        if not self.ok:
+            return
+        self._stop = threading.Event()
+
+        def poll():
+            while not self._stop.is_set():
+                self.sample()
+                time.sleep(0.0002)
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self._stop is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        reasons = set()
+        for _, _, bits in inside:
+            for b, name in self.REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(m for _, m, _ in inside),
+                "sm_min_mhz": min(m for _, m, _ in inside),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(inside), "window": "timed region (NVML, ~0.2 ms polling)"}
+
+
 # ------------------------------------------------------------------ oracle timing
 
 def oracle_sample_run(w_host, spec, groups, threads):
@@ -278,22 +358,8 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
 
-    # --op: the decode alone, or with each sequence's new token appended to the
-    # cache first (fused into the decode launch, or as a separate launch)
-    op = args.op
-    k_new = v_new = None
-    if op != "decode":
-        gk = torch.Generator(device="cpu").manual_seed(seed + 17)
-        shape = (spec.num_seqs, spec.H_kv, spec.D)
-        k_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
-        v_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
-        rows = sum(1 for L in lens if L > 0) * spec.H_kv
-        nbytes = dict(nbytes)
-        nbytes["append"] = rows * spec.D * 2 * 2 * 2  # K and V rows, read once, written once
-        nbytes["total"] += nbytes["append"]
-
     # --qlen > 1: multi-token decode, the last qlen tokens of every sequence query
-    # the cache (causal); q and out grow to qlen rows per sequence
+    # the cache (causal unless --noncausal); q and out grow to qlen rows per sequence
     qlen = args.qlen
     q_in = w.q
     qo = None
@@ -306,6 +372,24 @@ def run_ours(args, world, rank, local):
         nbytes = dict(nbytes)
         nbytes["q_out"] = spec.num_seqs * qlen * spec.H_q * spec.D * 2 * 2
         nbytes["total"] = nbytes["kv"] + nbytes["q_out"] + nbytes["block_table"]
+    causal = not args.noncausal
+
+    # --op: the decode alone, or with each sequence's new tokens appended to the
+    # cache first (fused into the decode launch, or as a separate launch; FP8
+    # caches quantize the new rows on the way in)
+    op = args.op
+    k_new = v_new = None
+    if op != "decode":
+        gk = torch.Generator(device="cpu").manual_seed(seed + 17)
+        new_rows = spec.num_seqs * qlen
+        shape = (new_rows, spec.H_kv, spec.D)
+        k_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
+        v_new = torch.randn(shape, generator=gk).to(torch.bfloat16).to(dev)
+        rows = sum(min(qlen, L) for L in lens) * spec.H_kv
+        written = 2 * (spec.D + 4) if fp8 else 2 * spec.D * 2  # K and V: e4m3 + float, or bf16
+        nbytes = dict(nbytes)
+        nbytes["append"] = rows * (spec.D * 2 * 2 + written)  # bf16 rows read, cache rows written
+        nbytes["total"] += nbytes["append"]
 
     # Early prologue (include/paged_attn.h): in the plain decode ops the work
     # ahead of a launch (the previous step) writes the output only, never the
@@ -318,11 +402,27 @@ def run_ours(args, world, rank, local):
         st = stream if st is None else st
         kc, vc, ksc, vsc = cache
         if qo is not None:
-            pa.paged_attn_decode_multi(q, kc, vc, qo, bt, sl, w.scale, qlen, out=out,
-                                       stream=st)
+            if op == "decode":
+                pa.paged_attn_decode_multi(q, kc, vc, qo, bt, sl, w.scale, qlen, out=out,
+                                           stream=st, causal=causal)
+            elif op == "append_decode":
+                pa.paged_attn_append_decode_multi(q, kn, vn, kc, vc, qo, bt, sl, w.scale, qlen,
+                                                  out=out, stream=st, causal=causal)
+            else:
+                pa.paged_kv_append_multi(kn, vn, kc, vc, qo, bt, sl, stream=st)
+                pa.paged_attn_decode_multi(q, kc, vc, qo, bt, sl, w.scale, qlen, out=out,
+                                           stream=st, causal=causal)
         elif fp8:
-            pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
-                                     stream=st)
+            if op == "decode":
+                pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
+                                         stream=st)
+            elif op == "append_decode":
+                pa.paged_attn_append_decode_fp8(q, kn, vn, kc, vc, ksc, vsc, bt, sl, w.scale,
+                                                out=out, stream=st)
+            else:
+                pa.paged_kv_append_fp8(kn, vn, kc, vc, ksc, vsc, bt, sl, stream=st)
+                pa.paged_attn_decode_fp8(q, kc, vc, ksc, vsc, bt, sl, w.scale, out=out,
+                                         stream=st)
         elif args.kv == "xpacked":
             pa.paged_attn_decode_xpacked(q, kc, vc, bt, sl, w.scale, out=out, stream=st)
         elif op == "decode":
@@ -334,8 +434,28 @@ def run_ours(args, world, rank, local):
             pa.paged_kv_append(kn, vn, kc, vc, bt, sl, stream=st)
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=st)
 
-    def step(i):
-        run_op(q_in, w.block_tables, w.seq_lens, caches[i % reps], k_new, v_new)
+    # Kernel launches per step, by the library's rules: one decode launch per
+    # 4,096 sequences; the append is a launch of its own for FP8 caches, for
+    # multi-token rows, for --op append_then_decode, and for the fused bf16 op when
+    # the batch has four or more (sequence, KV head) pieces per CTA of the
+    # persistent grid (two CTAs per SM unless a stage is 16 KB or more).
+    fmt = ("multi-token, %d %s queries per sequence" % (qlen, "causal" if causal else
+                                                           "non-causal") if qlen > 1 else
+           "FP8 caches" if fp8 else "x-packed caches" if args.kv == "xpacked" else "bf16 caches")
+    kernel_desc = {"decode": f"paged_decode_kernel ({fmt}; fused combine)",
+                   "append_decode": f"paged_decode_kernel ({fmt}) with the cache append of the "
+                                    "new tokens",
+                   "append_then_decode": f"append kernel + paged_decode_kernel ({fmt})"}[op]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ctas = sms * (1 if (spec.D >= 256 and spec.G > 8) or
+                  (not fp8 and spec.D * spec.block_size * 4 >= 16384) else 2)
+    append_launch = op == "append_then_decode" or (op == "append_decode" and (
+        fp8 or qo is not None or spec.num_seqs * spec.H_kv >= 4 * ctas))
+    launches_per_step = -(-len(lens) // 4096) + (1 if append_launch else 0)
+    kernel_desc += f" ({launches_per_step} launch{'es' if launches_per_step > 1 else ''} per step)"
+
+    def step(i, st=None):
+        run_op(q_in, w.block_tables, w.seq_lens, caches[i % reps], k_new, v_new, st=st)
 
     for i in range(args.warmup):
         step(i)
@@ -353,21 +473,72 @@ def run_ours(args, world, rank, local):
     else:
         steps = args.steps
 
+    # The timed steps are issued as CUDA graphs, as a decode loop on this GPU
+    # would issue them: groups of up to 64 steps (a multiple of the replica count,
+    # so that consecutive steps never read the same replica) captured once and
+    # replayed, so host-side call latency stays off the GPU's critical path.  The
+    # launches inside are the same kernel launches (programmatic dependent launch
+    # kept as graph edges).  Eager issue is timed as well and reported beside it.
+    per_graph = max(reps, (min(steps, 64) // reps) * reps)
+    graphs = {}
+    timing_mode = f"CUDA graphs of {per_graph} steps replayed"
+    if not args.eager:
+        try:
+            for n in sorted({per_graph, steps % per_graph} - {0}):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(n):
+                        step(i, st=torch.cuda.current_stream())
+                graphs[n] = g
+            for g in graphs.values():  # one untimed replay each
+                g.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture unsupported here: eager issue
+            torch.cuda.synchronize()
+            graphs = {}
+            timing_mode = f"eager issue (graph capture failed: {type(exc).__name__})"
+    else:
+        timing_mode = "eager issue (--eager)"
+
+    def timed_steps():
+        if graphs:
+            for _ in range(steps // per_graph):
+                graphs[per_graph].replay()
+            if steps % per_graph:
+                graphs[steps % per_graph].replay()
+        else:
+            for i in range(steps):
+                step(i)
+
     clocks = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    nvml = NvmlClocks(local) if rank == 0 and not args.no_clocks else None
     time.sleep(0.3 if clocks else 0)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     barrier(world)
     torch.cuda.synchronize()
+    if nvml:
+        nvml.start()
     t0 = time.monotonic()
     ev[0].record(stream)
-    for i in range(steps):
-        step(i)
+    timed_steps()
     ev[1].record(stream)
     torch.cuda.synchronize()
     t1 = time.monotonic()
+    if nvml:
+        nvml.stop()
     barrier(world)
     elapsed = ev[0].elapsed_time(ev[1]) / 1e3
     elapsed = reduce_max(elapsed, world)
+    # the same K steps issued eagerly, one call after another
+    eager_s = None
+    if graphs:
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(steps):
+            step(i)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        eager_s = reduce_max(ev[0].elapsed_time(ev[1]) / 1e3, world) / steps
     # after the timed region: event pairs around single launches on the launching
     # stream (each pair holds one step alone: no overlap with its neighbours)
     j = min(steps, 2000)
@@ -383,8 +554,11 @@ def run_ours(args, world, rank, local):
     if clocks:
         clocks.stop()
         clock_info = clocks.summary(t0, t1)
+    if nvml:
+        inside = nvml.summary(t0, t1)
+        if inside is not None:
+            clock_info = dict(inside, nvidia_smi_whole_run=clock_info)
     per_step = elapsed / steps
-    launches_per_step = -(-len(lens) // 4096) + (1 if op == "append_then_decode" else 0)
 
     # End to end through the public API: every step copies its inputs from
     # pinned host memory to the device and its result back to pinned host
@@ -530,23 +704,16 @@ def run_ours(args, world, rank, local):
                 "launch": "early prologue (the producer starts before the previous launch "
                           "ends; caches, tables and lengths are not written between steps)"
                 if early else "plain (each step writes the cache)",
+                "issue": timing_mode,
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback 6800 GB/s",
-                "kernel": f"paged_decode_kernel, multi-token ({qlen} causal queries per "
-                          "sequence; one launch per step)" if qlen > 1 else
-                "paged_decode_kernel over FP8 caches (one launch per step)" if fp8 else
-                "paged_decode_kernel over x-packed caches (one launch per step)"
-                if args.kv == "xpacked" else
-                {"decode": "paged_decode_kernel (one launch per step, fused combine)",
-                           "append_decode": "paged_decode_kernel with the fused cache append "
-                                            "(one launch per step)",
-                           "append_then_decode": "paged_kv_append_kernel + paged_decode_kernel "
-                                                 "(two launches per step)"}[op],
+                "kernel": kernel_desc,
                 "kernel_us": round(launch_s * 1e6, 2),
+                "eager_us_per_step": round(eager_s * 1e6, 2) if eager_s else None,
                 "kernel_us_isolated": round(kernel_s * 1e6, 2),
                 "frac_isolated": round(nbytes["total"] / kernel_s / 1e9 / peak, 4),
                 "timing": (f"CUDA events over the timed region on the launching stream, "
@@ -635,6 +802,10 @@ def main():
                          "cache first (fused into the decode launch, or a separate launch)")
     ap.add_argument("--qlen", type=int, default=1,
                     help="query tokens per sequence: > 1 runs the multi-token (causal) decode")
+    ap.add_argument("--noncausal", action="store_true",
+                    help="with --qlen > 1: every query row attends all of its sequence's tokens")
+    ap.add_argument("--eager", action="store_true",
+                    help="issue the timed steps one call at a time instead of as CUDA graphs")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -644,10 +815,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.kv != "bf16" and args.op != "decode":
-        ap.error(f"--kv {args.kv} runs the decode alone (--op decode)")
-    if args.qlen > 1 and (args.kv != "bf16" or args.op != "decode"):
-        ap.error("--qlen > 1 runs the bf16 decode alone")
+    if args.kv == "xpacked" and args.op != "decode":
+        ap.error("--kv xpacked runs the decode alone (--op decode)")
+    if args.qlen > 1 and args.kv != "bf16":
+        ap.error("--qlen > 1 runs over bf16 caches")
+    if args.noncausal and args.qlen < 2:
+        ap.error("--noncausal needs --qlen > 1")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)
