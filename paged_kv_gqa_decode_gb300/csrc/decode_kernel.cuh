@@ -67,6 +67,16 @@ __host__ __device__ constexpr int ctas_per_sm(int D, bool g16, int BS = 16, bool
   return (D >= 256 && g16) || (!fp8 && D * BS * 2 * 2 >= (16 << 10)) ? 1 : 2;
 }
 constexpr int kMinPagesPerCta = 8;
+// Fixed cost of one (sequence, KV head) piece in pages, for the work split.
+#ifndef PAGED_ATTN_PIECE_WEIGHT_BF16
+#define PAGED_ATTN_PIECE_WEIGHT_BF16 4
+#endif
+#ifndef PAGED_ATTN_PIECE_WEIGHT_FP8
+#define PAGED_ATTN_PIECE_WEIGHT_FP8 4
+#endif
+#ifndef PAGED_ATTN_PIECE_WEIGHT_MULTI
+#define PAGED_ATTN_PIECE_WEIGHT_MULTI 10
+#endif
 constexpr int kMaxStages = 16;  // ring depth cap (slot s belongs to consumer warp s % 4)
 constexpr int kMaxIssueLanes = 4;   // producer lanes issuing loads at once
 constexpr int kConsumerBarrier = 1;
@@ -205,6 +215,32 @@ __device__ __forceinline__ long long range_begin(long long c, long long W, long 
   return c * W / C;
 }
 
+// The work split runs over weighted positions: unit p of piece (sw, g) sits at
+// H_kv * wprefix[sw] + g * (n + wgt) + p (n: the pages of walked sequence sw),
+// and the wgt positions after a piece's units stand for its fixed cost (the
+// merge of the warps' states, the output or partial store, the next query
+// group) and belong to no unit.  Returns the first unit at or after position T
+// (W, the unit count, past the end; Wt: the weighted total).
+__device__ __forceinline__ long long first_unit(long long T, long long W, long long Wt,
+                                                const int* prefix, const int* wprefix, int NW,
+                                                int H_kv, int wgt) {
+  if (T >= Wt) return W;
+  int lo = 0, hi = NW - 1;  // largest sw with H_kv * wprefix[sw] <= T: a sequence with pages
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)wprefix[mid] * H_kv <= T)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int n = prefix[lo + 1] - prefix[lo];
+  if (n == 0) return (long long)prefix[lo + 1] * H_kv;  // (not reached for T < Wt)
+  const long long off = T - (long long)wprefix[lo] * H_kv;
+  const long long g = off / (n + wgt), r = off - g * (n + wgt);
+  const long long base = (long long)prefix[lo] * H_kv + g * n;
+  return r < n ? base + r : base + n;
+}
+
 // FP8: the caches hold e4m3 bytes (head_dim 128 or 256) and one float per cache
 // row; the products run on f16 tensor cores (e4m3 -> f16 is exact, q is turned
 // into f16 once per piece), the K row floats scale the scores and the V row
@@ -239,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   constexpr int kQ16Stride = L::kQ16Stride;      // FP8: padded f16 query row
   constexpr int kQSlotBytes =                     // = lay.q_slot_bytes()
       (kQTileBytes + (FP8 ? kQRows * kQ16Stride : 4 * D + 16) + 127) / 128 * 128;
-  constexpr int kScaleBytes = L::kScaleBytes;     // FP8: a stage's K and V row floats
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -257,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   uint8_t* sm_q = smem + lay.qtile();
   float* sm_scales = reinterpret_cast<float*>(smem + lay.scales());  // FP8: [stages][2][BS]
   int* sm_prefix = reinterpret_cast<int*>(smem + lay.prefix());
+  int* sm_wprefix = reinterpret_cast<int*>(smem + lay.wprefix());
   int* sm_len = reinterpret_cast<int*>(smem + lay.lens());
   int* sm_qo = reinterpret_cast<int*>(smem + lay.qo());  // multi: qo_indptr[0..N]
 
@@ -274,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // walked sequence sw = c * N + s.
   const int NW = N * QC;
   const int cap = p.maxb * BS;
+  constexpr int kWgt = MULTI ? PAGED_ATTN_PIECE_WEIGHT_MULTI
+                      : FP8  ? PAGED_ATTN_PIECE_WEIGHT_FP8
+                             : PAGED_ATTN_PIECE_WEIGHT_BF16;
   // Status bits are written only after the work ahead in the stream has
   // completed: with the early prologue the producer runs before that point,
   // and a caller that zero-fills the status word in that work must not erase
@@ -309,12 +348,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     }
   }
 
-  // ---- 1. clamped lengths and the exclusive prefix of pages per sequence
+  // ---- 1. clamped lengths, the exclusive prefix of pages per sequence and the
+  // same prefix with every piece weighted by its fixed cost (first_unit)
   {
     const int per = (N + kThreads - 1) / kThreads;
     const int s0 = tid * per;
     const int s1 = min(N, s0 + per);
-    int local = 0;
+    int local = 0, wlocal = 0;
     for (int s = s0; s < s1; ++s) {
       int len = __ldg(p.seq_lens + s);
       if (len < 0 || len > cap) {
@@ -322,37 +362,59 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         len = min(max(len, 0), cap);
       }
       sm_len[s] = len;
-      local += (len + BS - 1) / BS;
+      const int pages = (len + BS - 1) / BS;
+      local += pages;
+      wlocal += pages + (pages > 0 ? kWgt : 0);
     }
-    int incl = local;  // block-wide exclusive scan of `local`
+    int incl = local, wincl = wlocal;  // block-wide exclusive scans of both
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int wv = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) {
+        incl += v;
+        wincl += wv;
+      }
     }
-    __shared__ int warp_tot[kThreads / 32];
-    if (lane == 31) warp_tot[warp] = incl;
+    __shared__ int warp_tot[kThreads / 32], warp_wtot[kThreads / 32];
+    if (lane == 31) {
+      warp_tot[warp] = incl;
+      warp_wtot[warp] = wincl;
+    }
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_tot[w];
-    int run = base + incl - local;
+    int base = 0, wbase = 0;
+    for (int w = 0; w < warp; ++w) {
+      base += warp_tot[w];
+      wbase += warp_wtot[w];
+    }
+    int run = base + incl - local, wrun = wbase + wincl - wlocal;
     for (int s = s0; s < s1; ++s) {
       sm_prefix[s] = run;
-      run += (sm_len[s] + BS - 1) / BS;
+      sm_wprefix[s] = wrun;
+      const int pages = (sm_len[s] + BS - 1) / BS;
+      run += pages;
+      wrun += pages + (pages > 0 ? kWgt : 0);
     }
-    if (tid == kThreads - 1) sm_prefix[N] = base + incl;
+    if (tid == kThreads - 1) {
+      sm_prefix[N] = base + incl;
+      sm_wprefix[N] = wbase + wincl;
+    }
     if (multi) {
       for (int s = tid; s <= N; s += kThreads) sm_qo[s] = __ldg(p.qo_indptr + s);
     }
     __syncthreads();
-    if (multi && QC > 1) {  // page prefix of the later passes: offset by c * (all pages)
-      const int P = sm_prefix[N];
+    if (multi && QC > 1) {  // prefixes of the later passes: offset by c * (all pages)
+      const int P = sm_prefix[N], WP = sm_wprefix[N];
       for (int i = tid; i < (QC - 1) * N; i += kThreads) {
         const int c = 1 + i / N;
         const int sq = i - (c - 1) * N;
         sm_prefix[c * N + sq] = c * P + sm_prefix[sq];
+        sm_wprefix[c * N + sq] = c * WP + sm_wprefix[sq];
       }
-      if (tid == 0) sm_prefix[NW] = QC * P;
+      if (tid == 0) {
+        sm_prefix[NW] = QC * P;
+        sm_wprefix[NW] = QC * WP;
+      }
       __syncthreads();
     }
     if (multi && blockIdx.x == 0) {
@@ -393,9 +455,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   if ((long long)blockIdx.x >= C) return;
   // (with the early prologue the consumers zero them once they have waited)
   if (!p.early) zero_empty(C, tid, kThreads);
-  const long long u0 = range_begin(blockIdx.x, W, C);
-  const long long u1 = range_begin(blockIdx.x + 1, W, C);
-  if (u0 >= u1) return;
+  // CTA c takes the units at weighted positions [c Wt / C, (c + 1) Wt / C): a
+  // CTA crossing many short pieces gets fewer pages.  An interval that falls
+  // inside the gap after a piece (possible only for tiny batches) holds no
+  // units; that CTA is never part of a split, since the CTAs of a split piece
+  // are those whose intervals meet the piece's (gap-free) unit positions.
+  const long long Wt = (long long)sm_wprefix[NW] * H_kv;
+  auto unit_at = [&](long long T) {
+    return first_unit(T, W, Wt, sm_prefix, sm_wprefix, NW, H_kv, kWgt);
+  };
+  const long long u0 = unit_at(range_begin(blockIdx.x, Wt, C));
+  const long long u1 = unit_at(range_begin(blockIdx.x + 1, Wt, C));
+  if (u0 >= u1) {
+    if (p.early) {  // its share of the empty sequences is still to be zeroed
+      griddep_wait();
+      zero_empty(C, tid, kThreads);
+    }
+    return;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -456,8 +533,28 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
 #endif
           else {
             issued = true;
-            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes + kScaleBytes);
             uint8_t* st = smem + stage * kStageBytes;
+            if constexpr (FP8) {
+              // The page's K and V row floats (64 or 128 bytes each) come with
+              // 16-byte cp.async, not as two more bulk copies: with 2 KB pages the
+              // tensor-copy engine's operations per byte, not the bytes, set the
+              // pace (LLaMA-shaped batch 37.0 -> 33.2 us, ragged batch 454 -> 410).
+              // The copies complete on the stage's barrier (cp.async.mbarrier.arrive
+              // raises its pending count now, before the arrive below, and lowers it
+              // when they land).  A block outside a checked pool reads block 0's
+              // floats: its rows are zero-filled by the tensor copy anyway.
+              const long long b =
+                  pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
+              const size_t row = ((size_t)b * H_kv + g) * BS;
+              float* sc = sm_scales + (size_t)stage * 2 * BS;
+#pragma unroll
+              for (int c = 0; c < BS / 4; ++c) {
+                cp_async_16(sc + 4 * c, p.k_scale + row + 4 * c, 16);
+                cp_async_16(sc + BS + 4 * c, p.v_scale + row + 4 * c, 16);
+              }
+              cp_async_mbar_arrive(&full_bar[stage]);
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
             if constexpr (XP) {
               // a page of one KV head is contiguous in both x-packed caches: K
               // (and V of 16-token pages) come as one bulk copy each; V of 32-token
@@ -476,16 +573,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
             } else {
               tma_load_4d(st, &tm_k, &full_bar[stage], 0, g * BS, 0, pb, policy);
               tma_load_4d(st + kPageBytes, &tm_v, &full_bar[stage], 0, g * BS, 0, pb, policy);
-            }
-            if constexpr (FP8) {
-              // the page's K and V row floats (a block outside a checked pool reads
-              // block 0's: its rows are zero-filled by the tensor copy anyway)
-              const long long b =
-                  pb < 0 || (p.num_blocks > 0 && (long long)pb >= p.num_blocks) ? 0 : pb;
-              const size_t row = ((size_t)b * H_kv + g) * BS;
-              float* sc = sm_scales + (size_t)stage * 2 * BS;
-              bulk_load(sc, p.k_scale + row, BS * 4, &full_bar[stage]);
-              bulk_load(sc + BS, p.v_scale + row, BS * 4, &full_bar[stage]);
             }
           }
         }
@@ -536,9 +623,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   float m_run[kNH][2];        // running max per owned head (log2 domain)
   float l_run[kNH][2];        // running sum per owned head (this lane's tokens)
 
-  // The query group of a piece lives in one of two shared tiles
+  // The query group of a piece lives in one of kQSlots shared tiles
   // [16 heads][D] (16-byte chunk c of head h at c ^ (h % 8) within each 128
-  // bytes; heads >= G are zero) and is fetched one piece ahead with cp.async.
+  // bytes; heads >= G are zero) and is fetched kQSlots - 1 pieces ahead with
+  // cp.async, one commit group per piece (an empty group past the range's last
+  // piece, so that the group count stays exact).
   // With the fused cache append the slot also receives the piece's new K and V
   // rows and the block id of its last page, so the warp that patches that page
   // finds them in shared memory.
@@ -983,9 +1072,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     Split x;
     x.s = s;
     x.g = g;
-    x.c_first = cta_of(sb, W, C);
-    x.c_last = cta_of(se - 1, W, C);
-    x.slot_first = 2 * x.c_first + (sb == range_begin(x.c_first, W, C) ? 0 : 1);
+    const long long n = se - sb;
+    const long long xs = (long long)sm_wprefix[s] * H_kv + (long long)g * (n + kWgt);
+    x.c_first = cta_of(xs, Wt, C);
+    x.c_last = cta_of(xs + n - 1, Wt, C);
+    x.slot_first = 2 * x.c_first + (sb == unit_at(range_begin(x.c_first, Wt, C)) ? 0 : 1);
     return x;
   };
 
@@ -1206,6 +1297,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     long long sb;  // first unit of the whole (s, g)
   };
   auto next_piece = [&](Piece pc) -> Piece {
+    if (pc.s >= NW) return pc;  // already past the last walked sequence
     const int n = sm_prefix[pc.s + 1] - sm_prefix[pc.s];
     if (++pc.g == H_kv) {
       pc.g = 0;
@@ -1236,15 +1328,26 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
     sm_split_flags[1] = last_sb < u0 || last_sb + wl.n > u1;
   }
-  Piece ahead{wk.s, wk.g, 0};  // the next piece whose query group gets prefetched
+  // The query slots: the current piece's (qbuf) and the next kQSlots - 1
+  // pieces' in the slots after it; `ahead` is the next piece to prefetch.
+  auto prefetch_or_skip = [&](int buf, const Piece& pc) {
+    if (pc.s < NW && pc.sb < u1)
+      prefetch_q(buf, pc.s, pc.g);
+    else
+      cp_async_commit();  // an empty group keeps the count
+  };
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
-  ahead = next_piece(ahead);
+  Piece ahead = next_piece(Piece{wk.s, wk.g, 0});
   cp_async_wait_all();
   if constexpr (FP8) convert_own_q(0);
   __syncwarp();
   named_barrier(kConsumerBarrier, kConsumerThreads);
-  if (ahead.s < NW && ahead.sb < u1) prefetch_q(1, ahead.s, ahead.g);
+#pragma unroll
+  for (int k = 1; k < kQSlots; ++k) {
+    prefetch_or_skip(k, ahead);
+    ahead = next_piece(ahead);
+  }
   reset();
   set_limits(wk.s, wk.g);
   // Ring ownership: unit i of the range (i = u - u0) sits in slot i % stages,
@@ -1382,18 +1485,20 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
       const bool split = sb < u0;
       merge_warps(nullptr, nullptr);
       emit(s, g, split ? p.partials + (size_t)my_slot(sb) * R * kPartialRow : nullptr);
-      // The next piece's query group was prefetched into the other tile: make
-      // every thread's copies visible (FP8: after converting its own to f16),
-      // then prefetch the piece after it into the tile just freed.
-      cp_async_wait_all();
-      if constexpr (FP8) convert_own_q(qbuf ^ 1);
+      // The next piece's query group is the oldest of the kQSlots - 1 groups in
+      // flight: wait for it alone and make every thread's copies visible (FP8:
+      // after converting its own to f16), then prefetch into the slot just
+      // freed the piece kQSlots - 1 further on.
+      const int qnext = qbuf + 1 == kQSlots ? 0 : qbuf + 1;
+      cp_async_wait_group<kQSlots - 2>();
+      if constexpr (FP8) convert_own_q(qnext);
       __syncwarp();
       named_barrier(kConsumerBarrier, kConsumerThreads);
       if (ctid == 0 && split)
         first_old = atom_add_release_gpu(p.counters + sm_split[0].c_first, 1 + (1 << 16));
-      qbuf ^= 1;
+      prefetch_or_skip(qbuf, ahead);
       ahead = next_piece(ahead);
-      if (ahead.s < NW && ahead.sb < u1) prefetch_q(qbuf ^ 1, ahead.s, ahead.g);
+      qbuf = qnext;
       reset();
       set_limits(wk.s, wk.g);
       continue;

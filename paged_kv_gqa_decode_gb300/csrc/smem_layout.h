@@ -17,6 +17,9 @@
 namespace pagedattn {
 
 constexpr int kConsumerWarps = 4;
+// Query slots: the current piece's query group and the next kQSlots - 1 pieces'
+// (prefetched ahead, so a run of short pieces does not wait on each fetch).
+constexpr int kQSlots = 2;
 
 PAGEDATTN_HD constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -55,13 +58,14 @@ struct SmemLayout {
   PAGEDATTN_HD int q_slot_bytes() const {
     return align_up(q_tile_bytes() + q_extra_bytes(), 128);
   }
-  PAGEDATTN_HD int qtile() const {  // two query slots
+  PAGEDATTN_HD int qtile() const {  // kQSlots query slots
     return merge_o() + align_up(kConsumerWarps * G * kRowStride * 4, 128);
   }
-  PAGEDATTN_HD int prefix() const { return qtile() + 2 * q_slot_bytes(); }
-  PAGEDATTN_HD int lens() const {
-    return prefix() + align_up((walks * num_seqs + 1) * 4, 128);  // page prefix of each pass
-  }
+  PAGEDATTN_HD int prefix() const { return qtile() + kQSlots * q_slot_bytes(); }
+  // the page prefix of each pass, then the same prefix with each (sequence, KV
+  // head) piece weighted by its fixed cost (the work split's positions)
+  PAGEDATTN_HD int wprefix() const { return prefix() + align_up((walks * num_seqs + 1) * 4, 128); }
+  PAGEDATTN_HD int lens() const { return wprefix() + align_up((walks * num_seqs + 1) * 4, 128); }
   PAGEDATTN_HD int qo() const { return align_up(lens() + num_seqs * 4, 16); }
   PAGEDATTN_HD int total() const { return qo() + qo_entries * 4; }
 };

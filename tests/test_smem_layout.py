@@ -42,7 +42,7 @@ void run() {
         CHECK(l.scales() >= l.bars() + (2 * st + 1) * 8, "scales overlap\n");
         CHECK(l.merge_m() >= l.scales() + st * L::kScaleBytes, "scale ring size\n");
         const int starts[] = {l.scales(), l.merge_m(), l.merge_l(), l.final_ml(), l.flag(),
-                              l.merge_o(), l.qtile(), l.prefix(), l.lens()};
+                              l.merge_o(), l.qtile(), l.prefix(), l.wprefix(), l.lens()};
         for (int x : starts)
           CHECK(x % 128 == 0, "region at %d D%d BS%d st%d G%d n%d\n", x, D, BS, st, G, n);
         CHECK(l.merge_l() - l.merge_m() >= kConsumerWarps * 16 * 4, "merge_m size\n");
@@ -50,7 +50,8 @@ void run() {
         CHECK(l.flag() - l.final_ml() >= 32 * 4, "final size\n");
         CHECK(l.merge_o() - l.flag() >= 4 * 4, "flag size\n");
         CHECK(l.qtile() - l.merge_o() >= kConsumerWarps * G * L::kRowStride * 4, "merge_o size\n");
-        CHECK(l.prefix() - l.qtile() >= 2 * ((G > 8 ? 16 : 8) * D * 2 + 4 * D + 4), "qtile size\n");
+        CHECK(l.prefix() - l.qtile() >= kQSlots * ((G > 8 ? 16 : 8) * D * 2 + 4 * D + 4),
+              "qtile size\n");
         if (FP8) {
           CHECK(l.q_extra_bytes() >= (G > 8 ? 16 : 8) * (2 * D + 32), "q16 size\n");
           CHECK(L::kQ16Stride % 32 == 0, "q16 stride\n");
@@ -59,7 +60,8 @@ void run() {
         CHECK(l.q_slot_bytes() % 128 == 0, "q slot\n");
         CHECK(l.q_tile_bytes() % 128 == 0, "qtile bytes\n");
         CHECK((L::kRowStride * 4) % 16 == 0, "row stride\n");
-        CHECK(l.lens() - l.prefix() >= (walks * n + 1) * 4, "prefix size\n");
+        CHECK(l.wprefix() - l.prefix() >= (walks * n + 1) * 4, "prefix size\n");
+        CHECK(l.lens() - l.wprefix() >= (walks * n + 1) * 4, "wprefix size\n");
         CHECK(l.qo() - l.lens() >= n * 4, "lens size\n");
         CHECK(l.qo() % 16 == 0, "qo alignment\n");
         CHECK(l.total() - l.qo() >= qo * 4, "qo size\n");
