@@ -154,6 +154,14 @@ struct DecodeParams {
 #endif
 };
 
+// a / b for 0 <= a, 0 < b, in 32-bit arithmetic when both fit (a 64-bit
+// division is a long emulated sequence, and these sit ahead of the first copy).
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+  if (((unsigned long long)a | (unsigned long long)b) <= 0xffffffffull)
+    return (long long)((unsigned int)a / (unsigned int)b);
+  return a / b;
+}
+
 // Position of one unit (page of one KV head) in the flattened (s, g, p) order.
 struct Walker {
   int s, g, p, n;  // sequence, KV head, page within the sequence, pages of the sequence
@@ -170,7 +178,7 @@ struct Walker {
     s = lo;
     n = prefix[s + 1] - prefix[s];
     const long long off = u - (long long)prefix[s] * H_kv;
-    g = (int)(off / n);
+    g = (int)div_nonneg(off, n);
     p = (int)(off - (long long)g * n);
   }
 
@@ -208,11 +216,11 @@ struct Walker {
 
 // The CTA whose range contains unit u, for ranges [floor(c W / C), floor((c+1) W / C)).
 __device__ __forceinline__ int cta_of(long long u, long long W, long long C) {
-  return (int)(((u + 1) * C - 1) / W);
+  return (int)div_nonneg((u + 1) * C - 1, W);
 }
 
 __device__ __forceinline__ long long range_begin(long long c, long long W, long long C) {
-  return c * W / C;
+  return div_nonneg(c * W, C);
 }
 
 // The work split runs over weighted positions: unit p of piece (sw, g) sits at
@@ -236,7 +244,7 @@ __device__ __forceinline__ long long first_unit(long long T, long long W, long l
   const int n = prefix[lo + 1] - prefix[lo];
   if (n == 0) return (long long)prefix[lo + 1] * H_kv;  // (not reached for T < Wt)
   const long long off = T - (long long)wprefix[lo] * H_kv;
-  const long long g = off / (n + wgt), r = off - g * (n + wgt);
+  const long long g = div_nonneg(off, n + wgt), r = off - g * (n + wgt);
   const long long base = (long long)prefix[lo] * H_kv + g * n;
   return r < n ? base + r : base + n;
 }
@@ -310,9 +318,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // walked sequence sw = c * N + s.
   const int NW = N * QC;
   const int cap = p.maxb * BS;
-  constexpr int kWgt = MULTI ? PAGED_ATTN_PIECE_WEIGHT_MULTI
-                      : FP8  ? PAGED_ATTN_PIECE_WEIGHT_FP8
-                             : PAGED_ATTN_PIECE_WEIGHT_BF16;
+  // (a multi-token piece of one 8-row tile and one pass costs what a decode
+  // piece costs, and splits as the decode does)
+  const int kWgt = FP8 ? PAGED_ATTN_PIECE_WEIGHT_FP8
+                 : MULTI && (R > 8 || QC > 1) ? PAGED_ATTN_PIECE_WEIGHT_MULTI
+                                              : PAGED_ATTN_PIECE_WEIGHT_BF16;
   // Status bits are written only after the work ahead in the stream has
   // completed: with the early prologue the producer runs before that point,
   // and a caller that zero-fills the status word in that work must not erase
@@ -1076,7 +1086,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     const long long xs = (long long)sm_wprefix[s] * H_kv + (long long)g * (n + kWgt);
     x.c_first = cta_of(xs, Wt, C);
     x.c_last = cta_of(xs + n - 1, Wt, C);
-    x.slot_first = 2 * x.c_first + (sb == unit_at(range_begin(x.c_first, Wt, C)) ? 0 : 1);
+    // The piece is c_first's first (slot 0) unless the unit before it -- the
+    // previous piece's last, kWgt + 1 positions earlier -- is c_first's too.
+    const bool first_of_cta = sb == 0 || cta_of(xs - 1 - kWgt, Wt, C) != x.c_first;
+    x.slot_first = 2 * x.c_first + (first_of_cta ? 0 : 1);
     return x;
   };
 
@@ -1318,16 +1331,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   // at the end) and kept in shared memory, not in registers, through the loop.
   Split* const sm_split = reinterpret_cast<Split*>(sm_flag + 4);  // [0] first, [1] last
   int* const sm_split_flags = sm_flag + 4 + 2 * (int)(sizeof(Split) / sizeof(int));
-  if (ctid == 0) {
-    const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
-    Walker wl;
-    wl.start(u1 - 1, sm_prefix, NW, H_kv);
-    const long long last_sb = (long long)sm_prefix[wl.s] * H_kv + (long long)wl.g * wl.n;
-    sm_split[0] = make_split(wk.s, wk.g, first_sb, first_sb + wk.n);
-    sm_split[1] = make_split(wl.s, wl.g, last_sb, last_sb + wl.n);
-    sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
-    sm_split_flags[1] = last_sb < u0 || last_sb + wl.n > u1;
-  }
   // The query slots: the current piece's (qbuf) and the next kQSlots - 1
   // pieces' in the slots after it; `ahead` is the next piece to prefetch.
   auto prefetch_or_skip = [&](int buf, const Piece& pc) {
@@ -1339,6 +1342,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   int qbuf = 0;
   prefetch_q(0, wk.s, wk.g);
   Piece ahead = next_piece(Piece{wk.s, wk.g, 0});
+  if (ctid == 0) {  // while the first query group is in flight
+    const long long first_sb = (long long)sm_prefix[wk.s] * H_kv + (long long)wk.g * wk.n;
+    Walker wl;
+    wl.start(u1 - 1, sm_prefix, NW, H_kv);
+    const long long last_sb = (long long)sm_prefix[wl.s] * H_kv + (long long)wl.g * wl.n;
+    sm_split[0] = make_split(wk.s, wk.g, first_sb, first_sb + wk.n);
+    sm_split[1] = make_split(wl.s, wl.g, last_sb, last_sb + wl.n);
+    sm_split_flags[0] = first_sb < u0 && first_sb != last_sb;  // split, and not also the last
+    sm_split_flags[1] = last_sb < u0 || last_sb + wl.n > u1;
+  }
   cp_async_wait_all();
   if constexpr (FP8) convert_own_q(0);
   __syncwarp();
