@@ -84,8 +84,10 @@ extern "C" {
  *
  * Scratch: the split-KV partial states live in a per-device workspace that the
  * library owns.  The first call on a device (and any call that needs a larger
- * workspace than before) allocates it with cudaMalloc and zero-fills it on
- * `stream`; later calls allocate nothing.  Because the workspace is shared,
+ * workspace than before) allocates it with cudaMallocAsync on `stream` from the
+ * device's default memory pool and zero-fills it there (a smaller one is
+ * released with cudaFreeAsync on `stream`, after the calls before it on that
+ * stream); later calls allocate nothing.  Because the workspace is shared,
  * calls that may overlap on the GPU (different streams, same device) race:
  * give each concurrent stream its own workspace through paged_attn_decode_ws.
  */

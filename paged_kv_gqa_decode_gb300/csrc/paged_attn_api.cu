@@ -534,16 +534,18 @@ int owned_workspace(size_t bytes, cudaStream_t stream, void** out) {
   OwnedWorkspace& w = g_ws[dev];
   if (w.bytes < bytes) {
     if (w.ptr) {
-      // earlier calls on any stream may still use the old buffer
-      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
-      cudaFree(w.ptr);
+      // Earlier calls on this stream may still use the old buffer: free it in
+      // stream order (calls on other streams overlapping this one race on the
+      // shared workspace anyway, as the header says).  No device-wide sync.
+      if ((e = cudaFreeAsync(w.ptr, stream)) != cudaSuccess) return cuda_fail(e);
       w.ptr = nullptr;
       w.bytes = 0;
     }
     void* p = nullptr;
-    if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
+    // stream-ordered, like the release of the old one (the device's default pool)
+    if ((e = cudaMallocAsync(&p, bytes, stream)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemsetAsync(p, 0, bytes, stream)) != cudaSuccess) {
-      cudaFree(p);
+      cudaFreeAsync(p, stream);
       return cuda_fail(e);
     }
     w.ptr = p;
