@@ -435,10 +435,10 @@ def run_ours(args, world, rank, local):
             pa.paged_attn_decode(q, kc, vc, bt, sl, w.scale, out=out, stream=st)
 
     # Kernel launches per step, by the library's rules: one decode launch per
-    # 4,096 sequences; the append is a launch of its own for FP8 caches, for
-    # multi-token rows, for --op append_then_decode, and for the fused bf16 op when
-    # the batch has four or more (sequence, KV head) pieces per CTA of the
-    # persistent grid (two CTAs per SM unless a stage is 16 KB or more).
+    # 4,096 sequences; the append is a launch of its own for multi-token rows, for
+    # --op append_then_decode, for FP8 caches of head_dim 256, and for the fused
+    # op when the batch has four or more (sequence, KV head) pieces per CTA of the
+    # persistent grid (two CTAs per SM unless a bf16 stage is 16 KB or more).
     fmt = ("multi-token, %d %s queries per sequence" % (qlen, "causal" if causal else
                                                            "non-causal") if qlen > 1 else
            "FP8 caches" if fp8 else "x-packed caches" if args.kv == "xpacked" else "bf16 caches")
@@ -450,7 +450,7 @@ def run_ours(args, world, rank, local):
     ctas = sms * (1 if (spec.D >= 256 and spec.G > 8) or
                   (not fp8 and spec.D * spec.block_size * 4 >= 16384) else 2)
     append_launch = op == "append_then_decode" or (op == "append_decode" and (
-        fp8 or qo is not None or spec.num_seqs * spec.H_kv >= 4 * ctas))
+        (fp8 and spec.D != 128) or qo is not None or spec.num_seqs * spec.H_kv >= 4 * ctas))
     launches_per_step = -(-len(lens) // 4096) + (1 if append_launch else 0)
     kernel_desc += f" ({launches_per_step} launch{'es' if launches_per_step > 1 else ''} per step)"
 

@@ -392,9 +392,16 @@ PAGED_ATTN_API int paged_kv_append_fp8(const void* k_new, const void* v_new, voi
                                        int max_blocks_per_seq, int block_size, void* stream);
 
 /*
- * paged_kv_append_fp8 followed by paged_attn_decode_fp8, as two launches on
- * `stream` (the decode waits for the append to complete before it reads
- * anything, whatever the launch flags).  Arguments as the two calls.
+ * paged_kv_append_fp8 followed by paged_attn_decode_fp8, fused into the decode
+ * launch as paged_attn_append_decode is for bf16 caches: the warp that reads the
+ * page holding a sequence's new token quantizes the new K and V rows exactly as
+ * paged_kv_append_fp8 does, puts the bytes and row floats into its copy of the
+ * page in shared memory and stores them to the cache.  For head_dim 256, or
+ * with four or more (sequence, KV head) pairs per CTA of the persistent grid,
+ * the append runs as its own launch and the decode after it is a plain launch
+ * (whatever the launch flags).  The same bytes, floats and output either way.  Arguments as the two
+ * calls; the blocks receiving new tokens must not also be read by another
+ * sequence of the same call.
  */
 PAGED_ATTN_API int paged_attn_append_decode_fp8(const void* q, const void* k_new,
                                                 const void* v_new, void* k_cache, void* v_cache,

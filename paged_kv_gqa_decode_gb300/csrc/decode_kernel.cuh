@@ -47,6 +47,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -249,7 +250,60 @@ __device__ __forceinline__ long long first_unit(long long T, long long W, long l
   return r < n ? base + r : base + n;
 }
 
-// FP8: the caches hold e4m3 bytes (head_dim 128 or 256) and one float per cache
+// Fused cache append into an FP8 page held in shared memory: the new token's
+// bf16 K and V rows (at `rows`: D values of K, then D of V) are quantized as the
+// standalone FP8 append does -- float f = max|x| / 448 (1 for a zero row), byte
+// = e4m3(x / f) rounded to nearest even, saturating -- and written into row
+// `slot` of the page's K and V tiles (128-byte swizzle) and into that row's
+// floats (`scales`: BS K floats, then BS V floats).  One warp; lane l holds the
+// values l * D / 32 .. of each row.  Out of line: its registers are spent only
+// when a page holds a new token, not in the page loop around it.
+template <int D>
+__device__ __noinline__ void fp8_patch_row(const uint8_t* rows, uint8_t* st, int page_bytes,
+                                           int tile_bytes, int slot, float* scales, int BS,
+                                           int lane) {
+  constexpr int kE = D / 32;
+  const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(rows) + lane * kE;
+  const __nv_bfloat16* vr = kr + D;
+  float xk[kE], xv[kE], ak = 0.f, av = 0.f;
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    xk[e] = __bfloat162float(kr[e]);
+    xv[e] = __bfloat162float(vr[e]);
+    ak = fmaxf(ak, fabsf(xk[e]));
+    av = fmaxf(av, fabsf(xv[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, o));
+    av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
+  }
+  const float fk = ak > 0.f ? ak / 448.f : 1.f;  // IEEE division (no fast math)
+  const float fv = av > 0.f ? av / 448.f : 1.f;
+  // byte lane * kE of the row: 16-byte chunk c (128-byte half c / 8, swizzled
+  // position c ^ slot % 8 within it), offset o in the chunk
+  const int c = (lane * kE) >> 4, o = (lane * kE) & 15;
+  const int off = (c >> 3) * tile_bytes + slot * 128 + (((c & 7) ^ (slot & 7)) << 4) + o;
+#pragma unroll
+  for (int k = 0; k < kE / 4; ++k) {
+    uint32_t kw = 0u, vw = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      kw |= (uint32_t)__nv_cvt_float_to_fp8(xk[4 * k + b] / fk, __NV_SATFINITE, __NV_E4M3)
+            << (8 * b);
+      vw |= (uint32_t)__nv_cvt_float_to_fp8(xv[4 * k + b] / fv, __NV_SATFINITE, __NV_E4M3)
+            << (8 * b);
+    }
+    *reinterpret_cast<uint32_t*>(st + off + 4 * k) = kw;
+    *reinterpret_cast<uint32_t*>(st + page_bytes + off + 4 * k) = vw;
+  }
+  if (lane == 0) {
+    scales[slot] = fk;
+    scales[BS + slot] = fv;
+  }
+}
+
+// FP8: the caches hold e4m3 bytes (head_dim 128 or 256) and one float per cache// FP8: the caches hold e4m3 bytes (head_dim 128 or 256) and one float per cache
 // row; the products run on f16 tensor cores (e4m3 -> f16 is exact, q is turned
 // into f16 once per piece), the K row floats scale the scores and the V row
 // floats are folded into the probabilities.
@@ -281,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   constexpr int kQRows = 8 * kNH;                 // query rows one tile holds
   constexpr int kQTileBytes = kQRows * D * 2;     // = lay.q_tile_bytes()
   constexpr int kQ16Stride = L::kQ16Stride;      // FP8: padded f16 query row
-  constexpr int kQSlotBytes =                     // = lay.q_slot_bytes()
-      (kQTileBytes + (FP8 ? kQRows * kQ16Stride : 4 * D + 16) + 127) / 128 * 128;
+  // the fused append's new rows and block id, after the tile (and its f16 copy)
+  constexpr int kAppendOff = kQTileBytes + (FP8 ? kQRows * kQ16Stride : 0);
+  constexpr bool kFp8FusedAppend = FP8 && D == 128;  // FP8 caches: fused append compiled in
+  constexpr int kQSlotBytes = (kAppendOff + 4 * D + 16 + 127) / 128 * 128;  // = lay.q_slot_bytes()
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -676,17 +732,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
                           : static_cast<const void*>(p.q),
                   qr >= 0 ? 16 : 0);
     }
-    if (!FP8 && p.k_new != nullptr) {
+    if (!multi && !XP && (!FP8 || kFp8FusedAppend) && p.k_new != nullptr) {
       const size_t row = ((size_t)s * H_kv + g) * D;
       for (int i = ctid; i < D / 4; i += kConsumerThreads) {  // K then V, 16 bytes each
         const bool is_v = i >= D / 8;
         const int c = is_v ? i - D / 8 : i;
-        cp_async_16(tile + kQTileBytes + (is_v ? 2 * D : 0) + c * 16,
+        cp_async_16(tile + kAppendOff + (is_v ? 2 * D : 0) + c * 16,
                     (is_v ? p.v_new : p.k_new) + row + c * 8, 16);
       }
       if (ctid == kConsumerThreads - 1) {
         const int last_page = sm_prefix[s + 1] - sm_prefix[s] - 1;
-        cp_async_4(tile + kQTileBytes + 4 * D, p.block_tables + (size_t)s * p.maxb + last_page);
+        cp_async_4(tile + kAppendOff + 4 * D, p.block_tables + (size_t)s * p.maxb + last_page);
       }
     }
     cp_async_commit();
@@ -1414,6 +1470,30 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
               }
               __syncwarp();
             }
+            // Fused cache append (FP8 caches): the piece's last page holds the new
+            // token.  Its bf16 K and V rows (prefetched with the query group) are
+            // quantized here as the standalone append does -- float f = max|x| /
+            // 448 (1 for a zero row), byte = e4m3(x / f) rounded to nearest even,
+            // saturating -- patched into the page and its row floats in shared
+            // memory, and stored to the cache after the page is processed.
+            // (head_dim 128 only: at 256 the code would cost the page loop a spill,
+            // and the library runs the append as its own launch instead)
+            const bool patch = kFp8FusedAppend && !multi && p.k_new != nullptr && pg == n - 1;
+            constexpr int kE = D / 32;  // values of a row per lane
+            const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kAppendOff;  // k row, v row, block
+            // byte lane * kE of row `slot`: 16-byte chunk c (128-byte half c / 8,
+            // swizzled position c ^ slot % 8 within it), offset o in the chunk
+            auto patch_off = [&](int slot) {
+              const int c = (lane * kE) >> 4, o = (lane * kE) & 15;
+              return (c >> 3) * kTileBytes + slot * 128 + (((c & 7) ^ (slot & 7)) << 4) + o;
+            };
+            if constexpr (kFp8FusedAppend) {
+              if (patch) {
+                fp8_patch_row<D>(extra, st, kPageBytes, kTileBytes, valid - 1,
+                                 sm_scales + (size_t)own_slot * 2 * BS, BS, lane);
+                __syncwarp();
+              }
+            }
             const uint32_t sc = smem_addr(sm_scales + (size_t)own_slot * 2 * BS);
             const uint32_t q16 = smem_addr(sm_q + qbuf * kQSlotBytes + kQTileBytes);
             const uint32_t k0 = smem_addr(st), v0 = smem_addr(st + kPageBytes);
@@ -1426,8 +1506,33 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
                                    max(0, valid - 16)}};
               process_fp8(std::integral_constant<int, 2>(), t, q16);
             }
-            // the zeroing's generic writes precede the next tensor copy into the slot
-            if (tail) fence_proxy_async_shared();
+            // the zeroing's and the patch's generic writes precede the next tensor
+            // copy into the slot
+            if (tail || patch) fence_proxy_async_shared();
+            if (kFp8FusedAppend && patch) {  // the patched bytes and floats, read back from the slot
+              const int slot = valid - 1;
+              const int new_block = *reinterpret_cast<const int*>(extra + 4 * D);
+              if (p.num_blocks <= 0 || (new_block >= 0 && (long long)new_block < p.num_blocks)) {
+                const size_t row = ((size_t)new_block * H_kv + g) * BS + slot;
+                const int off = patch_off(slot);
+                uint8_t* k8 = reinterpret_cast<uint8_t*>(p.k_cache) + row * D + lane * kE;
+                uint8_t* v8 = reinterpret_cast<uint8_t*>(p.v_cache) + row * D + lane * kE;
+                if constexpr (kE == 4) {
+                  *reinterpret_cast<uint32_t*>(k8) = *reinterpret_cast<const uint32_t*>(st + off);
+                  *reinterpret_cast<uint32_t*>(v8) =
+                      *reinterpret_cast<const uint32_t*>(st + kPageBytes + off);
+                } else {
+                  *reinterpret_cast<uint2*>(k8) = *reinterpret_cast<const uint2*>(st + off);
+                  *reinterpret_cast<uint2*>(v8) =
+                      *reinterpret_cast<const uint2*>(st + kPageBytes + off);
+                }
+                if (lane == 0) {
+                  const_cast<float*>(p.k_scale)[row] = sm_scales[(size_t)own_slot * 2 * BS + slot];
+                  const_cast<float*>(p.v_scale)[row] =
+                      sm_scales[(size_t)own_slot * 2 * BS + BS + slot];
+                }
+              }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[own_slot]);
           }
@@ -1451,7 +1556,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
           } else {
             const int valid = min(BS, len - pg * BS);
             uint8_t* st = smem + own_slot * kStageBytes;
-            const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kQTileBytes;  // k row, v row, block
+            const uint8_t* extra = sm_q + qbuf * kQSlotBytes + kAppendOff;  // k row, v row, block
             if (patch) {
               const int slot = valid - 1;  // the new token, t = L - 1
               if (lane < D / 8) {

@@ -933,22 +933,41 @@ int paged_attn_append_decode_fp8(const void* q, const void* k_new, const void* v
                       num_seqs, H_q, H_kv, head_dim, max_blocks_per_seq, block_size, scale);
   if (rc != PAGED_ATTN_OK || num_seqs == 0) return rc;
   if (!aligned16(k_new) || !aligned16(v_new)) return PAGED_ATTN_ERR_POINTER;
-  int sms = 0;
-  if ((rc = sms_of_device(&sms)) != PAGED_ATTN_OK) return rc;
+  int dev = 0;
+  DeviceInfo di;
+  if ((rc = device_info(&di, &dev)) != PAGED_ATTN_OK) return rc;
+  Plan pl;
+  if ((rc = cached_plan(num_seqs, H_q, H_kv, head_dim, block_size, dev, di, &pl, true)) !=
+      PAGED_ATTN_OK)
+    return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
-                                 H_kv, head_dim, max_blocks_per_seq, block_size);
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  cudaError_t e = launch_append_fp8(a, sms, st);
-  if (e != cudaSuccess) return cuda_fail(e);
   Operands o = operands(q, k_cache, v_cache, out, block_tables, seq_lens, num_seqs, H_q, H_kv,
                         max_blocks_per_seq, scale);
   o.k_scale = k_scale;
   o.v_scale = v_scale;
-  o.early = false;  // the decode reads the rows just appended
   apply_checks(&o);
-  return plan_and_run(o, head_dim, block_size, true, false, 0, 0, st);
+  if ((rc = owned_workspace(pl.ws_bytes, st, &o.ws)) != PAGED_ATTN_OK) return rc;
+  // As for bf16 caches: fused (each piece's last page quantized and patched in
+  // shared memory, then stored) unless CTAs average kAppendApartPieces or more
+  // pieces, when the append runs as its own launch and the decode after it is
+  // a plain launch.
+  // The fused form is compiled for head_dim 128 only (at 256 its code would cost
+  // the page loop a register spill).
+  if (head_dim != 128 ||
+      (long long)num_seqs * H_kv >= (long long)kAppendApartPieces * pl.grid) {
+    AppendParams a = append_params(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                   num_seqs, H_kv, head_dim, max_blocks_per_seq, block_size);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = launch_append_fp8(a, di.sms, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    o.early = false;  // the decode reads the rows just appended
+    return run(pl, o, st);
+  }
+  o.early = early_requested();
+  o.k_new = k_new;
+  o.v_new = v_new;
+  return run(pl, o, st);
 }
 
 size_t paged_attn_workspace_bytes(int num_seqs, int H_q, int H_kv, int head_dim,

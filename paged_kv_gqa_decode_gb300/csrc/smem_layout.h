@@ -52,9 +52,11 @@ struct SmemLayout {
   // one query tile: the group's rows padded to 8 (G <= 8) or 16 heads
   PAGEDATTN_HD int q_rows() const { return G > 8 ? 16 : 8; }
   PAGEDATTN_HD int q_tile_bytes() const { return q_rows() * D * 2; }
-  // one query slot: the bf16 tile, then (fused cache append) the piece's new K
-  // row, new V row and the block id of its last page, or (FP8) the tile as f16
-  PAGEDATTN_HD int q_extra_bytes() const { return FP8 ? q_rows() * kQ16Stride : 4 * D + 16; }
+  // one query slot: the bf16 tile, then (FP8) the tile as f16, then (fused cache
+  // append) the piece's new K row, new V row (bf16) and the block id of its last
+  // page
+  PAGEDATTN_HD int q_f16_bytes() const { return FP8 ? q_rows() * kQ16Stride : 0; }
+  PAGEDATTN_HD int q_extra_bytes() const { return q_f16_bytes() + 4 * D + 16; }
   PAGEDATTN_HD int q_slot_bytes() const {
     return align_up(q_tile_bytes() + q_extra_bytes(), 128);
   }

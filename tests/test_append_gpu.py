@@ -286,3 +286,61 @@ def test_fp8_append_decode_matches_oracle(name):
         pa.paged_attn_set_launch_flags(0)
     assert np.array_equal(f.k8.cpu().numpy(), exp.k8)
     assert_parity(out, oracle.decode_fp8(exp), name)
+
+
+@pytest.mark.parametrize("name", ["edges", "llama8b"])
+def test_fused_fp8_append_decode_equals_append_then_decode(name):
+    """The fused FP8 append (quantized in the decode's shared memory) writes the
+    bytes and floats the standalone append writes and gives the same output bits
+    as the standalone append followed by the decode."""
+    sp = EDGE if name == "edges" else workloads.spec(name)
+    res = []
+    for fused in (True, False):
+        w = workloads.make(sp, seed=42, device="cuda", poison="nan")
+        f = workloads.to_fp8(w)
+        k_new, v_new = new_rows(w, 43)
+        if fused:
+            out = pa.paged_attn_append_decode_fp8(f.q, k_new, v_new, f.k8, f.v8, f.k_scale,
+                                                  f.v_scale, f.block_tables, f.seq_lens, f.scale)
+        else:
+            pa.paged_kv_append_fp8(k_new, v_new, f.k8, f.v8, f.k_scale, f.v_scale,
+                                   f.block_tables, f.seq_lens)
+            out = pa.paged_attn_decode_fp8(f.q, f.k8, f.v8, f.k_scale, f.v_scale, f.block_tables,
+                                           f.seq_lens, f.scale)
+        torch.cuda.synchronize()
+        res.append((out, f.k8, f.v8, f.k_scale.view(torch.int32), f.v_scale.view(torch.int32)))
+    for a, b in zip(*res):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_fused_fp8_append_decode_with_early_prologue_back_to_back():
+    """Two fused FP8 append-decode steps under the early prologue, each after a
+    kernel that writes q, against the oracle (the fused branch: LLaMA shape)."""
+    w = workloads.make("llama8b", seed=44, device="cuda", poison="nan")
+    f = workloads.to_fp8(w)
+    host = oracle.Fp8Inputs(f.q.cpu(), f.k8.cpu(), f.v8.cpu(), f.k_scale.cpu(),
+                            f.v_scale.cpu(), f.block_tables.cpu(), f.seq_lens.cpu(), f.scale)
+    q0 = f.q.clone()
+    k1, v1 = new_rows(w, 45)
+    k2, v2 = new_rows(w, 46)
+    pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE)
+    try:
+        w.q.copy_(q0 * 2)
+        o1 = pa.paged_attn_append_decode_fp8(w.q, k1, v1, f.k8, f.v8, f.k_scale, f.v_scale,
+                                             f.block_tables, f.seq_lens, f.scale).clone()
+        w.q.copy_(q0)
+        o2 = pa.paged_attn_append_decode_fp8(w.q, k2, v2, f.k8, f.v8, f.k_scale, f.v_scale,
+                                             f.block_tables, f.seq_lens, f.scale)
+        torch.cuda.synchronize()
+    finally:
+        pa.paged_attn_set_launch_flags(0)
+    step1 = oracle.append_fp8(host, k1.cpu(), v1.cpu())
+    step1.q = oracle.Inputs(q0 * 2, w.k_cache[:1], w.v_cache[:1], w.block_tables, w.seq_lens,
+                            w.scale).q
+    assert_parity(o1, oracle.decode_fp8(step1), "first step")
+    step2 = oracle.append_fp8(step1, k2.cpu(), v2.cpu())
+    step2.q = oracle.Inputs(q0, w.k_cache[:1], w.v_cache[:1], w.block_tables, w.seq_lens,
+                            w.scale).q
+    assert np.array_equal(f.k8.cpu().numpy(), step2.k8)
+    assert np.array_equal(f.v_scale.cpu().numpy().view(np.uint32), step2.vs.view(np.uint32))
+    assert_parity(o2, oracle.decode_fp8(step2), "second step")
