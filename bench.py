@@ -398,7 +398,7 @@ def run_ours(args, world, rank, local):
     early = op == "decode"
     pa.paged_attn_set_launch_flags(pa.FLAG_EARLY_PROLOGUE if early else 0)
 
-    def run_op(q, bt, sl, cache, kn, vn, out=out, st=None):
+    def run_op(q, bt, sl, cache, kn, vn, out=out, st=None, qo=qo):
         st = stream if st is None else st
         kc, vc, ksc, vsc = cache
         if qo is not None:
@@ -570,7 +570,69 @@ def run_ours(args, world, rank, local):
             clock_info = dict(inside, nvidia_smi_whole_run=clock_info)
     per_step = elapsed / steps
 
-    # End to end through the public API: every step copies its inputs from
+    # End to end through the public API with host buffers (the `e2e` figure):
+    # every step's inputs -- q, block table, lengths (and the new K/V rows, the
+    # query offsets) -- sit in pinned host memory of their own, and its output
+    # goes to pinned host memory.  The library's kernels read and write those
+    # buffers directly over the host link (NVLink-C2C on GB300; pinned memory is
+    # addressable from the device), so the transfers happen inside each call and
+    # the decode launches still chain as they do on device buffers.  Groups of
+    # 32 steps are captured once in a CUDA graph and replayed; the timed region
+    # ends when the last output is in host memory.
+    per_graph = 32
+
+    def pinned(t):
+        return None if t is None else t.cpu().pin_memory()
+
+    zbufs = [dict(q=pinned(q_in), bt=pinned(w.block_tables), sl=pinned(w.seq_lens),
+                  kn=pinned(k_new), vn=pinned(v_new), qo=pinned(qo),
+                  out=torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory())
+             for _ in range(per_graph)]
+
+    def zero_copy_group(cs):
+        for i in range(per_graph):
+            b = zbufs[i]
+            run_op(b["q"], b["bt"], b["sl"], caches[i % reps], b["kn"], b["vn"], out=b["out"],
+                   st=cs, qo=b["qo"])
+
+    zero_copy_group(stream)  # warm-up, outside any capture
+    torch.cuda.synchronize()
+    # the host buffers give the device buffers' result, bit for bit
+    check = torch.empty_like(out)
+    run_op(q_in, w.block_tables, w.seq_lens, caches[0], k_new, v_new, out=check)
+    torch.cuda.synchronize()
+    if op == "decode" and not torch.equal(check.cpu().view(torch.int16),
+                                          zbufs[0]["out"].view(torch.int16)):
+        raise RuntimeError("zero-copy output differs from the device-buffer output")
+    zgraph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            zero_copy_group(torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        zgraph = g
+    except Exception:  # capture unsupported here: issue the groups directly
+        torch.cuda.synchronize()
+    zgroups = max(3, min(steps, 2000) // per_graph)
+    barrier(world)
+    t = time.perf_counter()
+    for _ in range(zgroups):
+        if zgraph is not None:
+            zgraph.replay()
+        else:
+            zero_copy_group(stream)
+    torch.cuda.synchronize()
+    zc_time = reduce_max((time.perf_counter() - t) / (zgroups * per_graph), world)
+    zb = zbufs[0]
+    zc_h2d = sum(zb[k].numel() * zb[k].element_size() for k in ("q", "bt", "sl", "kn", "vn", "qo")
+                 if zb[k] is not None)
+    zc_d2h = zb["out"].numel() * zb["out"].element_size()
+    zc_mode = ("kernels read each step's pinned host inputs and write its pinned host output "
+               f"(no separate copies); CUDA graph of {per_graph} steps" +
+               ("" if zgraph is not None else ", no graph"))
+
+    # The same with explicit copies (`e2e_copies`): every step copies its inputs from
     # pinned host memory to the device and its result back to pinned host
     # memory.  The copies run on two copy streams with double-buffered device
     # inputs and outputs, so step i + 1's inputs go up and step i - 1's result
@@ -596,7 +658,6 @@ def run_ours(args, world, rank, local):
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer uploaded
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the step using the buffer computed
     ev_out = [torch.cuda.Event() for _ in range(2)]   # its result downloaded
-    per_graph = 32
 
     def e2e_group(cs):
         """per_graph steps issued on compute stream cs, the copy streams forked from
@@ -731,9 +792,13 @@ def run_ours(args, world, rank, local):
                            f"CUDA events around {j} of the {steps} timed launches") +
                           f"; isolated: event pairs around {j} single launches after it",
             },
-            "e2e": {"value": round(world * nbytes["total"] / e2e_time / 1e9, 2), "unit": "GB/s",
-                    "us_per_step": round(e2e_time * 1e6, 2), "mode": e2e_mode,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": round(world * nbytes["total"] / zc_time / 1e9, 2), "unit": "GB/s",
+                    "us_per_step": round(zc_time * 1e6, 2), "mode": zc_mode,
+                    "h2d_bytes_per_step": zc_h2d, "d2h_bytes_per_step": zc_d2h},
+            "e2e_copies": {"value": round(world * nbytes["total"] / e2e_time / 1e9, 2),
+                           "unit": "GB/s", "us_per_step": round(e2e_time * 1e6, 2),
+                           "mode": e2e_mode, "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h},
             "gpu_launches": steps * launches_per_step,
             "clocks": clock_info,
         }

@@ -14,8 +14,15 @@
  *   The caller passes `scale` (the tutorial's launcher recomputed 1/sqrt(head_dim)
  *   and ignored its argument; here the argument is used as given).
  *
- * Tensors (all DEVICE pointers, owned by the caller, densely packed row-major,
- * base addresses 16-byte aligned):
+ * Tensors (DEVICE-ADDRESSABLE pointers, owned by the caller, densely packed
+ * row-major, base addresses 16-byte aligned).  The caches (and their row floats)
+ * must be device memory.  Every other tensor -- q, out, block_tables, seq_lens,
+ * qo_indptr, the new K/V rows of the appends, status words -- may also be
+ * pinned host memory (cudaMallocHost / cudaHostAlloc, which unified addressing
+ * makes directly addressable from the device): the kernels then read and write
+ * it over the host link (NVLink-C2C on GB300) inside the call, with no separate
+ * copy, and the results are the same bits.  The library never dereferences any
+ * of these pointers on the host.
  *   q            [num_seqs, H_q, head_dim]                      bf16   (read)
  *   k_cache      [num_blocks, H_kv, block_size, head_dim]       bf16   (read)
  *   v_cache      [num_blocks, H_kv, block_size, head_dim]       bf16   (read)

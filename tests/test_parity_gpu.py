@@ -368,3 +368,102 @@ def test_unknown_launch_flags_are_rejected():
     lib = pa.load()
     assert lib.paged_attn_set_launch_flags(2) == -10
     assert lib.paged_attn_set_launch_flags(0) == 0
+
+
+_GROWTH = r"""
+import sys, json
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import oracle, workloads
+import paged_kv_gqa_decode_gb300 as pa
+pa.load()
+wide = workloads.custom_spec("g16d256", 4, 32, 2, 256, 16, [2000, 1500, 900, 3000])
+specs = ["tiny", "llama8b", "tiny", wide, "llama8b"]
+ws = [workloads.make(sp, device="cuda", poison="nan") for sp in specs]
+side = torch.cuda.Stream()
+torch.cuda.synchronize()
+outs = []
+with torch.cuda.stream(side):
+    for w in ws:  # the library-owned workspace grows at calls 1 and 3, no host sync
+        outs.append(pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                                         w.scale))
+side.synchronize()
+errs = []
+for w, o in zip(ws, outs):
+    ref = oracle.decode(workloads.host_copy(w))
+    got = o.float().cpu().double().numpy()
+    e = np.abs(got - ref)
+    errs.append([float(e.max()), float(e.mean()), bool(np.isfinite(got).all())])
+print("RESULT " + json.dumps(errs))
+"""
+
+
+def test_owned_workspace_grows_in_stream_order():
+    """In a fresh process the library-owned workspace grows twice inside one
+    stream of back-to-back calls with no host synchronisation: the smaller buffer
+    is released in stream order after the calls that use it, and every call's
+    output still matches the oracle."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _GROWTH.format(root=root)], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    for mx, mean, finite in json.loads(r.stdout.split("RESULT ", 1)[1]):
+        assert finite and mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean)
+
+
+def test_pinned_host_buffers_give_the_same_bits():
+    """q, tables, lengths, query offsets, new rows and outputs in pinned host memory
+    (read and written by the kernels over the host link) give the bits that
+    device buffers give, for every entry point that takes them."""
+    def pin(t):
+        return t.cpu().pin_memory()
+
+    w = workloads.make("llama8b", seed=71, device="cuda", poison="nan")
+    hq, hbt, hsl = pin(w.q), pin(w.block_tables), pin(w.seq_lens)
+    dev = pa.paged_attn_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale)
+    hout = torch.empty(tuple(w.q.shape), dtype=w.q.dtype).pin_memory()
+    pa.paged_attn_decode(hq, w.k_cache, w.v_cache, hbt, hsl, w.scale, out=hout)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu().view(torch.int16), hout.view(torch.int16))
+    # FP8 and x-packed caches
+    f = workloads.to_fp8(w)
+    dev8 = pa.paged_attn_decode_fp8(w.q, f.k8, f.v8, f.k_scale, f.v_scale, w.block_tables,
+                                    w.seq_lens, w.scale)
+    h8 = torch.empty_like(hout).pin_memory()
+    pa.paged_attn_decode_fp8(hq, f.k8, f.v8, f.k_scale, f.v_scale, hbt, hsl, w.scale, out=h8)
+    x = workloads.to_xpacked(w)
+    devx = pa.paged_attn_decode_xpacked(w.q, x.kx, x.vt, w.block_tables, w.seq_lens, w.scale)
+    hx = torch.empty_like(hout).pin_memory()
+    pa.paged_attn_decode_xpacked(hq, x.kx, x.vt, hbt, hsl, w.scale, out=hx)
+    # multi-token, query offsets on the host too
+    qlens = [3] * len(w.lens_list)
+    qo = torch.tensor(np.concatenate([[0], np.cumsum(qlens)]), dtype=torch.int32)
+    qm = torch.randn(int(qo[-1]), 32, 128, generator=torch.Generator().manual_seed(72)).to(
+        torch.bfloat16)
+    devm = pa.paged_attn_decode_multi(qm.cuda(), w.k_cache, w.v_cache, qo.cuda(), w.block_tables,
+                                      w.seq_lens, w.scale, 3)
+    hm = torch.empty(tuple(qm.shape), dtype=qm.dtype).pin_memory()
+    pa.paged_attn_decode_multi(qm.pin_memory(), w.k_cache, w.v_cache, qo.pin_memory(), hbt, hsl,
+                               w.scale, 3, out=hm)
+    torch.cuda.synchronize()
+    assert torch.equal(dev8.cpu().view(torch.int16), h8.view(torch.int16))
+    assert torch.equal(devx.cpu().view(torch.int16), hx.view(torch.int16))
+    assert torch.equal(devm.cpu().view(torch.int16), hm.view(torch.int16))
+    # append + decode with the new rows on the host: same rows in the cache, same output
+    g = torch.Generator().manual_seed(73)
+    kn = torch.randn(32, 8, 128, generator=g).to(torch.bfloat16)
+    vn = torch.randn(32, 8, 128, generator=g).to(torch.bfloat16)
+    w2 = workloads.make("llama8b", seed=71, device="cuda", poison="nan")
+    dev_a = pa.paged_attn_append_decode(w.q, kn.cuda(), vn.cuda(), w.k_cache, w.v_cache,
+                                        w.block_tables, w.seq_lens, w.scale)
+    h_a = torch.empty_like(hout).pin_memory()
+    pa.paged_attn_append_decode(hq, kn.pin_memory(), vn.pin_memory(), w2.k_cache, w2.v_cache,
+                                hbt, hsl, w.scale, out=h_a)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_a.cpu().view(torch.int16), h_a.view(torch.int16))
+    assert torch.equal(w.k_cache.view(torch.int16), w2.k_cache.view(torch.int16))
