@@ -202,7 +202,10 @@ PAGED_ATTN_API int paged_attn_set_checks(long long num_blocks, int32_t* d_status
  * head_dim must be 128 or 256 (PAGED_ATTN_ERR_HEAD_DIM otherwise).  The
  * products run on f16 tensor cores: q is rounded to f16 (exact for bf16 values
  * of magnitude 2^-14 .. 65504), the probabilities times the V row factors are
- * rounded to f16; accumulation is fp32.  Workspace, allocation and errors as
+ * rounded to f16; accumulation is fp32.  The probabilities are taken against a
+ * running maximum that may trail the true one by up to a factor of 16 (so each
+ * is at most 16): V row factors below 4094 (rows of magnitude below about
+ * 1.8e6) keep the f16 products finite.  Workspace, allocation and errors as
  * paged_attn_decode; rows past a sequence's length may hold anything (NaN
  * bytes and factors included).
  */

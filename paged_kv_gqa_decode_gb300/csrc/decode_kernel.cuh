@@ -103,6 +103,15 @@ constexpr int kStatusConfig = 8;
 #endif
 constexpr uint32_t kPublishPolls = PAGED_ATTN_PUBLISH_POLLS;
 
+// Lazy rescaling of the online softmax (log2 domain): a warp's running max
+// is raised only when some score of a page exceeds it by more than this, so
+// most pages skip the cross-lane max and the rescale of the accumulators.
+// Weights are then up to 2^4 instead of 1; the result is the same softmax
+// (every state is taken against its own max, and merges rescale by those).
+// For FP8 caches the f16 weight times the V row float stays finite while
+// that float is below 65504 / 16 = 4094.
+constexpr float kLazyMaxLog2 = 4.f;
+
 struct DecodeParams {
   const __nv_bfloat16* q;       // [num_seqs, H_q, D]
   __nv_bfloat16* out;           // [num_seqs, H_q, D]
@@ -871,23 +880,40 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         }
     float m_sub[kNH][2];
     float alpha[kNH][2];
-    bool changed = false;
+    // The running max moves only when a score of the page passes it by more
+    // than kLazyMaxLog2; otherwise the weights are taken against the old max
+    // (at most 2^kLazyMaxLog2) and nothing is rescaled.
+    bool grow = false;
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = mx[nh][e];
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        const float m_new = fmaxf(m_run[nh][e], v);
-        // a column that has seen no token yet (all masked) keeps -inf; subtract 0
-        // then, so its weights are exp2(-inf) = 0 instead of NaN
-        m_sub[nh][e] = MULTI && m_new == -INFINITY ? 0.f : m_new;
-        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_sub[nh][e]);
-        changed |= m_new != m_run[nh][e];
-        m_run[nh][e] = m_new;
-      }
+      for (int e = 0; e < 2; ++e) grow |= mx[nh][e] > m_run[nh][e] + kLazyMaxLog2;
+    const bool changed = __any_sync(0xffffffffu, grow);
+    if (changed) {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = mx[nh][e];
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          const float m_new = fmaxf(m_run[nh][e], v);
+          // a column that has seen no token yet (all masked) keeps -inf; subtract 0
+          // then, so its weights are exp2(-inf) = 0 instead of NaN
+          m_sub[nh][e] = MULTI && m_new == -INFINITY ? 0.f : m_new;
+          alpha[nh][e] = fast_exp2(m_run[nh][e] - m_sub[nh][e]);
+          m_run[nh][e] = m_new;
+        }
+    } else {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          m_sub[nh][e] = MULTI && m_run[nh][e] == -INFINITY ? 0.f : m_run[nh][e];
+          alpha[nh][e] = 1.f;
+        }
+    }
     uint32_t pb0[kTG][kNH], pb1[kTG][kNH];  // B operand P^T (tokens 0-7 / 8-15 of a group)
     float psum[kNH][2];
 #pragma unroll
@@ -911,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
       for (int e = 0; e < 2; ++e) l_run[nh][e] = l_run[nh][e] * alpha[nh][e] + psum[nh][e];
-    if (__any_sync(0xffffffffu, changed)) {
+    if (changed) {
 #pragma unroll
       for (int dt = 0; dt < kDT; ++dt)
 #pragma unroll
@@ -1042,20 +1068,31 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
         }
     }
     float alpha[kNH][2];
-    bool changed = false;
+    bool grow = false;  // as in process_page: the max moves only past kLazyMaxLog2
 #pragma unroll
     for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = mx[nh][e];
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        const float m_new = fmaxf(m_run[nh][e], v);
-        alpha[nh][e] = fast_exp2(m_run[nh][e] - m_new);
-        changed |= m_new != m_run[nh][e];
-        m_run[nh][e] = m_new;
-      }
+      for (int e = 0; e < 2; ++e) grow |= mx[nh][e] > m_run[nh][e] + kLazyMaxLog2;
+    const bool changed = __any_sync(0xffffffffu, grow);
+    if (changed) {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = mx[nh][e];
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          const float m_new = fmaxf(m_run[nh][e], v);
+          alpha[nh][e] = fast_exp2(m_run[nh][e] - m_new);
+          m_run[nh][e] = m_new;
+        }
+    } else {
+#pragma unroll
+      for (int nh = 0; nh < kNH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) alpha[nh][e] = 1.f;
+    }
     uint32_t pb0[NT][kNH], pb1[NT][kNH];
     float psum[kNH][2];
 #pragma unroll
@@ -1082,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
     for (int nh = 0; nh < kNH; ++nh)
 #pragma unroll
       for (int e = 0; e < 2; ++e) l_run[nh][e] = l_run[nh][e] * alpha[nh][e] + psum[nh][e];
-    if (__any_sync(0xffffffffu, changed)) {
+    if (changed) {
 #pragma unroll
       for (int dt = 0; dt < kDT; ++dt)
 #pragma unroll
