@@ -7,11 +7,13 @@
 //  * Work split (section 6 of the BI-V100 design splits each sequence into
 //    fixed 512-token partitions; here the split is re-derived for ragged
 //    batches): the units of work are pages (s, g, p) -- one physical block of
-//    one KV head.  Flattened in (s, g, p) order they are cut into C equal
+//    one KV head.  Flattened in (s, g, p) order they are cut into C
 //    contiguous ranges, one per persistent CTA (two CTAs per SM, C reduced so
-//    each CTA gets at least kMinPagesPerCta pages).  Every CTA streams the same
-//    number of bytes whatever the length mix, and a range crossing (s, g)
-//    boundaries simply produces one partial softmax state per piece.
+//    each CTA gets at least kMinPagesPerCta pages), of equal weight: a page
+//    weighs one and each (s, g) piece adds a fixed weight for its end phase
+//    (first_unit).  CTAs stream about the same number of bytes whatever the
+//    length mix, and a range crossing (s, g) boundaries simply produces one
+//    partial softmax state per piece.
 //
 //  * Data movement: a producer warp walks the range, reads the block table
 //    and issues TMA tiled loads (cp.async.bulk.tensor.4d) into a ring of
@@ -26,7 +28,8 @@
 //    S^T = K Q^T (K read with ldmatrix from the swizzled tile, Q^T with
 //    ldmatrix from the piece's query tile in shared memory), online softmax
 //    in fp32 on the accumulator fragments (BI-V100 design, section 2, Level
-//    1: running max, exp-sum and weighted V), P^T turned into the B operand
+//    1: running max, exp-sum and weighted V; the max is raised only when a
+//    page passes it by kLazyMaxLog2), P^T turned into the B operand
 //    with movmatrix, then O^T += V^T P^T (V read with ldmatrix.trans).  Every
 //    K/V byte leaves HBM once and feeds all G heads of its group.  The FP8,
 //    x-packed and multi-token variants change the operands' loads, the

@@ -97,10 +97,6 @@ int device_info(DeviceInfo* out, int* dev_out = nullptr) {
     *out = tl_info[dev] = g_info[dev];
     return PAGED_ATTN_OK;
   }
-  if (g_info[dev].sms > 0) {
-    *out = g_info[dev];
-    return PAGED_ATTN_OK;
-  }
   DeviceInfo di;
   if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return cuda_fail(e);
