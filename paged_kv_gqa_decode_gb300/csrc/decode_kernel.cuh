@@ -66,10 +66,18 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 // hold only one ring slot per consumer warp, which then idles while its next
 // page loads; one CTA with two slots a warp and the registers of a whole SM
 // streams faster (Qwen-shaped 100K decode 246 -> 237 us, GQA-8 batch 306 -> 303
-// us).  FP8 stages are half as large and its consumers need the warps.
+// us).  FP8 stages are half as large and its consumers need the warps: at
+// head_dim 128 with 16-token pages and up to 8 query rows, three CTAs per SM
+// (15 warps, 128 registers a thread, no spills; 12-stage rings) decode the
+// LLaMA-shaped batch in 31.0 us against 34.2 with two, the ragged 256-sequence
+// batch in 320 against 378 us.  (Four CTAs spill and are slower; with
+// 32-token pages three are slower, 163 -> 202 us on the GQA-8 batch.)
 __host__ __device__ constexpr int ctas_per_sm(int D, bool g16, int BS = 16, bool fp8 = false) {
-  return (D >= 256 && g16) || (!fp8 && D * BS * 2 * 2 >= (16 << 10)) ? 1 : 2;
+  return (D >= 256 && g16) || (!fp8 && D * BS * 2 * 2 >= (16 << 10)) ? 1
+         : fp8 && D == 128 && BS == 16 && !g16                        ? 3
+                                                                      : 2;
 }
+constexpr int kMaxCtasPerSm = 3;  // the largest ctas_per_sm
 constexpr int kMinPagesPerCta = 8;
 // Fixed cost of one (sequence, KV head) piece in pages, for the work split.
 #ifndef PAGED_ATTN_PIECE_WEIGHT_BF16

@@ -34,6 +34,7 @@ constexpr int kAppendApartPieces = 4;  // (s, g) pieces per CTA from which the a
 constexpr int kMaxMultiRows = 256;      // multi-token decode: max q_len * G (16 pieces of 16 rows)
 constexpr long long kRingBytesPerSm = 128 << 10;            // K/V rings of one SM, few pieces per CTA
 constexpr long long kRingBytesPerSmManyPieces = 160 << 10;  // ... two or more pieces per CTA
+constexpr long long kRingBytesPerSmThreeCtas = 150 << 10;   // three FP8 CTAs: 12 stages each
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -199,9 +200,14 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
       // CTAs per SM: 8 stages 51.4 us, 10 52.2, 12 53.3); CTAs that cross many
       // (s, g) pieces gain from a deeper ring that absorbs the stall at each
       // piece end (ragged 256-sequence batch: 8 stages 617 us, 10 608).
+      // Three FP8 CTAs per SM: 12 stages each (8 measured slower on the
+      // LLaMA-shaped batch, 32.7 against 31.0 us; 16 do not fit).
       const long long pieces = (long long)chunk * H_kv * (pl->qchunks > 0 ? pl->qchunks : 1);
       const long long ring_cap =
-          (pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces : kRingBytesPerSm) / occ;
+          (occ >= 3                           ? kRingBytesPerSmThreeCtas
+           : pieces >= 2LL * di.sms * occ ? kRingBytesPerSmManyPieces
+                                          : kRingBytesPerSm) /
+          occ;
       if (plan_smem_any(D, BS, fp8, pl->rows, chunk, budget, ring_cap, pl->qchunks,
                         &pl->stages, &pl->smem) &&
           (pl->stages >= 4 || chunk <= 64)) {
@@ -216,12 +222,13 @@ int make_plan(int num_seqs, int H_q, int H_kv, int D, int BS, const DeviceInfo& 
   if (!ok) return PAGED_ATTN_ERR_SIZES;
   pl->chunk = chunk;
   // [0, 256): status word; then one combine counter per CTA of the largest grid
-  // any launch on this device uses (two CTAs per SM); then the partial states.
+  // any launch on this device uses (kMaxCtasPerSm CTAs per SM); then the
+  // partial states.
   // The counter region depends on the device only (not on this launch's grid,
   // which is one CTA per SM for some shapes), so a workspace reused by calls of
   // any size always finds it zero: partials never land on it.
   pl->off_counters = kWsAlign;
-  pl->off_partials = pl->off_counters + round_up((size_t)di.sms * 2 * 4, kWsAlign);
+  pl->off_partials = pl->off_counters + round_up((size_t)di.sms * kMaxCtasPerSm * 4, kWsAlign);
   pl->ws_bytes = pl->off_partials +
                  round_up((size_t)pl->grid * 2 * pl->rows * (size_t)(D + 4) * 4, kWsAlign);
   return PAGED_ATTN_OK;

@@ -302,19 +302,34 @@ def test_one_workspace_serves_calls_of_different_sizes():
     del ws_list
 
 
-def test_workspace_reuse_across_grids_of_one_and_two_ctas_per_sm():
-    """head_dim 256 with G = 16 runs one CTA per SM, the others two: partial states
-    written by the smaller grid must never land where the larger grid's combine
-    counters live (a stale counter corrupts the next call's merge)."""
-    wide = workloads.custom_spec("g16d256", 4, 32, 2, 256, 16, [20000, 15000, 9000, 30000])
-    specs = [wide, "llama8b", wide, "gqa8"]
-    ws_list = [workloads.make(sp, device="cuda", poison="nan") for sp in specs]
-    refs = [reference(w) for w in ws_list]
+def test_workspace_reuse_across_grids_of_one_two_and_three_ctas_per_sm():
+    """head_dim 256 with G = 16 runs one CTA per SM, FP8 caches of head_dim 128
+    with 16-token pages three, the others two: partial states written by a
+    smaller grid must never land where a larger grid's combine counters live (a
+    stale counter corrupts the next call's merge)."""
+    wide = workloads.make(workloads.custom_spec("g16d256", 4, 32, 2, 256, 16,
+                                                [20000, 15000, 9000, 30000]),
+                          device="cuda", poison="nan")
+    llama = workloads.make("llama8b", device="cuda", poison="nan")
+    gqa8 = workloads.make("gqa8", device="cuda", poison="nan")
+    f = workloads.to_fp8(workloads.make("llama8b", seed=7, device="cuda", poison="nan"))
+    fref = oracle.decode_fp8(oracle.Fp8Inputs(
+        f.q.cpu(), f.k8.cpu(), f.v8.cpu(), f.k_scale.cpu(), f.v_scale.cpu(),
+        f.block_tables.cpu(), f.seq_lens.cpu(), f.scale))
+
+    def fp8():
+        out = pa.paged_attn_decode_fp8(f.q, f.k8, f.v8, f.k_scale, f.v_scale, f.block_tables,
+                                       f.seq_lens, f.scale)
+        torch.cuda.synchronize()
+        return out
+
+    calls = [(lambda: run_gpu(wide), reference(wide)), (lambda: run_gpu(llama), reference(llama)),
+             (fp8, fref), (lambda: run_gpu(wide), None), (lambda: run_gpu(gqa8), reference(gqa8)),
+             (fp8, fref)]
+    calls[3] = (calls[3][0], calls[0][1])
     for rnd in range(2):
-        for i, w in enumerate(ws_list):
-            out = run_gpu(w)
-            assert_parity(out, refs[i], f"call {i} round {rnd}")
-    del ws_list
+        for i, (call, ref) in enumerate(calls):
+            assert_parity(call(), ref, f"call {i} round {rnd}")
 
 
 def _with_flags(flags, fn):
