@@ -86,6 +86,13 @@ constexpr int kMinPagesPerCta = 8;
 #ifndef PAGED_ATTN_PIECE_WEIGHT_FP8
 #define PAGED_ATTN_PIECE_WEIGHT_FP8 4
 #endif
+// FP8 with three CTAs per SM: a CTA streams a third of an SM, so a piece's
+// fixed cost is worth more pages (swept 2-12: 8 best on the LLaMA-shaped batch,
+// 30.4 against 31.0 us at 4; 6 best on the ragged 256-sequence batch, 314
+// against 323 us at 4 and 317 at 8).
+#ifndef PAGED_ATTN_PIECE_WEIGHT_FP8_3CTA
+#define PAGED_ATTN_PIECE_WEIGHT_FP8_3CTA 8
+#endif
 #ifndef PAGED_ATTN_PIECE_WEIGHT_MULTI
 #define PAGED_ATTN_PIECE_WEIGHT_MULTI 10
 #endif
@@ -396,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, G16, BS, KV == kKvFp8
   const int cap = p.maxb * BS;
   // (a multi-token piece of one 8-row tile and one pass costs what a decode
   // piece costs, and splits as the decode does)
-  const int kWgt = FP8 ? PAGED_ATTN_PIECE_WEIGHT_FP8
+  const int kWgt = FP8 ? (ctas_per_sm(D, G16, BS, true) == 3 ? PAGED_ATTN_PIECE_WEIGHT_FP8_3CTA
+                                                             : PAGED_ATTN_PIECE_WEIGHT_FP8)
                  : MULTI && (R > 8 || QC > 1) ? PAGED_ATTN_PIECE_WEIGHT_MULTI
                                               : PAGED_ATTN_PIECE_WEIGHT_BF16;
   // Status bits are written only after the work ahead in the stream has
