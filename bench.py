@@ -60,6 +60,19 @@ def group_bytes(spec, L: int) -> int:
 
 # ------------------------------------------------------------------ environment
 
+def ctas_per_sm(D: int, BS: int, G: int, fp8: bool) -> int:
+    """CTAs per SM of the library's persistent grid for a single-token decode
+    (the kernel's own rule, ctas_per_sm in csrc/decode_kernel.cuh): one when a
+    bf16 stage is 16 KB or more or head_dim 256 has more than 8 query rows,
+    three for FP8 caches of head_dim 128 with 16-token pages and up to 8 query
+    rows, two otherwise."""
+    if (D >= 256 and G > 8) or (not fp8 and D * BS * 4 >= 16384):
+        return 1
+    if fp8 and D == 128 and BS == 16 and G <= 8:
+        return 3
+    return 2
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -438,9 +451,7 @@ def run_ours(args, world, rank, local):
     # 4,096 sequences; the append is a launch of its own for multi-token rows, for
     # --op append_then_decode, for FP8 caches of head_dim 256, and for the fused
     # op when the batch has four or more (sequence, KV head) pieces per CTA of the
-    # persistent grid (two CTAs per SM; one when a bf16 stage is 16 KB or more or
-    # head_dim 256 has more than 8 query rows; three for FP8 caches of head_dim
-    # 128 with 16-token pages and up to 8 query rows).
+    # persistent grid (ctas_per_sm).
     fmt = ("multi-token, %d %s queries per sequence" % (qlen, "causal" if causal else
                                                            "non-causal") if qlen > 1 else
            "FP8 caches" if fp8 else "x-packed caches" if args.kv == "xpacked" else "bf16 caches")
@@ -449,9 +460,7 @@ def run_ours(args, world, rank, local):
                                     "new tokens",
                    "append_then_decode": f"append kernel + paged_decode_kernel ({fmt})"}[op]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    ctas = sms * (1 if (spec.D >= 256 and spec.G > 8) or
-                  (not fp8 and spec.D * spec.block_size * 4 >= 16384) else
-                  3 if fp8 and spec.D == 128 and spec.block_size == 16 and spec.G <= 8 else 2)
+    ctas = sms * ctas_per_sm(spec.D, spec.block_size, spec.G, fp8)
     append_launch = op == "append_then_decode" or (op == "append_decode" and (
         (fp8 and spec.D != 128) or qo is not None or spec.num_seqs * spec.H_kv >= 4 * ctas))
     launches_per_step = -(-len(lens) // 4096) + (1 if append_launch else 0)
